@@ -1,0 +1,453 @@
+"""Benchmark of the paged-KV attention path on GB300.
+
+Default workload: the Llama-3-8B-shaped decode step (bf16, 256 sequences,
+32 query / 8 KV heads, head 128, block 16, seq_len ~ U[512, 4096], pool =
+needed blocks + 10%, tables randomly permuted).  One step = kv_cache_write of
+the 256 new tokens, then paged_attn_decode (split-KV pass + combine).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload decode|prefill|mixed|swa]
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own
+replica of the workload on its own GPU (the path has no exchange step), so
+scaling is weak and `value` counts the tokens of all ranks.
+--impl reference times the fp64 CPU oracle on this host's cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+if HERE not in sys.path:
+    sys.path.insert(0, HERE)
+
+from paged_kv_cache_246_gb300 import workloads as W  # noqa: E402
+
+METRIC = ("decode tokens/s and HBM GB/s (%peak); prefill TFLOP/s (%bf16 peak), 1×GB300")
+CFG_OF = {"decode": 2, "prefill": 3, "mixed": 4, "swa": 5}
+
+
+def peaks():
+    try:
+        with open(os.path.join(HERE, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(
+            d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = list(csv.reader(io.StringIO(out)))
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the workload on the device
+# ---------------------------------------------------------------------------
+class Step:
+    """Device-resident tensors of one workload and the calls of one step."""
+
+    def __init__(self, w: W.Workload, dev, B):
+        self.w, self.B, self.dev = w, B, dev
+        self.slopes = None if w.alibi_slopes is None else w.alibi_slopes.to(dev)
+        self.p = B.make_params(w.num_heads, w.num_kv_heads, w.head_size, w.block_size, w.dtype,
+                               w.scale, self.slopes, w.sliding_window)
+        self.cache = w.kv_cache.to(dev)
+        self.key, self.value = w.key.to(dev), w.value.to(dev)
+        self.slots = w.slot_mapping.to(dev)
+        self.query = w.query.to(dev)
+        self.tables = w.block_tables.to(dev)
+        self.seq_lens = w.seq_lens.to(dev)
+        self.out = torch.empty_like(self.query)
+        P, Tp = w.num_prefill_seqs, w.num_prefill_tokens
+        self.P, self.Tp = P, Tp
+        self.has_prefill = P > 0
+        self.has_decode = w.num_seqs > P
+        if self.has_prefill:
+            q, cuq, cuk, bt, mq, mk = w.prefill_slices()
+            self.cuq, self.cuk, self.mq, self.mk = cuq.to(dev), cuk.to(dev), mq, mk
+        if self.has_decode:
+            self.dmax = int(w.seq_lens[P:].max())
+            n = B.paged_attn_decode_workspace_size(w.num_seqs - P, self.dmax, self.p)
+            self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+            self.multi_split = n > 0
+        self.ev = []
+
+    def launches_per_step(self) -> int:
+        n = 1
+        if self.has_prefill:
+            n += 1
+        if self.has_decode:
+            n += 2 if self.multi_split else 1
+        return n
+
+    def run(self, mark=False):
+        B = self.B
+        B.kv_cache_write(self.key, self.value, self.cache, self.slots, self.p)
+        if mark:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+        if self.has_prefill:
+            B.paged_attn_prefill_varlen(self.out[:self.Tp], self.query[:self.Tp], self.cuq,
+                                        self.cuk, self.mq, self.mk, self.cache,
+                                        self.tables[:self.P], self.p)
+        if mark:
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record()
+        if self.has_decode:
+            B.paged_attn_decode(self.out[self.Tp:], self.query[self.Tp:], self.cache,
+                                self.tables[self.P:], self.seq_lens[self.P:], self.dmax, self.p,
+                                self.ws)
+        if mark:
+            e2 = torch.cuda.Event(enable_timing=True)
+            e2.record()
+            self.ev.append((e0, e1, e2))
+
+
+def algorithmic(w: W.Workload):
+    """Bytes read+written by the decode call and flops of the prefill call."""
+    P = w.num_prefill_seqs
+    el = 2
+    row = w.num_kv_heads * w.head_size
+    dec_bytes = 0
+    for L in w.seq_lens[P:].tolist():
+        keys = min(L, w.sliding_window) if w.sliding_window > 0 else L
+        dec_bytes += keys * row * el * 2          # K and V of every visible token
+    nd = w.num_seqs - P
+    dec_bytes += nd * w.num_heads * w.head_size * el * 2   # query in, output out
+    flops = 0
+    for q, L in zip(w.query_lens[:P].tolist(), w.seq_lens[:P].tolist()):
+        c = L - q
+        pairs = 0
+        for t in range(q):      # keys visible to query row t
+            i = c + t
+            lo = max(0, i - w.sliding_window + 1) if w.sliding_window > 0 else 0
+            pairs += i - lo + 1
+        flops += 4 * w.num_heads * w.head_size * pairs   # q.k and p.V
+    return dec_bytes, flops
+
+
+def step_io_bytes(st: Step):
+    h2d = sum(t.numel() * t.element_size() for t in
+              (st.query, st.key, st.value, st.slots, st.tables, st.seq_lens))
+    if st.has_prefill:
+        h2d += (st.cuq.numel() + st.cuk.numel()) * 4
+    d2h = st.out.numel() * st.out.element_size()
+    return h2d, d2h
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reported baseline; never the target)
+# ---------------------------------------------------------------------------
+def oracle_rate(w: W.Workload, budget_s: float):
+    """Oracle throughput on a bounded sample of the workload: decode
+    sequences (tokens/s) or prefill query rows (TFLOP/s-equivalent rows/s)."""
+    import oracle as O
+    op = O.AttnParams(w.num_heads, w.num_kv_heads, w.head_size, w.block_size, w.scale,
+                      None if w.alibi_slopes is None else w.alibi_slopes.tolist(),
+                      w.sliding_window)
+    ref = w.kv_cache.clone()
+    P = w.num_prefill_seqs
+    t0 = time.perf_counter()
+    O.kv_cache_write(w.key, w.value, ref, w.slot_mapping, op)
+    t_write = time.perf_counter() - t0
+    done, t_attn = 0, 0.0
+    if w.num_seqs > P:
+        q, bt, sl, _ = w.decode_slices()
+        order = torch.randperm(q.shape[0], generator=torch.Generator().manual_seed(0)).tolist()
+        for b in order:
+            t1 = time.perf_counter()
+            O.paged_attn_decode(q, ref, bt, sl, op, seqs=[b])
+            t_attn += time.perf_counter() - t1
+            done += 1
+            if t_attn > budget_s:
+                break
+        per_seq = t_attn / done
+        step_s = t_write + per_seq * q.shape[0]
+        return {"value": q.shape[0] / step_s, "unit": "tokens/s",
+                "sample": f"kv_cache_write of all {w.key.shape[0]} tokens + decode of {done} of "
+                          f"{q.shape[0]} sequences (random order), scaled to the full step",
+                "step_s": step_s}
+    q, cuq, cuk, bt, _, _ = w.prefill_slices()
+    _, flops = algorithmic(w)
+    rows = torch.randperm(q.shape[0], generator=torch.Generator().manual_seed(0)).tolist()
+    t1 = time.perf_counter()
+    n = 0
+    for k in range(0, len(rows), 8):
+        O.paged_attn_prefill_varlen(q, cuq, cuk, ref, bt, op, rows=rows[k:k + 8])
+        n = k + 8
+        if time.perf_counter() - t1 > budget_s:
+            break
+    frac = min(n, len(rows)) / len(rows)
+    step_s = t_write + (time.perf_counter() - t1) / frac
+    return {"value": flops / step_s / 1e12, "unit": "TFLOP/s",
+            "sample": f"kv_cache_write of all tokens + {min(n, len(rows))} of {len(rows)} query "
+                      f"rows (random), scaled to the full step", "step_s": step_s}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = W.make_config(CFG_OF[args.workload])
+    cores = torch.get_num_threads()
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm state
+    vals = []
+    sample = None
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = oracle_rate(w, budget_s=max(2.0, 20.0 / max(1, args.steps)))
+        vals.append(r["value"])
+        sample = r["sample"]
+        unit = r["unit"]
+    elapsed = time.perf_counter() - t0
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "seed": W.SEED_BASE + CFG_OF[args.workload]},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    from paged_kv_cache_246_gb300 import binding as B
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = CFG_OF[args.workload]
+    w = W.make_config(cfg, scale_down=args.scale_down)
+    st = Step(w, dev, B)
+    hbm, bf16_burst, bf16_sust, peak_kind = peaks()
+    dec_bytes, flops = algorithmic(w)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    B.check_device_error("warmup")
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    st.ev.clear()
+    t_start.record(stream)
+    for _ in range(args.steps):
+        st.run(mark=True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+    pre_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in st.ev)
+    dec_ms = statistics.mean(b.elapsed_time(c) for _, b, c in st.ev)
+    B.check_device_error("timed region")
+
+    # ---- end to end through host buffers ----------------------------------
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = [pin(t) for t in (st.query, st.key, st.value, st.slots, st.tables, st.seq_lens)]
+    d_in = [st.query, st.key, st.value, st.slots, st.tables, st.seq_lens]
+    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d, d2h = step_io_bytes(st)
+    for _ in range(max(1, args.warmup)):
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        st.run()
+        h_out.copy_(st.out, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        st.run()
+        h_out.copy_(st.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+
+    # ---- metric ------------------------------------------------------------
+    if st.has_decode:
+        units = (w.num_seqs - w.num_prefill_seqs) * world
+        value = units / (ms_step * 1e-3)
+        unit = "tokens/s"
+        e2e_value = units / (e2e_ms * 1e-3)
+        achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None,
+                "kernel": "paged_attn_decode (split-KV pass + combine)",
+                "peak_kind": peak_kind, "algorithmic_bytes_per_launch": dec_bytes,
+                "avg_launch_ms": dec_ms}
+    else:
+        value = flops * world / (ms_step * 1e-3) / 1e12
+        unit = "TFLOP/s"
+        e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+        achieved = flops / (pre_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_burst, "unit": "TFLOP/s",
+                "frac": achieved / bf16_burst, "traffic": None,
+                "kernel": "paged_attn_prefill_varlen", "peak_kind": peak_kind,
+                "algorithmic_flops_per_launch": flops, "avg_launch_ms": pre_ms,
+                "frac_of_sustained": achieved / bf16_sust}
+    extra = {}
+    if st.has_prefill and st.has_decode:
+        extra = {"prefill_tflops": flops / (pre_ms * 1e-3) / 1e12,
+                 "prefill_frac_of_bf16": flops / (pre_ms * 1e-3) / 1e12 / bf16_burst,
+                 "decode_gbs": dec_bytes / (dec_ms * 1e-3) / 1e9,
+                 "decode_frac_of_hbm": dec_bytes / (dec_ms * 1e-3) / 1e9 / hbm}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = oracle_rate(w, budget_s=args.cpu_budget)
+        cpu = {"value": r["value"], "unit": r["unit"], "cores": torch.get_num_threads(),
+               "kind": "oracle", "sample": r["sample"]}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.dtype == torch.bfloat16 else "fp16", "data": "synthetic",
+                "config": {"workload": f"{w.name}: B={w.num_seqs} H={w.num_heads} "
+                                       f"KVH={w.num_kv_heads} D={w.head_size} bs={w.block_size}",
+                           "seed": W.SEED_BASE + cfg, "num_blocks": w.num_blocks,
+                           "l2": "inputs larger than L2 (KV read per step "
+                                 f"{dec_bytes / 1e9:.2f} GB)" if st.has_decode else
+                                 "no flush; per-step K/V footprint stated in DESIGN.md",
+                           "parallelism": f"replicas x{world}"},
+                "roofline": roof, "clocks": clocks,
+                "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h},
+                "gpu_launches": st.launches_per_step() * args.steps,
+                "cpu_baseline": cpu}
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(CFG_OF), default="decode")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scale-down", type=int, default=1,
+                    help="divide the batch (for small profiling captures only)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

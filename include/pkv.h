@@ -1,0 +1,238 @@
+/*
+ * pkv.h -- C ABI of libpkv.so: attention over a paged KV cache on GB300
+ * (sm_103a).
+ *
+ * The operations are the attention-layer steps of the vLLM / Aphrodite
+ * attention backends described on the pages
+ *   "aphrodite-engine/aphrodite/attention/backends/xformers.py"   (xformers.py)
+ *   "vllm.v1.attention.backends.cpu_attn"                         (cpu_attn)
+ *   "vllm.v1.attention.backends.utils"                            (backends.utils)
+ * Each entry point cites the class or function there that defines it.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Memory: every pointer is a DEVICE pointer (or pinned host memory mapped
+ *   into the device's address space where stated) unless marked "host".  The
+ *   caller owns and allocates all buffers; the library allocates nothing per
+ *   call and keeps no pointer after a call returns.
+ * - Ordering: work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream) and the call returns without synchronising.  No call
+ *   reads device memory on the host.
+ * - Element type: fp16 or bf16 (pkv_attn_params.dtype) for queries, keys,
+ *   values, outputs and the cache; arithmetic is fp32; outputs are rounded to
+ *   nearest even.
+ * - KV cache: kv_cache is [2][num_blocks][block_size * num_kv_heads *
+ *   head_size] elements, contiguous (the shape of xformers.py
+ *   XFormersImpl.forward and cpu_attn TorchSDPABackendImpl.forward).  Half 0
+ *   holds keys, half 1 values.  Inside a block the layout is token-major,
+ *   [block_size][num_kv_heads][head_size], so one slot holds one token's
+ *   key (or value) row exactly as it appears in the `key` input.
+ *   Slot s is token s % block_size of block s / block_size (cpu_attn,
+ *   TorchSDPAMetadata.slot_mapping).
+ * - Errors: argument errors are found on the host before anything is
+ *   enqueued and return PKV_ERR_INVALID / PKV_ERR_UNSUPPORTED with nothing
+ *   done.  A failed launch returns PKV_ERR_CUDA.  Indices that live in
+ *   device memory (slots, block-table entries, lengths, copy pairs) are
+ *   range-checked inside the kernels: a bad one is never dereferenced, the
+ *   affected output is unspecified, and a sticky per-device error word
+ *   records the first such event; read it with pkv_device_error().
+ * - Empty work (num_tokens, num_seqs or num_pairs == 0) returns PKV_OK and
+ *   enqueues nothing (the profiling run with an empty cache in xformers.py
+ *   XFormersImpl.forward and cpu_attn TorchSDPABackendImpl.forward).
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_ABI_VERSION 1
+
+typedef struct CUstream_st *pkv_stream_t; /* == cudaStream_t */
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID = 1,     /* bad argument (null pointer, bad size, ...)   */
+  PKV_ERR_UNSUPPORTED = 2, /* valid but not built (head size, dtype, ...)  */
+  PKV_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed          */
+  PKV_ERR_BOUNDS = 4,      /* pkv_device_error: an index was out of range   */
+  PKV_ERR_TIMEOUT = 5      /* pkv_device_error: a bounded wait gave up      */
+} pkv_status;
+
+typedef enum pkv_dtype { PKV_FP16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/*
+ * Per-layer attention constants: the constructor arguments of
+ * xformers.py XFormersImpl / cpu_attn TorchSDPABackendImpl (num_heads,
+ * head_size, scale, num_kv_heads, alibi_slopes, sliding_window) plus the
+ * cache block size and the element type.
+ *   num_heads % num_kv_heads == 0 (xformers.py XFormersImpl.__init__);
+ *     query head h reads KV head h / (num_heads / num_kv_heads).
+ *   head_size: 64 or 128.  block_size: 8, 16, 32 or 64.
+ *   scale: multiplies q.k before the softmax.
+ *   alibi_slopes: device fp32[num_heads] or NULL; adds slope_h * (j - i) to
+ *     the score of key position j for query position i
+ *     (xformers.py _make_alibi_bias).
+ *   sliding_window: W > 0 keeps keys i - W < j <= i; W <= 0 means none.
+ *     It applies together with ALiBi when both are given.
+ */
+typedef struct pkv_attn_params {
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int32_t head_size;
+  int32_t block_size;
+  int32_t dtype; /* pkv_dtype */
+  float scale;
+  const float *alibi_slopes;
+  int32_t sliding_window;
+} pkv_attn_params;
+
+/*
+ * kv_cache_write -- store each new token's key and value in its cache slot
+ * (reshape_and_cache).  xformers.py XFormersImpl.forward and cpu_attn
+ * TorchSDPABackendImpl.forward call PagedAttention.write_to_paged_cache with
+ * key, value, the split cache and slot_mapping before any attention.
+ *
+ *   key, value    [num_tokens][num_kv_heads * head_size] elements, contiguous
+ *   num_tokens    >= 0
+ *   kv_cache      the cache (layout above), written in place
+ *   num_blocks    blocks per cache half
+ *   slot_mapping  int64[num_tokens]; slot < 0 is a padding token and is
+ *                 skipped; slot >= num_blocks * block_size is recorded as a
+ *                 bounds error and skipped.
+ * Result is a bit-exact row copy.  Two tokens with the same slot race.
+ */
+pkv_status kv_cache_write(const void *key, const void *value,
+                          int64_t num_tokens, void *kv_cache,
+                          int64_t num_blocks, const int64_t *slot_mapping,
+                          const pkv_attn_params *params, pkv_stream_t stream);
+
+/*
+ * paged_attn_decode -- one query token per sequence attending to its cached
+ * K/V, gathered through block_tables (xformers.py XFormersImpl.forward ->
+ * PagedAttention.forward_decode; cpu_attn TorchSDPABackendImpl.forward ->
+ * forward_decode).  The new token was already written, so seq_lens counts it
+ * and the query sits at position seq_len - 1 (xformers.py XFormersMetadata
+ * note on context_len).  Split-KV: a sequence's keys are cut into pieces
+ * processed in parallel whose partial softmax states are merged by a second
+ * kernel (needs `workspace`).
+ *
+ *   out            [num_seqs][num_heads * head_size] elements
+ *   query          [num_seqs][num_heads * head_size] elements
+ *   block_tables   int32[num_seqs][max_blocks_per_seq]: physical block of
+ *                  each logical block (cpu_attn TorchSDPAMetadata
+ *                  .block_tables); entries past a sequence's length unused
+ *   seq_lens       int32[num_seqs]; 0 gives an all-zero output row;
+ *                  must be <= max_seq_len and <= max_blocks_per_seq *
+ *                  block_size (else a bounds error is recorded)
+ *   max_seq_len    host upper bound on seq_lens (sizes the grid)
+ *   workspace      device scratch of at least
+ *                  paged_attn_decode_workspace_size(...) bytes, 256-byte
+ *                  aligned; may be NULL when that size is 0.  Contents on
+ *                  entry do not matter; calls sharing a workspace must not
+ *                  overlap on the GPU.
+ */
+pkv_status paged_attn_decode(void *out, const void *query, int32_t num_seqs,
+                             const void *kv_cache, int64_t num_blocks,
+                             const int32_t *block_tables,
+                             int32_t max_blocks_per_seq,
+                             const int32_t *seq_lens, int32_t max_seq_len,
+                             const pkv_attn_params *params, void *workspace,
+                             size_t workspace_bytes, pkv_stream_t stream);
+
+/* Bytes of workspace paged_attn_decode needs for these sizes (host only,
+ * never fails; 0 when no split is used).  Returns 0 for invalid params. */
+size_t paged_attn_decode_workspace_size(int32_t num_seqs, int32_t max_seq_len,
+                                        const pkv_attn_params *params);
+
+/*
+ * paged_attn_prefill_varlen -- packed prompts or prompt chunks attending
+ * causally to their cached context plus themselves, all K/V read from the
+ * paged cache (the chunk's own K/V are stored by kv_cache_write first).
+ * xformers.py XFormersImpl.forward -> PagedAttention.forward_prefix (and,
+ * with no cached context, _run_memory_efficient_xformers_forward); cpu_attn
+ * flash_attn_varlen_func(out, query, key_cache, value_cache,
+ * query_start_loc, seq_start_loc, max_query_len, max_seq_len, scale,
+ * causal, block_tables, alibi_slopes).
+ *
+ *   out, query     [cu_seqlens_q[num_seqs]][num_heads * head_size] elements
+ *   cu_seqlens_q   int32[num_seqs + 1] (subquery_start_loc / query_start_loc)
+ *   cu_seqlens_k   int32[num_seqs + 1] (seq_start_loc): sequence b has
+ *                  L_b = cu_k[b+1] - cu_k[b] tokens, of which the last
+ *                  q_b = cu_q[b+1] - cu_q[b] are its query rows, at positions
+ *                  L_b - q_b + t (backends.utils CommonAttentionMetadata:
+ *                  computed tokens = seq_lens - query lens).  q_b > L_b is
+ *                  recorded as a bounds error and sequence b is skipped.
+ *   max_query_len  host upper bound on q_b;  max_seq_len: on L_b
+ *   block_tables   int32[num_seqs][max_blocks_per_seq]
+ */
+pkv_status paged_attn_prefill_varlen(
+    void *out, const void *query, int32_t num_seqs,
+    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+    int32_t max_query_len, int32_t max_seq_len, const void *kv_cache,
+    int64_t num_blocks, const int32_t *block_tables,
+    int32_t max_blocks_per_seq, const pkv_attn_params *params,
+    pkv_stream_t stream);
+
+/*
+ * kv_copy_blocks -- for every layer's cache and every pair (s, d), copy block
+ * s to block d in both halves (xformers.py XFormersBackend.copy_blocks,
+ * kv_caches: List[Tensor], src_to_dists: Dict[int, List[int]] flattened to
+ * pairs).
+ *
+ *   kv_caches   host array of num_layers device pointers, each a cache of
+ *               num_blocks blocks (same params); num_layers <= 256
+ *   pairs       device int64[num_pairs][2] (src, dst).  Destinations must be
+ *               unique and never also a source (undefined result otherwise);
+ *               an index outside [0, num_blocks) is a bounds error.
+ */
+pkv_status kv_copy_blocks(void *const *kv_caches, int32_t num_layers,
+                          int64_t num_blocks, const int64_t *pairs,
+                          int64_t num_pairs, const pkv_attn_params *params,
+                          pkv_stream_t stream);
+
+/*
+ * kv_swap_blocks -- dst[:, d] = src[:, s] for every pair, between two caches
+ * (xformers.py XFormersBackend.swap_blocks(src_kv_cache, dst_kv_cache,
+ * src_to_dst)).  A one-way move: swap out, later swap in.
+ *
+ *   src_cache, dst_cache  caches of src_num_blocks / dst_num_blocks blocks;
+ *                         each is device memory or pinned host memory that
+ *                         the device can address (cudaHostAlloc /
+ *                         cudaHostRegister); anything else is
+ *                         PKV_ERR_INVALID
+ *   pairs                 HOST int64[num_pairs][2] (src, dst), checked on
+ *                         the host against both block counts; destinations
+ *                         must be unique.  Read during the call only.
+ * The copy runs as a kernel on `stream` (reading or writing host memory over
+ * the chip-to-host link), so it is stream-ordered like the other calls.
+ */
+pkv_status kv_swap_blocks(const void *src_cache, int64_t src_num_blocks,
+                          void *dst_cache, int64_t dst_num_blocks,
+                          const int64_t *pairs, int64_t num_pairs,
+                          const pkv_attn_params *params, pkv_stream_t stream);
+
+/* Static, never-NULL description of a status code. */
+const char *pkv_status_string(pkv_status status);
+
+/*
+ * pkv_device_error -- synchronise the current device, then read and clear
+ * its sticky device-side error word.  Returns PKV_OK when no kernel recorded
+ * an error since the last read; otherwise PKV_ERR_BOUNDS or PKV_ERR_TIMEOUT,
+ * with *detail (if non-NULL) set to the first offending index.  Diagnostic
+ * call: it blocks the host, so keep it off hot paths.
+ */
+pkv_status pkv_device_error(int64_t *detail);
+
+/* PKV_ABI_VERSION of the built library. */
+int32_t pkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

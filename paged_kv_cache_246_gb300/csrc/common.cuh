@@ -1,0 +1,164 @@
+// Internal helpers shared by the libpkv translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// Sticky device error word.  Each translation unit has its own copy (no
+// relocatable device code); host code reads them through the per-unit
+// read_device_error_* functions declared in internal.h.  Encoding: bits
+// 63..56 = pkv_status, bits 55..0 = the offending index (truncated).
+// The first error wins.
+// ---------------------------------------------------------------------------
+static __device__ unsigned long long g_dev_error = 0ull;
+
+__device__ __forceinline__ void record_error(pkv_status code, int64_t detail) {
+  unsigned long long v = (static_cast<unsigned long long>(code) << 56) |
+                         (static_cast<unsigned long long>(detail) & ((1ull << 56) - 1));
+  atomicCAS(&g_dev_error, 0ull, v);
+}
+
+// Host side: read and clear this unit's word (synchronises the device).
+static inline cudaError_t read_and_clear_unit_error(unsigned long long *out) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(out, g_dev_error, sizeof(*out));
+  if (e != cudaSuccess) return e;
+  const unsigned long long zero = 0ull;
+  return cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero));
+}
+
+// ---------------------------------------------------------------------------
+// Element types.  Storage is raw 16-bit; conversion to fp32 is exact.
+// ---------------------------------------------------------------------------
+struct BF16 {
+  using storage = __nv_bfloat16;
+  using pair = __nv_bfloat162;
+  // exact widening of a packed pair (low half = first element)
+  static __device__ __forceinline__ float2 to_f2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+  static __device__ __forceinline__ uint32_t from_f2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+  static __device__ __forceinline__ float to_f(uint16_t s) {
+    return __uint_as_float(static_cast<uint32_t>(s) << 16);
+  }
+};
+
+struct FP16 {
+  using storage = __half;
+  using pair = __half2;
+  static __device__ __forceinline__ float2 to_f2(uint32_t w) {
+    __half2 h = *reinterpret_cast<__half2 *>(&w);
+    return __half22float2(h);
+  }
+  static __device__ __forceinline__ uint32_t from_f2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+  static __device__ __forceinline__ float to_f(uint16_t s) {
+    return __half2float(__ushort_as_half(s));
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Bounded waits.  Every spin in this library gives up after kWaitLimitNs of
+// %globaltimer time, records PKV_ERR_TIMEOUT and reports failure so the
+// caller can drain and return instead of hanging the GPU.
+// ---------------------------------------------------------------------------
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s; legit waits are us
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false on timeout
+// (PKV_ERR_TIMEOUT recorded with `where` as detail).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int64_t where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      record_error(PKV_ERR_TIMEOUT, where);
+      return false;
+    }
+  }
+}
+
+// 4-D tiled TMA load into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace pkv

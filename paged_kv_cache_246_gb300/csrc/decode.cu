@@ -1,0 +1,512 @@
+// Split-KV paged decode (a query of one token per sequence) and the merge of
+// the split partials.
+//
+// What is computed (xformers.py XFormersImpl.forward -> forward_decode;
+// cpu_attn TorchSDPABackendImpl.forward -> forward_decode): for sequence b
+// of length L (the new token already written), query position i = L - 1,
+// query head h reading KV head h / qpk, keys lo <= j <= i with
+// lo = max(0, i - W + 1) under a window W (else 0):
+//     s_j = scale * q.k_j + slope_h * (j - i),   out = softmax(s) . V.
+//
+// Design (GB300): the kernel is HBM-bound (each cached K/V byte is read once
+// and used for qpk query heads), so the work is organised around the loads.
+//  * CTA = (split, KV head [, head group], sequence); 4 warps.  A split is a
+//    run of `split_blocks` logical blocks; warp w takes blocks w, w+4, ...
+//  * Each warp owns a ring of TMA stages in shared memory: one 4-D tiled TMA
+//    copy brings one block's keys of this KV head (block_size rows x
+//    head_size) and a second its values, both completing on the stage's
+//    mbarrier.  Lane 0 refills a stage as soon as the warp is done with it, so
+//    up to (4 warps x stages x 2 tiles) loads are in flight per CTA.
+//  * q.k: lane (dg = lane % 8, ts = lane / 8) holds 8-element chunks dg
+//    (and dg + 8) of the query heads in fp32 registers and dots them with the
+//    same chunks of token ts, ts + 4, ...; three xor-shuffles finish each dot.
+//  * Online softmax per warp in the log2 domain (q pre-scaled by
+//    scale * log2 e), probabilities staged in shared memory, then p.V with each
+//    lane owning head_size / 32 output dims of every query head.
+//  * Warps merge through shared memory; a single split writes the output,
+//    several splits write (o, m, l) partials that decode_combine_kernel
+//    merges (flash-decoding).
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+constexpr int kDecWarps = 4;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kSub = 16;  // tokens per compute sub-tile
+
+struct DecodeArgs {
+  void *out;
+  const uint16_t *query;
+  const int32_t *block_tables;
+  const int32_t *seq_lens;
+  const float *alibi;
+  float *part_o;   // [B][H][max_splits][D]
+  float *part_ml;  // [B][H][max_splits][2]
+  int64_t num_blocks;
+  int num_seqs, max_blocks_per_seq;
+  int H, QPK, head_groups;  // head_groups = QPK / QT
+  int BS, window, split_blocks, max_splits, stages;
+  float scale_log2;
+};
+
+struct SeqSpan {
+  int L;          // clamped length
+  int lo;         // first visible key position
+  int first_blk;  // logical block of lo
+  int nblk;       // logical blocks lo .. L-1 touch
+  int nsplit;     // splits this sequence uses (<= max_splits)
+};
+
+__device__ __forceinline__ SeqSpan seq_span(const DecodeArgs &a, int b, bool report) {
+  SeqSpan s;
+  int L = __ldg(a.seq_lens + b);
+  const int cap = a.max_blocks_per_seq * a.BS;
+  if (L < 0 || L > cap) {
+    if (report) record_error(PKV_ERR_BOUNDS, b);
+    L = L < 0 ? 0 : cap;
+  }
+  s.L = L;
+  if (L == 0) {
+    s.lo = s.first_blk = s.nblk = s.nsplit = 0;
+    return s;
+  }
+  const int i = L - 1;
+  s.lo = a.window > 0 ? max(0, i - a.window + 1) : 0;
+  s.first_blk = s.lo / a.BS;
+  s.nblk = i / a.BS - s.first_blk + 1;
+  s.nsplit = (s.nblk + a.split_blocks - 1) / a.split_blocks;
+  if (s.nsplit > a.max_splits) {  // seq_len above the host's max_seq_len
+    if (report) record_error(PKV_ERR_BOUNDS, b);
+    s.nsplit = a.max_splits;
+  }
+  return s;
+}
+
+template <class T>
+__device__ __forceinline__ void load_chunk_f32(const uint4 &u, float (&f)[8]) {
+  float2 t;
+  t = T::to_f2(u.x); f[0] = t.x; f[1] = t.y;
+  t = T::to_f2(u.y); f[2] = t.x; f[3] = t.y;
+  t = T::to_f2(u.z); f[4] = t.x; f[5] = t.y;
+  t = T::to_f2(u.w); f[6] = t.x; f[7] = t.y;
+}
+
+// T: element type; D: head size; QT: query heads per CTA (<= 4).
+template <class T, int D, int QT>
+__global__ void __launch_bounds__(kDecThreads)
+decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
+  constexpr int CPL = D / 64;  // 8-element chunks per lane per token (q.k)
+  constexpr int DPL = D / 32;  // output dims per lane (p.V)
+  constexpr int ROWC = D / 8;  // 16-byte chunks per K/V row
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y / a.head_groups;
+  const int hgrp = blockIdx.y % a.head_groups;
+  const int b = blockIdx.z;
+  const int head0 = kvh * a.QPK + hgrp * QT;  // first query head of this CTA
+  const int BS = a.BS;
+  const int nst = a.stages;
+  const int tile_elems = BS * D;
+  const uint32_t tile_bytes = static_cast<uint32_t>(tile_elems) * 2u;
+
+  const SeqSpan sp = seq_span(a, b, split == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+  const int H = a.H;
+  if (sp.L == 0) {  // no keys: the output row is zero
+    if (split == 0) {
+      uint16_t *o = static_cast<uint16_t *>(a.out) + static_cast<int64_t>(b) * H * D + head0 * D;
+      for (int k = threadIdx.x; k < QT * D; k += kDecThreads) o[k] = 0;
+    }
+    return;
+  }
+  const int blk_begin = sp.first_blk + split * a.split_blocks;
+  const int blk_end = min(blk_begin + a.split_blocks, sp.first_blk + sp.nblk);
+  if (split >= sp.nsplit || blk_begin >= blk_end) return;
+  const int nb_split = blk_end - blk_begin;
+
+  // ---- shared memory carve-up -------------------------------------------
+  uint16_t *tiles = reinterpret_cast<uint16_t *>(smem);  // [warp][stage][K,V][tile]
+  float *sP = reinterpret_cast<float *>(smem + static_cast<size_t>(kDecWarps) * nst * 2 * tile_bytes);
+  int32_t *sTable = reinterpret_cast<int32_t *>(sP + kDecWarps * kSub * QT);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(
+      reinterpret_cast<uint8_t *>(sTable) + ((a.split_blocks * 4 + 15) / 16) * 16);
+
+  if (threadIdx.x == 0) prefetch_tensormap(&tmap);
+  // Physical blocks of this split, range-checked once.
+  const int32_t *trow = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+  for (int k = threadIdx.x; k < nb_split; k += kDecThreads) {
+    int32_t pb = __ldg(trow + blk_begin + k);
+    if (pb < 0 || pb >= a.num_blocks) {
+      record_error(PKV_ERR_BOUNDS, static_cast<int64_t>(b) * a.max_blocks_per_seq + blk_begin + k);
+      pb = 0;
+    }
+    sTable[k] = pb;
+  }
+  uint64_t *wbar = bars + warp * nst;
+  if (lane == 0) {
+    for (int st = 0; st < nst; ++st) mbar_init(&wbar[st], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ---- this warp's blocks: k-th is split block warp + 4k -------------------
+  const int my_count = nb_split > warp ? (nb_split - warp + kDecWarps - 1) / kDecWarps : 0;
+  uint16_t *wtiles = tiles + static_cast<size_t>(warp) * nst * 2 * tile_elems;
+  auto issue = [&](int k) {
+    const int st = k % nst;
+    const int pb = sTable[warp + k * kDecWarps];
+    mbar_arrive_expect_tx(&wbar[st], 2u * tile_bytes);
+    uint16_t *kt = wtiles + static_cast<size_t>(st) * 2 * tile_elems;
+    tma_load_4d(kt, &tmap, &wbar[st], 0, kvh, pb * BS, 0);
+    tma_load_4d(kt + tile_elems, &tmap, &wbar[st], 0, kvh, pb * BS, 1);
+  };
+  int issued = 0;
+  if (lane == 0) {
+    for (; issued < min(nst, my_count); ++issued) issue(issued);
+  }
+
+  // ---- query registers (pre-scaled into the log2 domain) ------------------
+  const int dg = lane & 7, ts = lane >> 3;
+  float q[QT][CPL * 8];
+  {
+    const uint4 *qrow = reinterpret_cast<const uint4 *>(a.query + (static_cast<int64_t>(b) * H + head0) * D);
+#pragma unroll
+    for (int h = 0; h < QT; ++h)
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        float f[8];
+        load_chunk_f32<T>(__ldg(qrow + h * ROWC + c * 8 + dg), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[h][c * 8 + e] = f[e] * a.scale_log2;
+      }
+  }
+  float slope[QT];
+#pragma unroll
+  for (int h = 0; h < QT; ++h) slope[h] = a.alibi ? __ldg(a.alibi + head0 + h) * kLog2e : 0.f;
+
+  float m[QT], l[QT], o[QT][DPL];
+#pragma unroll
+  for (int h = 0; h < QT; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[h][e] = 0.f;
+  }
+  float *wP = sP + warp * kSub * QT;
+  const int qpos = sp.L - 1;
+  bool ok = true;
+  int consumed = 0;
+
+  for (int k = 0; k < my_count; ++k) {
+    const int st = k % nst;
+    // every lane observes the phase (acquire); the verdict is warp-uniform
+    const bool got = mbar_wait_bounded(&wbar[st], (k / nst) & 1, b);
+    if (!__all_sync(0xffffffffu, got)) {
+      ok = false;
+      break;
+    }
+    consumed = k + 1;
+    const uint16_t *kt = wtiles + static_cast<size_t>(st) * 2 * tile_elems;
+    const uint16_t *vt = kt + tile_elems;
+    const int blk = blk_begin + warp + k * kDecWarps;  // logical block
+    for (int sub = 0; sub < BS; sub += kSub) {
+      const int j0 = blk * BS + sub;  // position of the sub-tile's token 0
+      const int t_lo = max(sp.lo - j0, 0);
+      const int t_hi = min(sp.L - j0, kSub);
+      if (t_lo >= t_hi) continue;  // warp-uniform
+      // ---- q.k for 16 tokens --------------------------------------------
+      float s[kSub / 4][QT];
+      const uint4 *k4 = reinterpret_cast<const uint4 *>(kt + sub * D);
+#pragma unroll
+      for (int it = 0; it < kSub / 4; ++it) {
+        const int tok = it * 4 + ts;
+#pragma unroll
+        for (int h = 0; h < QT; ++h) s[it][h] = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          float f[8];
+          load_chunk_f32<T>(k4[tok * ROWC + c * 8 + dg], f);
+#pragma unroll
+          for (int h = 0; h < QT; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s[it][h] = fmaf(q[h][c * 8 + e], f[e], s[it][h]);
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < kSub / 4; ++it)
+#pragma unroll
+        for (int h = 0; h < QT; ++h) {
+          float v = s[it][h];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          const int tok = it * 4 + ts;
+          const int j = j0 + tok;
+          s[it][h] = (tok >= t_lo && tok < t_hi) ? v + slope[h] * static_cast<float>(j - qpos)
+                                                 : -INFINITY;
+        }
+      // ---- online softmax ------------------------------------------------
+#pragma unroll
+      for (int h = 0; h < QT; ++h) {
+        float bm = s[0][h];
+#pragma unroll
+        for (int it = 1; it < kSub / 4; ++it) bm = fmaxf(bm, s[it][h]);
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+        const float mn = fmaxf(m[h], bm);
+        const float alpha = fast_exp2(m[h] - mn);
+        float ps = 0.f;
+#pragma unroll
+        for (int it = 0; it < kSub / 4; ++it) {
+          s[it][h] = fast_exp2(s[it][h] - mn);
+          ps += s[it][h];
+        }
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        l[h] = l[h] * alpha + ps;
+        m[h] = mn;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[h][e] *= alpha;
+      }
+      if (dg == 0) {
+#pragma unroll
+        for (int it = 0; it < kSub / 4; ++it)
+#pragma unroll
+          for (int h = 0; h < QT; ++h) wP[(it * 4 + ts) * QT + h] = s[it][h];
+      }
+      __syncwarp();
+      // ---- p.V over the valid tokens ---------------------------------------
+      const uint16_t *vrow = vt + sub * D + lane * DPL;
+      for (int tok = t_lo; tok < t_hi; ++tok) {
+        float vf[DPL];
+        if constexpr (DPL == 4) {
+          const uint2 u = *reinterpret_cast<const uint2 *>(vrow + tok * D);
+          float2 t0 = T::to_f2(u.x), t1 = T::to_f2(u.y);
+          vf[0] = t0.x; vf[1] = t0.y; vf[2] = t1.x; vf[3] = t1.y;
+        } else {
+          const uint32_t u = *reinterpret_cast<const uint32_t *>(vrow + tok * D);
+          float2 t0 = T::to_f2(u);
+          vf[0] = t0.x; vf[1] = t0.y;
+        }
+        float pp[QT];
+        if constexpr (QT == 4) {
+          const float4 p4 = *reinterpret_cast<const float4 *>(wP + tok * 4);
+          pp[0] = p4.x; pp[1] = p4.y; pp[2] = p4.z; pp[3] = p4.w;
+        } else {
+#pragma unroll
+          for (int h = 0; h < QT; ++h) pp[h] = wP[tok * QT + h];
+        }
+#pragma unroll
+        for (int h = 0; h < QT; ++h)
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pp[h], vf[e], o[h][e]);
+      }
+      __syncwarp();
+    }
+    // stage st is free again: refill it
+    if (lane == 0 && issued < my_count) {
+      issue(issued);
+      ++issued;
+    }
+    __syncwarp();
+  }
+  issued = __shfl_sync(0xffffffffu, issued, 0);
+  if (!ok) {  // drain this warp's copies still in flight, bounded
+    for (int k = consumed; k < issued; ++k) mbar_wait_bounded(&wbar[k % nst], (k / nst) & 1, b);
+  }
+
+  // ---- merge the 4 warps' softmax states ----------------------------------
+  __syncthreads();  // every warp's TMA traffic has landed; tiles are reusable
+  float *sM = reinterpret_cast<float *>(smem);          // [warp][QT]
+  float *sL = sM + kDecWarps * QT;                       // [warp][QT]
+  float *sO = sL + kDecWarps * QT;                       // [warp][QT][D]
+#pragma unroll
+  for (int h = 0; h < QT; ++h) {
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) sO[(warp * QT + h) * D + lane * DPL + e] = o[h][e];
+    if (lane == 0) {
+      sM[warp * QT + h] = m[h];
+      sL[warp * QT + h] = l[h];
+    }
+  }
+  __syncthreads();
+  const bool single = sp.nsplit == 1;
+  for (int idx = threadIdx.x; idx < QT * D; idx += kDecThreads) {
+    const int h = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sM[w * QT + h]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) {
+      const float e = fast_exp2(sM[w * QT + h] - M);
+      num = fmaf(e, sO[(w * QT + h) * D + d], num);
+      den = fmaf(e, sL[w * QT + h], den);
+    }
+    const float val = num / den;
+    const int64_t hh = static_cast<int64_t>(b) * H + head0 + h;
+    if (single) {
+      uint16_t *o16 = static_cast<uint16_t *>(a.out);
+      const uint32_t packed = T::from_f2(val, 0.f);
+      o16[hh * D + d] = static_cast<uint16_t>(packed & 0xffffu);
+    } else {
+      const int64_t slot = hh * a.max_splits + split;
+      a.part_o[slot * D + d] = val;
+      if (d == 0) {
+        a.part_ml[slot * 2] = M;
+        a.part_ml[slot * 2 + 1] = den;
+      }
+    }
+  }
+}
+
+// One CTA per (query head, sequence) with more than one split.
+template <class T, int D>
+__global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  const SeqSpan sp = seq_span(a, b, false);
+  if (sp.nsplit <= 1) return;  // the split kernel wrote the output itself
+  const int64_t hh = static_cast<int64_t>(b) * a.H + h;
+  const float *ml = a.part_ml + hh * a.max_splits * 2;
+  float M = -INFINITY;
+  for (int s = 0; s < sp.nsplit; ++s) M = fmaxf(M, ml[2 * s]);
+  const int d = threadIdx.x;
+  const float *po = a.part_o + hh * a.max_splits * D + d;
+  float num = 0.f, den = 0.f;
+  for (int s = 0; s < sp.nsplit; ++s) {
+    const float w = fast_exp2(ml[2 * s] - M) * ml[2 * s + 1];
+    num = fmaf(w, po[static_cast<int64_t>(s) * D], num);
+    den += w;
+  }
+  const float val = num / den;
+  uint16_t *o16 = static_cast<uint16_t *>(a.out);
+  o16[hh * D + d] = static_cast<uint16_t>(T::from_f2(val, 0.f) & 0xffffu);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static int stages_for(int BS) { return BS <= 16 ? 3 : 2; }
+
+static size_t split_smem_bytes(int BS, int D, int QT, int split_blocks) {
+  const size_t tiles = static_cast<size_t>(kDecWarps) * stages_for(BS) * 2 * BS * D * 2;
+  const size_t p = static_cast<size_t>(kDecWarps) * kSub * QT * 4;
+  const size_t table = ((split_blocks * 4 + 15) / 16) * 16;
+  const size_t bars = static_cast<size_t>(kDecWarps) * stages_for(BS) * 8;
+  return tiles + p + table + bars;
+}
+
+DecodePlan plan_decode(int num_seqs, int max_seq_len, const Geometry &g, int sms) {
+  DecodePlan p{};
+  const int BS = g.BS;
+  int eff = max_seq_len;
+  int eff_blocks;
+  if (g.window > 0 && g.window < max_seq_len) {
+    eff = g.window;
+    eff_blocks = (eff + BS - 1) / BS + 1;  // a window start can straddle a block
+  } else {
+    eff_blocks = (eff + BS - 1) / BS;
+  }
+  eff_blocks = std::max(eff_blocks, 1);
+  const int QT = g.QPK >= 4 ? 4 : g.QPK;
+  const int64_t items = static_cast<int64_t>(num_seqs) * g.KVH * (g.QPK / QT);
+  // Splits of ~512 tokens bound the longest CTA (load balance over uneven
+  // lengths); shrink them while the grid would leave SMs idle.
+  int split_blocks = std::max(512 / BS, 4);
+  while (split_blocks > 8 &&
+         items * ((eff_blocks + split_blocks - 1) / split_blocks) < 8LL * sms)
+    split_blocks /= 2;
+  if (eff_blocks <= 2 * split_blocks) split_blocks = eff_blocks;  // short: one split
+  p.split_blocks = split_blocks;
+  p.max_splits = (eff_blocks + split_blocks - 1) / split_blocks;
+  p.workspace_bytes = 0;
+  if (p.max_splits > 1) {
+    const size_t n = static_cast<size_t>(num_seqs) * g.H * p.max_splits;
+    p.workspace_bytes = n * g.D * 4 + n * 2 * 4;
+    p.workspace_bytes = (p.workspace_bytes + 255) / 256 * 256;
+  }
+  return p;
+}
+
+template <class T, int D, int QT>
+static cudaError_t launch_typed(const DecodeArgs &a, const CUtensorMap &tmap, int KVH, int num_seqs,
+                                cudaStream_t stream) {
+  const size_t smem = split_smem_bytes(a.BS, D, QT, a.split_blocks);
+  auto kern = decode_split_kernel<T, D, QT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.max_splits, KVH * a.head_groups, num_seqs);
+  kern<<<grid, kDecThreads, smem, stream>>>(a, tmap);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.max_splits <= 1) return e;
+  decode_combine_kernel<T, D><<<dim3(a.H, num_seqs), D, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(void *out, const void *query, int num_seqs, const void *kv_cache,
+                          const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *seq_lens, int max_seq_len, const Geometry &g,
+                          const DecodePlan &plan, void *workspace, cudaStream_t stream) {
+  (void)max_seq_len;
+  // Tensor map over the whole cache: (D, KVH, NB * BS tokens, 2 halves).
+  CUtensorMap tmap;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.D), static_cast<cuuint64_t>(g.KVH),
+                              static_cast<cuuint64_t>(g.num_blocks * g.BS), 2};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.D) * 2,
+                                 static_cast<cuuint64_t>(g.row_elems) * 2,
+                                 static_cast<cuuint64_t>(g.num_blocks * g.block_elems) * 2};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(g.D), 1, static_cast<cuuint32_t>(g.BS), 1};
+  const CUtensorMapDataType dt =
+      g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (encode_tensor_map(&tmap, dt, 4, const_cast<void *>(kv_cache), dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  DecodeArgs a{};
+  a.out = out;
+  a.query = static_cast<const uint16_t *>(query);
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.alibi = g.alibi;
+  const size_t n = static_cast<size_t>(num_seqs) * g.H * plan.max_splits;
+  a.part_o = static_cast<float *>(workspace);
+  a.part_ml = plan.max_splits > 1 ? a.part_o + n * g.D : nullptr;
+  a.num_blocks = g.num_blocks;
+  a.num_seqs = num_seqs;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.H = g.H;
+  a.QPK = g.QPK;
+  const int QT = g.QPK >= 4 ? 4 : g.QPK;
+  a.head_groups = g.QPK / QT;
+  a.BS = g.BS;
+  a.window = g.window;
+  a.split_blocks = plan.split_blocks;
+  a.max_splits = plan.max_splits;
+  a.stages = stages_for(g.BS);
+  a.scale_log2 = g.scale * kLog2e;
+
+  const bool bf = g.dtype == PKV_BF16;
+#define PKV_DEC(TT, DD, QQ)                                              \
+  if (g.D == DD && QT == QQ)                                             \
+    return launch_typed<TT, DD, QQ>(a, tmap, g.KVH, num_seqs, stream);
+  if (bf) {
+    PKV_DEC(BF16, 128, 4) PKV_DEC(BF16, 128, 2) PKV_DEC(BF16, 128, 1)
+    PKV_DEC(BF16, 64, 4) PKV_DEC(BF16, 64, 2) PKV_DEC(BF16, 64, 1)
+  } else {
+    PKV_DEC(FP16, 128, 4) PKV_DEC(FP16, 128, 2) PKV_DEC(FP16, 128, 1)
+    PKV_DEC(FP16, 64, 4) PKV_DEC(FP16, 64, 2) PKV_DEC(FP16, 64, 1)
+  }
+#undef PKV_DEC
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t read_device_error_decode(unsigned long long *out) {
+  return read_and_clear_unit_error(out);
+}
+
+}  // namespace pkv

@@ -1,0 +1,68 @@
+// Host-side interfaces between the libpkv translation units.  Arguments are
+// validated by the front end (abi.cu) before any of these is called.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+// Validated, derived view of pkv_attn_params.
+struct Geometry {
+  int H, KVH, QPK, D, BS;
+  int dtype;  // pkv_dtype
+  float scale;
+  const float *alibi;
+  int window;            // <= 0: none
+  int64_t num_blocks;    // blocks per cache half
+  int64_t row_elems;     // KVH * D
+  int64_t block_elems;   // BS * KVH * D
+};
+
+// Streams/devices: the SM count and opt-in shared memory of the current device.
+struct DeviceInfo {
+  int device;
+  int sms;
+  int max_smem_optin;
+};
+cudaError_t current_device_info(DeviceInfo *out);
+
+// Driver entry point for cuTensorMapEncodeTiled, resolved once.
+CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank,
+                           void *base, const cuuint64_t *dims, const cuuint64_t *strides_bytes,
+                           const cuuint32_t *box, CUtensorMapSwizzle swizzle);
+
+// kv_ops.cu
+cudaError_t launch_kv_write(const void *key, const void *value, int64_t num_tokens, void *kv_cache,
+                            const int64_t *slot_mapping, const Geometry &g, cudaStream_t stream);
+cudaError_t launch_kv_copy(void *const *caches, int num_layers, const int64_t *pairs,
+                           int64_t num_pairs, const Geometry &g, cudaStream_t stream);
+cudaError_t launch_kv_swap(const void *src, int64_t src_blocks, void *dst, int64_t dst_blocks,
+                           const int64_t *pairs_host, int64_t num_pairs, const Geometry &g,
+                           cudaStream_t stream);
+cudaError_t read_device_error_kv_ops(unsigned long long *out);
+
+// decode.cu
+struct DecodePlan {
+  int split_blocks;  // logical blocks per split
+  int max_splits;    // grid extent over splits (1 = no split, no workspace)
+  size_t workspace_bytes;
+};
+DecodePlan plan_decode(int num_seqs, int max_seq_len, const Geometry &g, int sms);
+cudaError_t launch_decode(void *out, const void *query, int num_seqs, const void *kv_cache,
+                          const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *seq_lens, int max_seq_len, const Geometry &g,
+                          const DecodePlan &plan, void *workspace, cudaStream_t stream);
+cudaError_t read_device_error_decode(unsigned long long *out);
+
+// prefill.cu
+cudaError_t launch_prefill(void *out, const void *query, int num_seqs, const int32_t *cu_q,
+                           const int32_t *cu_k, int max_query_len, int max_seq_len,
+                           const void *kv_cache, const int32_t *block_tables,
+                           int max_blocks_per_seq, const Geometry &g, cudaStream_t stream);
+cudaError_t read_device_error_prefill(unsigned long long *out);
+
+}  // namespace pkv

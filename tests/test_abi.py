@@ -1,0 +1,109 @@
+"""The C ABI on the host: the library loads, exports every declared symbol,
+and rejects bad arguments before touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_246_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        from paged_kv_cache_246_gb300 import build_lib
+        build_lib.build()
+    return B.lib()
+
+
+def test_header_lists_the_calls():
+    names = declared_functions()
+    for must in ("kv_cache_write", "paged_attn_decode", "paged_attn_prefill_varlen",
+                 "kv_copy_blocks", "kv_swap_blocks", "paged_attn_decode_workspace_size"):
+        assert must in names
+    assert set(names) == set(B.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.pkv_abi_version() == 1
+    for s in range(6):
+        assert B.status_string(s)
+    assert B.status_string(99) == "unknown status"
+
+
+def _p(**kw):
+    base = dict(num_heads=32, num_kv_heads=8, head_size=128, block_size=16, dtype=B.PKV_BF16,
+                scale=0.088, alibi_slopes=None, sliding_window=0)
+    base.update(kw)
+    return B.AttnParams(**base)
+
+
+def test_params_validation(lib):
+    nul = ctypes.c_void_p(0)
+    write = lambda p, n=1, nb=4: lib.kv_cache_write(nul, nul, n, nul, nb, nul,
+                                                    ctypes.byref(p) if p else None, nul)
+    assert write(None) == B.PKV_ERR_INVALID
+    assert write(_p(num_heads=6, num_kv_heads=4)) == B.PKV_ERR_INVALID
+    assert write(_p(head_size=96)) == B.PKV_ERR_UNSUPPORTED
+    assert write(_p(block_size=24)) == B.PKV_ERR_UNSUPPORTED
+    assert write(_p(dtype=7)) == B.PKV_ERR_UNSUPPORTED
+    assert write(_p(scale=float("nan"))) == B.PKV_ERR_INVALID
+    assert write(_p(), nb=0) == B.PKV_ERR_INVALID
+    assert write(_p(), n=-1) == B.PKV_ERR_INVALID
+    assert write(_p(), n=1) == B.PKV_ERR_INVALID      # null pointers
+    assert write(_p(), n=0) == B.PKV_OK               # empty: nothing enqueued
+
+
+def test_decode_and_prefill_validation(lib):
+    nul = ctypes.c_void_p(0)
+    p = _p()
+    assert lib.paged_attn_decode(nul, nul, 0, nul, 4, nul, 1, nul, 0, ctypes.byref(p), nul, 0,
+                                 nul) == B.PKV_OK
+    assert lib.paged_attn_decode(nul, nul, 2, nul, 4, nul, 1, nul, 8, ctypes.byref(p), nul, 0,
+                                 nul) == B.PKV_ERR_INVALID
+    assert lib.paged_attn_decode(nul, nul, 70000, nul, 4, nul, 1, nul, 8, ctypes.byref(p), nul,
+                                 0, nul) == B.PKV_ERR_INVALID
+    p3 = _p(num_heads=24, num_kv_heads=8)  # 3 queries per KV head: not built for decode
+    assert lib.paged_attn_decode(nul, nul, 2, nul, 4, nul, 1, nul, 8, ctypes.byref(p3), nul, 0,
+                                 nul) == B.PKV_ERR_UNSUPPORTED
+    assert lib.paged_attn_prefill_varlen(nul, nul, 3, nul, nul, 0, 5, nul, 4, nul, 1,
+                                         ctypes.byref(p), nul) == B.PKV_OK
+    assert lib.paged_attn_prefill_varlen(nul, nul, 3, nul, nul, 5, 5, nul, 4, nul, 1,
+                                         ctypes.byref(p), nul) == B.PKV_ERR_INVALID
+
+
+def test_workspace_size_is_host_only(lib):
+    p = _p()
+    assert B.paged_attn_decode_workspace_size(0, 100, p) == 0
+    assert B.paged_attn_decode_workspace_size(4, 64, p) == 0            # one split
+    n = B.paged_attn_decode_workspace_size(256, 4096, p)
+    assert n > 0 and n % 256 == 0
+
+
+def test_copy_and_swap_validation(lib):
+    nul = ctypes.c_void_p(0)
+    p = _p()
+    assert lib.kv_copy_blocks(None, 1, 8, nul, 0, ctypes.byref(p), nul) == B.PKV_OK
+    assert lib.kv_copy_blocks(None, 300, 8, nul, 1, ctypes.byref(p), nul) == B.PKV_ERR_INVALID
+    pairs = (ctypes.c_int64 * 4)(0, 1, 2, 1)  # destination 1 twice
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.kv_swap_blocks(fake, 8, fake, 8, pairs, 2, ctypes.byref(p),
+                              nul) == B.PKV_ERR_INVALID
+    pairs = (ctypes.c_int64 * 2)(9, 0)        # source out of range
+    assert lib.kv_swap_blocks(fake, 8, fake, 8, pairs, 1, ctypes.byref(p),
+                              nul) == B.PKV_ERR_INVALID

@@ -1,0 +1,269 @@
+"""GPU parity: every call of the C ABI against the fp64 oracle on the same
+seeded inputs.  Cache writes and block moves must be bit-exact; attention
+outputs within max-abs 2e-2 and mean-abs 2e-3 (fp32 accumulation, outputs
+rounded to fp16/bf16).  Sizes span several tiles / splits and ragged tails."""
+import math
+
+import pytest
+import torch
+
+import oracle as O
+from paged_kv_cache_246_gb300 import binding as B
+from paged_kv_cache_246_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from gpu_helpers import (DEV, GpuRun, assert_close, assert_no_device_error,  # noqa: E402
+                             oracle_cache_after_write, oracle_params)
+
+
+def small(seed, *, dtype=torch.bfloat16, H=8, KVH=2, D=128, bs=16, seq_lens, query_lens=None,
+          P=0, alibi=False, window=0, num_blocks=None):
+    g = torch.Generator().manual_seed(seed)
+    if query_lens is None:
+        query_lens = [1] * len(seq_lens)
+    return W.build(name=f"case{seed}", g=g, dtype=dtype, num_heads=H, num_kv_heads=KVH,
+                   head_size=D, block_size=bs, seq_lens=seq_lens, query_lens=query_lens,
+                   num_prefill_seqs=P, alibi=alibi, sliding_window=window, num_blocks=num_blocks)
+
+
+def rand_lens(seed, n, lo, hi):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(lo, hi + 1, (n,), generator=g).tolist()
+
+
+# ---------------------------------------------------------------------------
+# a1: cache write
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_kv_cache_write_bit_exact(cfg):
+    w = W.make_config(cfg, scale_down=1 if cfg == 1 else 16)
+    r = GpuRun(w)
+    r.write()
+    assert_no_device_error("write")
+    ref = oracle_cache_after_write(w)
+    assert torch.equal(r.cache.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def test_kv_cache_write_padding_slots_and_empty():
+    w = small(11, seq_lens=[5, 9, 33], query_lens=[5, 9, 33], P=3)
+    w.slot_mapping[::3] = -1  # padding tokens
+    r = GpuRun(w)
+    r.write()
+    B.kv_cache_write(r.key[:0], r.value[:0], r.cache, r.slots[:0], r.p)  # empty: no-op
+    assert_no_device_error("write padding")
+    ref = oracle_cache_after_write(w)
+    assert torch.equal(r.cache.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def test_kv_cache_write_repeatable():
+    w = W.make_config(2, scale_down=32)
+    outs = []
+    for _ in range(3):
+        r = GpuRun(w)
+        r.write()
+        outs.append(r.cache.cpu())
+    assert all(torch.equal(outs[0].view(torch.int16), o.view(torch.int16)) for o in outs[1:])
+
+
+# ---------------------------------------------------------------------------
+# a2 + a3: decode
+# ---------------------------------------------------------------------------
+
+DECODE_CASES = {
+    "tiny_fp16_cfg1": lambda: W.make_config(1),
+    "qpk4_multi_split": lambda: small(21, H=32, KVH=8, seq_lens=rand_lens(1, 12, 1, 600)),
+    "qpk1": lambda: small(22, H=4, KVH=4, seq_lens=rand_lens(2, 7, 1, 300)),
+    "qpk2_d64": lambda: small(23, H=4, KVH=2, D=64, seq_lens=rand_lens(3, 9, 1, 400)),
+    "qpk8_groups": lambda: small(24, H=16, KVH=2, seq_lens=rand_lens(4, 5, 1, 700)),
+    "fp16_d128": lambda: small(25, dtype=torch.float16, seq_lens=rand_lens(5, 6, 1, 500)),
+    "block32": lambda: small(26, bs=32, seq_lens=rand_lens(6, 6, 1, 900)),
+    "alibi": lambda: small(27, H=8, KVH=2, alibi=True, seq_lens=rand_lens(7, 6, 1, 800)),
+    "window": lambda: small(28, window=100, seq_lens=rand_lens(8, 8, 1, 900)),
+    "window_alibi_bs32": lambda: small(29, bs=32, window=77, alibi=True,
+                                       seq_lens=rand_lens(9, 8, 1, 700)),
+    "one_token_seqs": lambda: small(30, seq_lens=[1, 1, 2, 17]),
+    "long_single": lambda: small(31, H=32, KVH=8, seq_lens=[5000]),
+    "window_ge_len": lambda: small(32, window=4096, seq_lens=rand_lens(10, 4, 1, 300)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(DECODE_CASES))
+def test_decode_parity(case):
+    w = DECODE_CASES[case]()
+    r = GpuRun(w)
+    r.write()
+    out = r.decode()
+    assert_no_device_error(case)
+    ref_cache = oracle_cache_after_write(w)
+    q, bt, sl, _ = w.decode_slices()
+    ref = O.paged_attn_decode(q, ref_cache, bt, sl, oracle_params(w))
+    assert_close(out, ref, case)
+
+
+def test_decode_zero_length_rows_are_zero():
+    w = small(33, seq_lens=[3, 40, 2])
+    r = GpuRun(w)
+    r.write()
+    P = 0
+    sl = w.seq_lens.clone()
+    sl[1] = 0
+    out = torch.full_like(r.query, float("nan"))
+    n = B.paged_attn_decode_workspace_size(3, 40, r.p)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=DEV)
+    B.paged_attn_decode(out, r.query, r.cache, r.tables, sl.to(DEV), 40, r.p, ws)
+    assert_no_device_error("zero rows")
+    assert torch.equal(out[1].cpu(), torch.zeros_like(out[1].cpu()))
+    ref = O.paged_attn_decode(w.query, oracle_cache_after_write(w), w.block_tables, sl,
+                              oracle_params(w))
+    assert_close(out, ref, "zero rows")
+
+
+def test_decode_split_invariance():
+    """A loose max_seq_len changes the split plan, not the result."""
+    w = small(34, H=32, KVH=8, seq_lens=rand_lens(11, 10, 200, 2000))
+    r = GpuRun(w)
+    r.write()
+    a = r.decode()
+    b = r.decode(max_seq_len=8 * int(w.seq_lens.max()))
+    assert_no_device_error("split invariance")
+    err = (a.double() - b.double()).abs().max().item()
+    assert err <= 2e-2
+
+
+# ---------------------------------------------------------------------------
+# a4: varlen / chunked prefill
+# ---------------------------------------------------------------------------
+
+def chunked(seed, ctx, q, **kw):
+    return small(seed, seq_lens=[c + n for c, n in zip(ctx, q)], query_lens=q, P=len(q), **kw)
+
+
+PREFILL_CASES = {
+    "varlen_qpk4": lambda: small(41, H=32, KVH=8, seq_lens=[1, 17, 64, 65, 130, 300],
+                                 query_lens=[1, 17, 64, 65, 130, 300], P=6),
+    "chunked_ctx": lambda: chunked(42, [0, 5, 64, 100, 333], [70, 1, 64, 129, 40]),
+    "chunked_alibi": lambda: chunked(43, [13, 200, 0], [150, 64, 90], alibi=True, H=8, KVH=2),
+    "window": lambda: small(44, window=50, seq_lens=[300, 77], query_lens=[300, 77], P=2),
+    "window_chunked_alibi": lambda: chunked(45, [120, 9], [200, 33], window=64, alibi=True),
+    "fp16_d64": lambda: chunked(46, [0, 31], [100, 70], dtype=torch.float16, D=64, H=4, KVH=2),
+    "block32_qpk1": lambda: chunked(47, [40, 0], [90, 200], bs=32, H=4, KVH=4),
+    "qpk8": lambda: chunked(48, [10, 300], [257, 3], H=16, KVH=2),
+    "single_row_chunks": lambda: chunked(49, [0, 10, 99, 500], [1, 1, 1, 1]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(PREFILL_CASES))
+def test_prefill_parity(case):
+    w = PREFILL_CASES[case]()
+    r = GpuRun(w)
+    r.write()
+    out = r.prefill()
+    assert_no_device_error(case)
+    ref_cache = oracle_cache_after_write(w)
+    q, cuq, cuk, bt, _, _ = w.prefill_slices()
+    ref = O.paged_attn_prefill_varlen(q, cuq, cuk, ref_cache, bt, oracle_params(w))
+    assert_close(out, ref, case)
+
+
+def test_prefill_last_row_equals_decode():
+    """Cross-path: the last prefill row of a sequence equals its decode."""
+    lens = [33, 130, 257]
+    w = small(50, H=32, KVH=8, seq_lens=lens, query_lens=lens, P=3)
+    r = GpuRun(w)
+    r.write()
+    pre = r.prefill()
+    last = torch.tensor([sum(lens[:k + 1]) - 1 for k in range(3)])
+    q = r.query[last.to(DEV)].contiguous()
+    out = torch.empty_like(q)
+    n = B.paged_attn_decode_workspace_size(3, max(lens), r.p)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=DEV)
+    B.paged_attn_decode(out, q, r.cache, r.tables, w.seq_lens.to(DEV), max(lens), r.p, ws)
+    assert_no_device_error("cross path")
+    err = (pre[last.to(DEV)].double() - out.double()).abs().max().item()
+    assert err <= 2e-2
+
+
+# ---------------------------------------------------------------------------
+# a5, a6: block moves
+# ---------------------------------------------------------------------------
+
+def test_copy_blocks_bit_exact_all_layers():
+    g = torch.Generator().manual_seed(60)
+    w = small(60, seq_lens=[64, 100], num_blocks=40)
+    layers = [w.kv_cache.clone() for _ in range(3)]
+    for L in layers:
+        L.view(-1).copy_(torch.randn(L.numel(), generator=g).to(L.dtype))
+    pairs = torch.tensor([[3, 20], [3, 21], [7, 30], [0, 39], [12, 22]], dtype=torch.int64)
+    dev_layers = [L.to(DEV) for L in layers]
+    r = GpuRun(w)
+    B.kv_copy_blocks(dev_layers, pairs.to(DEV), r.p)
+    assert_no_device_error("copy")
+    O.kv_copy_blocks(layers, pairs.tolist())
+    for got, ref in zip(dev_layers, layers):
+        assert torch.equal(got.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def test_swap_round_trip_pinned_host():
+    w = small(61, seq_lens=[300, 200], num_blocks=64)
+    r = GpuRun(w)
+    host = torch.zeros((2, 16, w.kv_cache.shape[2]), dtype=w.dtype).pin_memory()
+    out_pairs = torch.tensor([[5, 0], [17, 3], [40, 15], [63, 7]], dtype=torch.int64)
+    B.kv_swap_blocks(r.cache, host, out_pairs, r.p)
+    torch.cuda.synchronize()
+    ref_host = torch.zeros_like(host)
+    O.kv_swap_blocks(w.kv_cache, ref_host, out_pairs.tolist())
+    assert torch.equal(host.view(torch.int16), ref_host.view(torch.int16))
+    back = torch.zeros_like(r.cache)
+    in_pairs = out_pairs[:, [1, 0]].contiguous()
+    B.kv_swap_blocks(host, back, in_pairs, r.p)
+    assert_no_device_error("swap")
+    for s in out_pairs[:, 0].tolist():
+        assert torch.equal(back[:, s].cpu().view(torch.int16), w.kv_cache[:, s].view(torch.int16))
+
+
+def test_swap_rejects_pageable_host():
+    w = small(62, seq_lens=[20], num_blocks=4)
+    r = GpuRun(w)
+    pageable = torch.zeros((2, 4, w.kv_cache.shape[2]), dtype=w.dtype)
+    with pytest.raises(ValueError):
+        B.kv_swap_blocks(r.cache, pageable, torch.tensor([[0, 0]]), r.p)
+
+
+# ---------------------------------------------------------------------------
+# In-kernel range checks: bad indices are recorded, never dereferenced
+# ---------------------------------------------------------------------------
+
+def test_bad_slot_is_reported_not_written():
+    w = small(70, seq_lens=[8], query_lens=[8], P=1, num_blocks=2)
+    r = GpuRun(w)
+    before = r.cache.clone()
+    bad = r.slots.clone()
+    bad[3] = 2 * 16 + 5  # beyond num_blocks * block_size
+    B.kv_cache_write(r.key, r.value, r.cache, bad, r.p)
+    torch.cuda.synchronize()
+    st, detail = B.device_error()
+    assert st == B.PKV_ERR_BOUNDS and detail == 3
+    assert B.device_error()[0] == B.PKV_OK  # reading cleared it
+    ref = before.cpu().clone()
+    slots = bad.cpu().clone()
+    slots[3] = -1
+    O.kv_cache_write(w.key, w.value, ref, slots, oracle_params(w))
+    assert torch.equal(r.cache.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def test_bad_block_table_entry_is_reported():
+    w = small(71, seq_lens=[40, 40])
+    r = GpuRun(w)
+    r.tables[1, 1] = w.num_blocks + 7
+    r.decode()
+    torch.cuda.synchronize()
+    assert B.device_error()[0] == B.PKV_ERR_BOUNDS
+    w2 = small(72, seq_lens=[40], query_lens=[40], P=1)
+    r2 = GpuRun(w2)
+    r2.tables[0, 2] = -5
+    r2.prefill()
+    torch.cuda.synchronize()
+    assert B.device_error()[0] == B.PKV_ERR_BOUNDS
