@@ -159,7 +159,10 @@ size_t paged_attn_decode_workspace_size(int32_t num_seqs, int32_t max_seq_len,
  * query_start_loc, seq_start_loc, max_query_len, max_seq_len, scale,
  * causal, block_tables, alibi_slopes).
  *
- *   out, query     [cu_seqlens_q[num_seqs]][num_heads * head_size] elements
+ *   out, query     [num_query_tokens][num_heads * head_size] elements
+ *   num_query_tokens  rows of query / out; every cu_seqlens_q entry must lie
+ *                  in [0, num_query_tokens] (else a bounds error is recorded
+ *                  and the sequence skipped)
  *   cu_seqlens_q   int32[num_seqs + 1] (subquery_start_loc / query_start_loc)
  *   cu_seqlens_k   int32[num_seqs + 1] (seq_start_loc): sequence b has
  *                  L_b = cu_k[b+1] - cu_k[b] tokens, of which the last
@@ -171,7 +174,7 @@ size_t paged_attn_decode_workspace_size(int32_t num_seqs, int32_t max_seq_len,
  *   block_tables   int32[num_seqs][max_blocks_per_seq]
  */
 pkv_status paged_attn_prefill_varlen(
-    void *out, const void *query, int32_t num_seqs,
+    void *out, const void *query, int64_t num_query_tokens, int32_t num_seqs,
     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
     int32_t max_query_len, int32_t max_seq_len, const void *kv_cache,
     int64_t num_blocks, const int32_t *block_tables,

@@ -58,8 +58,8 @@ def lib() -> ctypes.CDLL:
             "kv_cache_write": (i32, [vp, vp, i64, vp, i64, vp, P, vp]),
             "paged_attn_decode": (i32, [vp, vp, i32, vp, i64, vp, i32, vp, i32, P, vp, sz, vp]),
             "paged_attn_decode_workspace_size": (sz, [i32, i32, P]),
-            "paged_attn_prefill_varlen": (i32, [vp, vp, i32, vp, vp, i32, i32, vp, i64, vp, i32,
-                                                P, vp]),
+            "paged_attn_prefill_varlen": (i32, [vp, vp, i64, i32, vp, vp, i32, i32, vp, i64, vp,
+                                                i32, P, vp]),
             "kv_copy_blocks": (i32, [vp, i32, i64, vp, i64, P, vp]),
             "kv_swap_blocks": (i32, [vp, i64, vp, i64, vp, i64, P, vp]),
             "pkv_status_string": (ctypes.c_char_p, [i32]),
@@ -186,7 +186,10 @@ def paged_attn_prefill_varlen(out: torch.Tensor, query: torch.Tensor, cu_seqlens
     B = cu_seqlens_q.numel() - 1
     if cu_seqlens_k.numel() != B + 1 or block_tables.shape[0] < B or out.shape != query.shape:
         raise ValueError("cu_seqlens/block_tables/out sizes disagree")
-    _check(lib().paged_attn_prefill_varlen(out.data_ptr(), query.data_ptr(), B,
+    rows = query.shape[0]
+    if query.numel() != rows * params.num_heads * params.head_size:
+        raise ValueError("query must be [num_query_tokens, num_heads * head_size]")
+    _check(lib().paged_attn_prefill_varlen(out.data_ptr(), query.data_ptr(), rows, B,
                                            cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
                                            int(max_query_len), int(max_seq_len),
                                            kv_cache.data_ptr(), nb, block_tables.data_ptr(),

@@ -34,8 +34,8 @@ def nvcc() -> str:
     return found
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, extra: list[str], tag: str) -> str:
+    obj = os.path.join(BUILD, os.path.splitext(src)[0] + tag + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -45,21 +45,24 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile all units (in parallel) and link libpkv.so; returns its path."""
+def build(verbose: bool = False, extra: list[str] | None = None, out: str | None = None) -> str:
+    """Compile all units (in parallel) and link the library (default
+    paged_kv_cache_246_gb300/libpkv.so); returns its path."""
     os.makedirs(BUILD, exist_ok=True)
     extra = list(extra or [])
     if verbose:
         extra += ["-Xptxas", "-v"]
+    target = out or LIB
+    tag = "" if target == LIB else "_" + os.path.splitext(os.path.basename(target))[0]
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, tag), SOURCES))
+    tmp = target + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, target)
+    return target
 
 
 if __name__ == "__main__":

@@ -196,7 +196,8 @@ pkv_status paged_attn_decode(void *out, const void *query, int32_t num_seqs, con
                                  seq_lens, max_seq_len, g, plan, workspace, s));
 }
 
-pkv_status paged_attn_prefill_varlen(void *out, const void *query, int32_t num_seqs,
+pkv_status paged_attn_prefill_varlen(void *out, const void *query, int64_t num_query_tokens,
+                                     int32_t num_seqs,
                                      const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                                      int32_t max_query_len, int32_t max_seq_len,
                                      const void *kv_cache, int64_t num_blocks,
@@ -206,9 +207,9 @@ pkv_status paged_attn_prefill_varlen(void *out, const void *query, int32_t num_s
   pkv_status st = make_geometry(params, num_blocks, &g);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || num_seqs > 65535 || max_query_len < 0 || max_seq_len < 0 ||
-      max_blocks_per_seq <= 0)
+      max_blocks_per_seq <= 0 || num_query_tokens < 0 || num_query_tokens > 0x7fffffffLL)
     return PKV_ERR_INVALID;
-  if (num_seqs == 0 || max_query_len == 0) return PKV_OK;
+  if (num_seqs == 0 || max_query_len == 0 || num_query_tokens == 0) return PKV_OK;
   if (static_cast<int64_t>(max_query_len) > 65535LL * 64) return PKV_ERR_UNSUPPORTED;
   if (!out || !query || !kv_cache || !block_tables || !cu_seqlens_q || !cu_seqlens_k)
     return PKV_ERR_INVALID;
@@ -218,8 +219,9 @@ pkv_status paged_attn_prefill_varlen(void *out, const void *query, int32_t num_s
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = select_device(s);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
-  return from_cuda(launch_prefill(out, query, num_seqs, cu_seqlens_q, cu_seqlens_k, max_query_len,
-                                  max_seq_len, kv_cache, block_tables, max_blocks_per_seq, g, s));
+  return from_cuda(launch_prefill(out, query, num_query_tokens, num_seqs, cu_seqlens_q,
+                                  cu_seqlens_k, max_query_len, max_seq_len, kv_cache,
+                                  block_tables, max_blocks_per_seq, g, s));
 }
 
 pkv_status kv_copy_blocks(void *const *kv_caches, int32_t num_layers, int64_t num_blocks,

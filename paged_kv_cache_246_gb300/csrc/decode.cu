@@ -94,9 +94,43 @@ __device__ __forceinline__ void load_chunk_f32(const uint4 &u, float (&f)[8]) {
   t = T::to_f2(u.w); f[6] = t.x; f[7] = t.y;
 }
 
+// Dots each lane finishes after the recursive halving of 4 * QT partials
+// over 8 lanes, and the head of its f-th one (token is (dg >> 1) * 4 + ts).
+template <int QT> struct NfOf { static constexpr int v = QT >= 2 ? QT / 2 : 1; };
+template <int QT>
+__device__ __forceinline__ int head_of(int dg, int f) {
+  if constexpr (QT == 4) return 2 * (dg & 1) + f;
+  else if constexpr (QT == 2) return dg & 1;
+  else return 0;
+}
+
+// One halving level over lanes xor MASK: N values -> N / 2 (or a plain sum
+// when one value is left).
+template <int N, int MASK>
+__device__ __forceinline__ void halve(float *v, int lane) {
+  if constexpr (N >= 2) {
+    const bool up = (lane & MASK) != 0;
+#pragma unroll
+    for (int k = 0; k < N / 2; ++k) {
+      const float send = up ? v[k] : v[k + N / 2];
+      const float keep = up ? v[k + N / 2] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, MASK);
+    }
+  } else {
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], MASK);
+  }
+}
+
+template <int NV>
+__device__ __forceinline__ void reduce_over_dg(float *v, int lane) {
+  halve<NV, 4>(v, lane);
+  halve<(NV >= 2 ? NV / 2 : 1), 2>(v, lane);
+  halve<(NV >= 4 ? NV / 4 : 1), 1>(v, lane);
+}
+
 // T: element type; D: head size; QT: query heads per CTA (<= 4).
 template <class T, int D, int QT>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, 3)
 decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
   constexpr int CPL = D / 64;  // 8-element chunks per lane per token (q.k)
   constexpr int DPL = D / 32;  // output dims per lane (p.V)
@@ -188,14 +222,24 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
   for (int h = 0; h < QT; ++h) slope[h] = a.alibi ? __ldg(a.alibi + head0 + h) * kLog2e : 0.f;
 
-  float m[QT], l[QT], o[QT][DPL];
+  constexpr int NF = NfOf<QT>::v;  // dots (heads) each lane finishes per sub-tile
+  float slope_own[NF];  // ALiBi slopes of this lane's heads head_of(dg, f)
 #pragma unroll
-  for (int h = 0; h < QT; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.f;
+  for (int f = 0; f < NF; ++f) {
+    if constexpr (QT == 4) slope_own[f] = (dg & 1) ? slope[2 + f] : slope[f];
+    else if constexpr (QT == 2) slope_own[f] = (dg & 1) ? slope[1] : slope[0];
+    else slope_own[f] = slope[0];
+  }
+  float m[NF], l[NF], o[QT][DPL];
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    m[f] = -INFINITY;
+    l[f] = 0.f;
+  }
+#pragma unroll
+  for (int h = 0; h < QT; ++h)
 #pragma unroll
     for (int e = 0; e < DPL; ++e) o[h][e] = 0.f;
-  }
   float *wP = sP + warp * kSub * QT;
   const int qpos = sp.L - 1;
   bool ok = true;
@@ -218,14 +262,16 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
       const int t_lo = max(sp.lo - j0, 0);
       const int t_hi = min(sp.L - j0, kSub);
       if (t_lo >= t_hi) continue;  // warp-uniform
-      // ---- q.k for 16 tokens --------------------------------------------
-      float s[kSub / 4][QT];
+      // ---- q.k for 16 tokens: lane (dg, ts) accumulates partial dots of
+      // tokens it*4 + ts over its dims, index it * QT + h ---------------------
+      constexpr int NV = (kSub / 4) * QT;  // partial dots per lane
+      float v[NV];
       const uint4 *k4 = reinterpret_cast<const uint4 *>(kt + sub * D);
 #pragma unroll
       for (int it = 0; it < kSub / 4; ++it) {
         const int tok = it * 4 + ts;
 #pragma unroll
-        for (int h = 0; h < QT; ++h) s[it][h] = 0.f;
+        for (int h = 0; h < QT; ++h) v[it * QT + h] = 0.f;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           float f[8];
@@ -233,51 +279,60 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
           for (int h = 0; h < QT; ++h)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) s[it][h] = fmaf(q[h][c * 8 + e], f[e], s[it][h]);
+            for (int e = 0; e < 8; ++e) v[it * QT + h] = fmaf(q[h][c * 8 + e], f[e], v[it * QT + h]);
         }
       }
+      // Recursive halving over the 8 dg lanes (xor 4, 2, 1): each level a lane
+      // keeps half of its values and adds the partner's copy of that half, so
+      // the 8 lanes finish the NV dots between them (NF each) instead of every
+      // lane finishing all of them.
+      reduce_over_dg<NV>(v, lane);
+      // lane now holds NF dots of token tk = (dg >> 1) * 4 + ts, heads head_of(dg, f)
+      const int tk = (dg >> 1) * 4 + ts;
+      const int j = j0 + tk;
+      const bool valid = tk >= t_lo && tk < t_hi;
+      float sc[NF];
 #pragma unroll
-      for (int it = 0; it < kSub / 4; ++it)
+      for (int f = 0; f < NF; ++f)
+        sc[f] = valid ? v[f] + slope_own[f] * static_cast<float>(j - qpos) : -INFINITY;
+      // ---- online softmax: max over the 16 lanes holding the same head ----
+      float alpha_own[NF];
 #pragma unroll
-        for (int h = 0; h < QT; ++h) {
-          float v = s[it][h];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          v += __shfl_xor_sync(0xffffffffu, v, 4);
-          const int tok = it * 4 + ts;
-          const int j = j0 + tok;
-          s[it][h] = (tok >= t_lo && tok < t_hi) ? v + slope[h] * static_cast<float>(j - qpos)
-                                                 : -INFINITY;
-        }
-      // ---- online softmax ------------------------------------------------
-#pragma unroll
-      for (int h = 0; h < QT; ++h) {
-        float bm = s[0][h];
-#pragma unroll
-        for (int it = 1; it < kSub / 4; ++it) bm = fmaxf(bm, s[it][h]);
+      for (int f = 0; f < NF; ++f) {
+        float bm = sc[f];
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-        const float mn = fmaxf(m[h], bm);
-        const float alpha = fast_exp2(m[h] - mn);
-        float ps = 0.f;
-#pragma unroll
-        for (int it = 0; it < kSub / 4; ++it) {
-          s[it][h] = fast_exp2(s[it][h] - mn);
-          ps += s[it][h];
-        }
-        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        l[h] = l[h] * alpha + ps;
-        m[h] = mn;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) o[h][e] *= alpha;
+        const float mn = fmaxf(m[f], bm);
+        alpha_own[f] = fast_exp2(m[f] - mn);
+        m[f] = mn;
+        const float p = fast_exp2(sc[f] - mn);
+        l[f] = l[f] * alpha_own[f] + p;  // per-lane partial, summed at the end
+        if (QT > 1 || (dg & 1) == 0) wP[tk * QT + head_of<QT>(dg, f)] = p;
       }
-      if (dg == 0) {
-#pragma unroll
-        for (int it = 0; it < kSub / 4; ++it)
-#pragma unroll
-          for (int h = 0; h < QT; ++h) wP[(it * 4 + ts) * QT + h] = s[it][h];
+      // every lane needs every head's rescale factor for its p.V accumulators
+      float alpha[QT];
+      if constexpr (QT == 4) {
+        const float x0 = __shfl_xor_sync(0xffffffffu, alpha_own[0], 1);
+        const float x1 = __shfl_xor_sync(0xffffffffu, alpha_own[1], 1);
+        const bool hi = dg & 1;
+        alpha[0] = hi ? x0 : alpha_own[0];
+        alpha[1] = hi ? x1 : alpha_own[1];
+        alpha[2] = hi ? alpha_own[0] : x0;
+        alpha[3] = hi ? alpha_own[1] : x1;
+      } else if constexpr (QT == 2) {
+        const float x0 = __shfl_xor_sync(0xffffffffu, alpha_own[0], 1);
+        const bool hi = dg & 1;
+        alpha[0] = hi ? x0 : alpha_own[0];
+        alpha[1] = hi ? alpha_own[0] : x0;
+      } else {
+        alpha[0] = alpha_own[0];
       }
+#pragma unroll
+      for (int h = 0; h < QT; ++h)
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[h][e] *= alpha[h];
       __syncwarp();
       // ---- p.V over the valid tokens ---------------------------------------
       const uint16_t *vrow = vt + sub * D + lane * DPL;
@@ -325,12 +380,20 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
   float *sL = sM + kDecWarps * QT;                       // [warp][QT]
   float *sO = sL + kDecWarps * QT;                       // [warp][QT][D]
 #pragma unroll
-  for (int h = 0; h < QT; ++h) {
+  for (int h = 0; h < QT; ++h)
 #pragma unroll
     for (int e = 0; e < DPL; ++e) sO[(warp * QT + h) * D + lane * DPL + e] = o[h][e];
-    if (lane == 0) {
-      sM[warp * QT + h] = m[h];
-      sL[warp * QT + h] = l[h];
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    float lt = l[f];
+    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+    if (lane < 2 && (QT > 1 || lane == 0)) {
+      const int hf = head_of<QT>(lane, f);
+      sM[warp * QT + hf] = m[f];
+      sL[warp * QT + hf] = lt;
     }
   }
   __syncthreads();
@@ -390,7 +453,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-static int stages_for(int BS) { return BS <= 16 ? 3 : 2; }
+static int stages_for(int BS) { return BS <= 16 ? 2 : 1; }
 
 static size_t split_smem_bytes(int BS, int D, int QT, int split_blocks) {
   const size_t tiles = static_cast<size_t>(kDecWarps) * stages_for(BS) * 2 * BS * D * 2;

@@ -59,9 +59,9 @@ cudaError_t launch_decode(void *out, const void *query, int num_seqs, const void
 cudaError_t read_device_error_decode(unsigned long long *out);
 
 // prefill.cu
-cudaError_t launch_prefill(void *out, const void *query, int num_seqs, const int32_t *cu_q,
-                           const int32_t *cu_k, int max_query_len, int max_seq_len,
-                           const void *kv_cache, const int32_t *block_tables,
+cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, int num_seqs,
+                           const int32_t *cu_q, const int32_t *cu_k, int max_query_len,
+                           int max_seq_len, const void *kv_cache, const int32_t *block_tables,
                            int max_blocks_per_seq, const Geometry &g, cudaStream_t stream);
 cudaError_t read_device_error_prefill(unsigned long long *out);
 

@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace pkv {
 
@@ -33,10 +34,41 @@ struct PrefillArgs {
   const int32_t *block_tables;
   const float *alibi;
   int64_t num_blocks;
+  int64_t num_q_tokens;  // rows of query / out
   int num_seqs, max_blocks_per_seq;
   int H, KVH, QPK, BS, window;
   float scale_log2;
 };
+
+// Per-(sequence, query tile) facts shared by both kernels; false if the tile
+// is empty or the sequence's metadata is inconsistent (recorded).
+struct TileSpan {
+  int qs, qb, Lb, cb, q0, q_rows, kv_start, kv_end, kv_lo, ntiles;
+};
+
+template <int BM_, int BN_>
+__device__ __forceinline__ bool tile_span(const PrefillArgs &a, int b, int tile, bool report,
+                                          TileSpan &t) {
+  t.q0 = tile * BM_;
+  t.qs = __ldg(a.cu_q + b);
+  const int qe = __ldg(a.cu_q + b + 1);
+  t.qb = qe - t.qs;
+  t.Lb = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
+  if (t.q0 >= t.qb) return false;
+  if (t.qs < 0 || qe > a.num_q_tokens || t.qb > t.Lb ||
+      static_cast<int64_t>(t.Lb) > static_cast<int64_t>(a.max_blocks_per_seq) * a.BS) {
+    if (report) record_error(PKV_ERR_BOUNDS, b);
+    return false;
+  }
+  t.cb = t.Lb - t.qb;
+  t.q_rows = min(BM_, t.qb - t.q0);
+  const int i_first = t.cb + t.q0, i_last = t.cb + t.q0 + t.q_rows - 1;
+  t.kv_lo = a.window > 0 ? max(0, i_first - a.window + 1) : 0;
+  t.kv_start = t.kv_lo / BN_ * BN_;
+  t.kv_end = i_last + 1;
+  t.ntiles = (t.kv_end - t.kv_start + BN_ - 1) / BN_;
+  return true;
+}
 
 namespace mma_path {
 
@@ -108,26 +140,13 @@ prefill_mma_kernel(const PrefillArgs a) {
 
   const int h = blockIdx.x, b = blockIdx.y;
   const int tile = gridDim.z - 1 - blockIdx.z;
-  const int q0 = tile * BM;
-  const int qs = __ldg(a.cu_q + b), qb = __ldg(a.cu_q + b + 1) - qs;
-  const int Lb = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
-  if (q0 >= qb) return;
-  const bool report = (threadIdx.x == 0 && h == 0);
-  if (qb > Lb || Lb > a.max_blocks_per_seq * a.BS) {
-    if (report) record_error(PKV_ERR_BOUNDS, b);
-    return;
-  }
-  const int cb = Lb - qb;
+  TileSpan sp;
+  if (!tile_span<BM, BN>(a, b, tile, threadIdx.x == 0 && h == 0, sp)) return;
+  const int q0 = sp.q0, qs = sp.qs, cb = sp.cb, q_rows = sp.q_rows;
+  const int kv_start = sp.kv_start, kv_end = sp.kv_end, ntiles = sp.ntiles;
   const int g = h / a.QPK;
-  const int q_rows = min(BM, qb - q0);
-  const int i_first = cb + q0, i_last = cb + q0 + q_rows - 1;
-  const int kv_lo = a.window > 0 ? max(0, i_first - a.window + 1) : 0;
-  const int kv_start = kv_lo / BN * BN;
-  const int kv_end = i_last + 1;  // exclusive
-  const int ntiles = (kv_end - kv_start + BN - 1) / BN;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t *trow = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
-  const int64_t kv_row_stride = static_cast<int64_t>(a.KVH) * D;
 
   // ---- async loads --------------------------------------------------------
   auto load_q = [&]() {
@@ -160,7 +179,6 @@ prefill_mma_kernel(const PrefillArgs a) {
       cp_async16(sV + buf * TILE_BYTES + swz<D>(r, c), a.v_half + off, v);
     }
   };
-  (void)kv_row_stride;
 
   load_q();
   load_kv(0, 0);
@@ -322,9 +340,378 @@ cudaError_t launch(const PrefillArgs &a, int max_query_len, cudaStream_t stream)
 
 }  // namespace mma_path
 
-cudaError_t launch_prefill(void *out, const void *query, int num_seqs, const int32_t *cu_q,
-                           const int32_t *cu_k, int max_query_len, int max_seq_len,
-                           const void *kv_cache, const int32_t *block_tables,
+// ===========================================================================
+// tcgen05 / TMEM kernel (sm_100a family)
+//
+// CTA = (query head, sequence, 128-row query tile); 8 warps:
+//   warp 0     TMA producer: the Q tile once, then per 128-key tile the K and
+//              V rows of this KV head, one 4-D box (block_size rows x 64
+//              dims, 128-byte swizzle) per cache block and 64-dim half,
+//              straight from the paged cache through the block table; blocks
+//              outside the visible range are loaded from an out-of-range
+//              coordinate, which the TMA unit fills with zeros.
+//   warp 1     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
+//              score buffers (issued one tile ahead so the tensor core works
+//              on S_{j+1} while the softmax warps work on S_j), then
+//              O += P_j V_j with P_j read from TMEM (the "TS" form) and V_j
+//              as an MN-major shared-memory operand.
+//   warps 4-7  softmax: thread r owns TMEM lane r = query row r.  It loads
+//              its 128 scores, applies scale, ALiBi and the causal / window
+//              mask in the log2 domain, keeps a running max that is only
+//              moved (and O rescaled in TMEM) when it grows by more than
+//              2^8, writes P as bf16/fp16 pairs over the first 64 columns of
+//              the score buffer, and finally normalises O and stores it.
+//   warps 2-3  idle.
+// TMEM: S0 = columns [0,128), S1 = [128,256), O = [256, 256 + head_size).
+// Every wait is bounded; a timeout raises a CTA-wide abort flag, the roles
+// stop, in-flight copies and MMAs are drained, TMEM is freed.
+// ===========================================================================
+namespace tc_path {
+
+constexpr int BM = 128, BN = 128, NST = 2;
+constexpr int kThreads = 256;
+
+template <int D>
+struct Lay {
+  static constexpr int REG = 128 * 128;   // one 64-column region of 128 rows
+  static constexpr int NREG = D / 64;
+  static constexpr int TILE = REG * NREG;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + TILE;
+  static constexpr int OFF_V = OFF_K + NST * TILE;
+  static constexpr int OFF_BAR = OFF_V + NST * TILE;
+  static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NST, B_EMPTY = B_VF + NST,
+                       B_SF = B_EMPTY + NST, B_PF = B_SF + 2, B_O = B_PF + 2, B_FIN = B_O + 1,
+                       NBAR = B_FIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 32;
+  // + alignment slack; at least ~114 KB so that one CTA owns an SM (and all
+  // of its tensor memory)
+  static constexpr int ALLOC = (BYTES + 1024) > 118 * 1024 ? (BYTES + 1024) : 118 * 1024;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
+                                              volatile uint32_t *abort_flag, int64_t where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1u;
+      record_error(PKV_ERR_TIMEOUT, where);
+      return false;
+    }
+  }
+}
+
+// Warp-uniform verdict of a bounded wait performed by every lane.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity,
+                                          volatile uint32_t *abort_flag, int64_t where) {
+  const bool got = wait_or_abort(bar, parity, abort_flag, where);
+  return __all_sync(0xffffffffu, got);
+}
+
+template <class T>
+struct AB;
+template <>
+struct AB<BF16> {
+  static constexpr int v = 1;
+};
+template <>
+struct AB<FP16> {
+  static constexpr int v = 0;
+};
+
+template <class T, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
+                  const __grid_constant__ CUtensorMap kvmap) {
+  using L = Lay<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+  volatile uint32_t *abort_flag = misc + 1;
+
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int tile = gridDim.z - 1 - blockIdx.z;
+  TileSpan sp;
+  if (!tile_span<BM, BN>(a, b, tile, threadIdx.x == 0 && h == 0, sp)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = h / a.QPK;
+  const int BS = a.BS;
+  const int TB = BN / BS;  // cache blocks per key tile
+  const int ntiles = sp.ntiles;
+  const int64_t where = static_cast<int64_t>(b) * a.H + h;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::NBAR; ++i) mbar_init(&bars[i], i == L::B_PF || i == L::B_PF + 1 ? 128 : 1);
+    misc[1] = 0;  // abort
+    misc[2] = 0;  // key tiles issued
+    fence_mbar_init();
+    prefetch_tensormap(&qmap);
+    prefetch_tensormap(&kvmap);
+  }
+  if (warp == 1) tc5::tmem_alloc<512>(misc);
+  tc5::fence_before_sync();
+  __syncthreads();
+  tc5::fence_after_sync();
+  const uint32_t tmem = misc[0];
+  const uint32_t tmem_o = tmem + 256;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const int32_t *trow = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars[L::B_Q], L::TILE);
+      for (int r = 0; r < L::NREG; ++r)
+        tc5::tma_load_3d(smem + L::OFF_Q + r * L::REG, &qmap, &bars[L::B_Q], 64 * r, h,
+                         sp.qs + sp.q0);
+    }
+    int j = 0;
+    for (; j < ntiles; ++j) {
+      const int s = j % NST;
+      if (j >= NST && !warp_wait(&bars[L::B_EMPTY + s], ((j / NST) - 1) & 1, abort_flag, where))
+        break;
+      const int kv0 = sp.kv_start + j * BN;
+      int coord = -BS;  // out of range: zero fill
+      if (lane < TB) {
+        const int lb = kv0 / BS + lane;
+        const int p0 = lb * BS;
+        if (p0 < sp.kv_end && p0 + BS > sp.kv_lo) {
+          const int pb = __ldg(trow + lb);
+          if (pb < 0 || pb >= a.num_blocks)
+            record_error(PKV_ERR_BOUNDS, static_cast<int64_t>(b) * a.max_blocks_per_seq + lb);
+          else
+            coord = pb * BS;
+        }
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[L::B_KF + s], L::TILE);
+        mbar_arrive_expect_tx(&bars[L::B_VF + s], L::TILE);
+      }
+      __syncwarp();
+      if (lane < TB) {
+        uint8_t *kd = smem + L::OFF_K + s * L::TILE + lane * BS * 128;
+        uint8_t *vd = smem + L::OFF_V + s * L::TILE + lane * BS * 128;
+        for (int r = 0; r < L::NREG; ++r) {
+          tma_load_4d(kd + r * L::REG, &kvmap, &bars[L::B_KF + s], 64 * r, g, coord, 0);
+          tma_load_4d(vd + r * L::REG, &kvmap, &bars[L::B_VF + s], 64 * r, g, coord, 1);
+        }
+      }
+    }
+    if (lane == 0) misc[2] = static_cast<uint32_t>(j);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t ID_QK = tc5::idesc_f16(AB<T>::v, 0, BM, BN);
+    constexpr uint32_t ID_PV = tc5::idesc_f16(AB<T>::v, 1, BM, D);
+    bool ok = warp_wait(&bars[L::B_Q], 0, abort_flag, where);
+    auto issue_qk = [&](int j) -> bool {
+      const int s = j % NST;
+      if (!warp_wait(&bars[L::B_KF + s], (j / NST) & 1, abort_flag, where)) return false;
+      tc5::fence_after_sync();
+      if (lane == 0) {
+        const uint32_t sb = tmem + (j & 1) * 128;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const int r = k / 4, kk = k % 4;
+          const uint64_t qd = tc5::sdesc_sw128(sbase + L::OFF_Q + r * L::REG + kk * 32, 16, 1024);
+          const uint64_t kd =
+              tc5::sdesc_sw128(sbase + L::OFF_K + s * L::TILE + r * L::REG + kk * 32, 16, 1024);
+          tc5::mma_ss(sb, qd, kd, ID_QK, k > 0 ? 1u : 0u);
+        }
+        tc5::commit(&bars[L::B_SF + (j & 1)]);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok) ok = issue_qk(0);
+    for (int j = 0; ok && j < ntiles; ++j) {
+      if (j + 1 < ntiles && !issue_qk(j + 1)) break;
+      const int s = j % NST;
+      if (!warp_wait(&bars[L::B_VF + s], (j / NST) & 1, abort_flag, where)) break;
+      // Positions past the sequence end hold whatever the cache holds there
+      // (possibly non-finite); their P is exactly 0, but 0 * NaN is NaN, so
+      // their V rows are zeroed before the PV product reads them.
+      const int kv0 = sp.kv_start + j * BN;
+      const int zr = max(0, sp.Lb - kv0);
+      if (zr < BN) {
+        uint8_t *vt = smem + L::OFF_V + s * L::TILE;
+        const int n16 = (BN - zr) * 8;  // 16-byte chunks per region
+        for (int r = 0; r < L::NREG; ++r)
+          for (int c = lane; c < n16; c += 32)
+            *reinterpret_cast<uint4 *>(vt + r * L::REG + zr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (!warp_wait(&bars[L::B_PF + (j & 1)], (j >> 1) & 1, abort_flag, where)) break;
+      tc5::fence_after_sync();
+      if (lane == 0) {
+        const uint32_t pb = tmem + (j & 1) * 128;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t vd =
+              tc5::sdesc_sw128(sbase + L::OFF_V + s * L::TILE + k * 2048, L::REG, 1024);
+          tc5::mma_ts(tmem_o, pb + k * 8, vd, ID_PV, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        tc5::commit(&bars[L::B_EMPTY + s]);
+        tc5::commit(&bars[L::B_O]);
+      }
+      __syncwarp();
+    }
+    // every MMA this thread issued has completed before TMEM is released
+    if (lane == 0) tc5::commit(&bars[L::B_FIN]);
+    __syncwarp();
+    mbar_wait_bounded(&bars[L::B_FIN], 0, where);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int row = (warp - 4) * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int pos = sp.cb + sp.q0 + row;
+    const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
+    const float slope = a.alibi ? __ldg(a.alibi + h) * kLog2e : 0.f;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      if (!warp_wait(&bars[L::B_SF + (j & 1)], (j >> 1) & 1, abort_flag, where)) {
+        ok = false;
+        break;
+      }
+      tc5::fence_after_sync();
+      const uint32_t sb = tmem + lane_base + (j & 1) * 128;
+      uint32_t raw[BN / 32][32];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tc5::tmem_ld32(sb + 32 * c, raw[c]);
+      tc5::tmem_ld_wait();
+      const int kv0 = sp.kv_start + j * BN;
+      const bool full = (kv0 + BN - 1 <= pos) && (kv0 >= lo);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int jj = kv0 + c * 32 + e;
+          float x = fmaf(__uint_as_float(raw[c][e]), a.scale_log2,
+                         slope * static_cast<float>(jj - pos));
+          if (!full && (jj > pos || jj < lo)) x = -INFINITY;
+          raw[c][e] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+      // running max: moved only when it grows by more than 8 (2^8 in p)
+      float alpha = 1.f;
+      bool resc = false;
+      if (m == -INFINITY) {
+        m = mx;
+      } else if (mx > m + 8.f) {
+        alpha = fast_exp2(m - mx);
+        m = mx;
+        resc = true;
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+        // PV_{j-1} must have landed in O before it is rescaled
+        if (!warp_wait(&bars[L::B_O], (j - 1) & 1, abort_flag, where)) {
+          ok = false;
+          break;
+        }
+        tc5::fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tc5::tmem_ld32(tmem_o + lane_base + 32 * c, o);
+          tc5::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc5::tmem_st32(tmem_o + lane_base + 32 * c, o);
+        }
+        tc5::tmem_st_wait();
+      }
+      l *= alpha;
+      const float mu = m == -INFINITY ? 0.f : m;
+      uint32_t pk[2][32];
+      float ps = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = fast_exp2(__uint_as_float(raw[c][e]) - mu);
+          const float p1 = fast_exp2(__uint_as_float(raw[c][e + 1]) - mu);
+          ps += p0 + p1;
+          pk[(c * 32 + e) / 64][((c * 32 + e) % 64) / 2] = T::from_f2(p0, p1);
+        }
+      l += ps;
+      tc5::tmem_st32(sb, pk[0]);
+      tc5::tmem_st32(sb + 32, pk[1]);
+      tc5::tmem_st_wait();
+      tc5::fence_before_sync();
+      mbar_arrive(&bars[L::B_PF + (j & 1)]);
+    }
+    if (ok && warp_wait(&bars[L::B_O], (ntiles - 1) & 1, abort_flag, where)) {
+      tc5::fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool valid = row < sp.q_rows;
+      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) +
+                                             (static_cast<int64_t>(sp.qs + sp.q0 + row) * a.H + h) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tc5::tmem_ld32(tmem_o + lane_base + 32 * c, o);
+        tc5::tmem_ld_wait();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = T::from_f2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[c * 4 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+      }
+    }
+    tc5::fence_before_sync();
+  }
+
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) {
+    // let every copy that was issued land before the CTA's memory goes away
+    mbar_wait_bounded(&bars[L::B_Q], 0, where);
+    const int issued = static_cast<int>(misc[2]);
+    for (int s = 0; s < NST; ++s) {
+      const int t_last = issued - 1 - ((issued - 1 - s) % NST + NST) % NST;
+      if (t_last >= 0 && t_last % NST == s) {
+        mbar_wait_bounded(&bars[L::B_KF + s], (t_last / NST) & 1, where);
+        mbar_wait_bounded(&bars[L::B_VF + s], (t_last / NST) & 1, where);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc5::fence_after_sync();
+    tc5::tmem_dealloc<512>(tmem);
+  }
+}
+
+template <class T, int D>
+cudaError_t launch(const PrefillArgs &a, int max_query_len, const CUtensorMap &qmap,
+                   const CUtensorMap &kvmap, cudaStream_t stream) {
+  const size_t smem = Lay<D>::ALLOC;
+  auto kern = prefill_tc_kernel<T, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int tiles = (max_query_len + BM - 1) / BM;
+  dim3 grid(a.H, a.num_seqs, tiles);
+  kern<<<grid, kThreads, smem, stream>>>(a, qmap, kvmap);
+  return cudaGetLastError();
+}
+
+}  // namespace tc_path
+
+cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, int num_seqs,
+                           const int32_t *cu_q, const int32_t *cu_k, int max_query_len,
+                           int max_seq_len, const void *kv_cache, const int32_t *block_tables,
                            int max_blocks_per_seq, const Geometry &g, cudaStream_t stream) {
   (void)max_seq_len;
   PrefillArgs a{};
@@ -337,6 +724,7 @@ cudaError_t launch_prefill(void *out, const void *query, int num_seqs, const int
   a.block_tables = block_tables;
   a.alibi = g.alibi;
   a.num_blocks = g.num_blocks;
+  a.num_q_tokens = num_q_tokens;
   a.num_seqs = num_seqs;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.H = g.H;
@@ -346,11 +734,45 @@ cudaError_t launch_prefill(void *out, const void *query, int num_seqs, const int
   a.window = g.window;
   a.scale_log2 = g.scale * kLog2e;
   const bool bf = g.dtype == PKV_BF16;
+#ifdef PKV_PREFILL_MMA_SYNC
   if (g.D == 128) return bf ? mma_path::launch<BF16, 128>(a, max_query_len, stream)
                             : mma_path::launch<FP16, 128>(a, max_query_len, stream);
   if (g.D == 64) return bf ? mma_path::launch<BF16, 64>(a, max_query_len, stream)
                            : mma_path::launch<FP16, 64>(a, max_query_len, stream);
   return cudaErrorInvalidValue;
+#else
+  // Q: (D, H, tokens); cache: (D, KVH, NB * BS tokens, 2 halves); 64-element
+  // (128-byte) inner boxes with the 128-byte swizzle the MMA descriptors use.
+  const CUtensorMapDataType dt =
+      bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap qmap, kvmap;
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.D), static_cast<cuuint64_t>(g.H),
+                                static_cast<cuuint64_t>(num_q_tokens)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.D) * 2,
+                                   static_cast<cuuint64_t>(g.H) * g.D * 2};
+    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(tc_path::BM)};
+    if (encode_tensor_map(&qmap, dt, 3, const_cast<void *>(query), dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.D), static_cast<cuuint64_t>(g.KVH),
+                                static_cast<cuuint64_t>(g.num_blocks * g.BS), 2};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.D) * 2,
+                                   static_cast<cuuint64_t>(g.row_elems) * 2,
+                                   static_cast<cuuint64_t>(g.num_blocks * g.block_elems) * 2};
+    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(g.BS), 1};
+    if (encode_tensor_map(&kvmap, dt, 4, const_cast<void *>(kv_cache), dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (g.D == 128) return bf ? tc_path::launch<BF16, 128>(a, max_query_len, qmap, kvmap, stream)
+                            : tc_path::launch<FP16, 128>(a, max_query_len, qmap, kvmap, stream);
+  if (g.D == 64) return bf ? tc_path::launch<BF16, 64>(a, max_query_len, qmap, kvmap, stream)
+                           : tc_path::launch<FP16, 64>(a, max_query_len, qmap, kvmap, stream);
+  return cudaErrorInvalidValue;
+#endif
 }
 
 cudaError_t read_device_error_prefill(unsigned long long *out) {

@@ -81,9 +81,11 @@ def test_decode_and_prefill_validation(lib):
     p3 = _p(num_heads=24, num_kv_heads=8)  # 3 queries per KV head: not built for decode
     assert lib.paged_attn_decode(nul, nul, 2, nul, 4, nul, 1, nul, 8, ctypes.byref(p3), nul, 0,
                                  nul) == B.PKV_ERR_UNSUPPORTED
-    assert lib.paged_attn_prefill_varlen(nul, nul, 3, nul, nul, 0, 5, nul, 4, nul, 1,
+    assert lib.paged_attn_prefill_varlen(nul, nul, 10, 3, nul, nul, 0, 5, nul, 4, nul, 1,
                                          ctypes.byref(p), nul) == B.PKV_OK
-    assert lib.paged_attn_prefill_varlen(nul, nul, 3, nul, nul, 5, 5, nul, 4, nul, 1,
+    assert lib.paged_attn_prefill_varlen(nul, nul, 10, 3, nul, nul, 5, 5, nul, 4, nul, 1,
+                                         ctypes.byref(p), nul) == B.PKV_ERR_INVALID
+    assert lib.paged_attn_prefill_varlen(nul, nul, -1, 3, nul, nul, 5, 5, nul, 4, nul, 1,
                                          ctypes.byref(p), nul) == B.PKV_ERR_INVALID
 
 
