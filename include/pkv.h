@@ -144,6 +144,38 @@ pkv_status paged_attn_decode(void *out, const void *query, int32_t num_seqs,
                              const pkv_attn_params *params, void *workspace,
                              size_t workspace_bytes, pkv_stream_t stream);
 
+/*
+ * paged_attn_decode_noalloc -- paged_attn_decode for callers that cannot
+ * allocate device memory.  The attention-backend pages have no counterpart of
+ * this call; it exists for code that is handed its device buffers by a host
+ * framework and may not call cudaMalloc itself (an inference-server plugin
+ * working inside the framework's memory budget, or a serving loop where an
+ * allocation would synchronise the device and stall the other streams).
+ *
+ * Arguments and results are those of paged_attn_decode without the
+ * workspace: the split partials go to a static device array of
+ * PKV_DECODE_STATIC_SCRATCH_BYTES bytes that is part of the library, so every
+ * GPU that loads the library holds it until the process exits.  The call
+ * allocates nothing and calls no allocating routine.
+ *   - Sizes whose workspace (paged_attn_decode_workspace_size) exceeds
+ *     PKV_DECODE_STATIC_SCRATCH_BYTES return PKV_ERR_UNSUPPORTED, nothing
+ *     enqueued.
+ *   - The first call on a device looks up the array's device address (a
+ *     one-time set-up per device); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array, which keeps the last call's contents.
+ *     Nothing in it needs to start at zero, but calls that overlap on the GPU
+ *     (on different streams, or otherwise unordered) race on it.
+ */
+#define PKV_DECODE_STATIC_SCRATCH_BYTES (64u << 20)
+pkv_status paged_attn_decode_noalloc(void *out, const void *query, int32_t num_seqs,
+                                     const void *kv_cache, int64_t num_blocks,
+                                     const int32_t *block_tables,
+                                     int32_t max_blocks_per_seq,
+                                     const int32_t *seq_lens, int32_t max_seq_len,
+                                     const pkv_attn_params *params,
+                                     pkv_stream_t stream);
+
 /* Bytes of workspace paged_attn_decode needs for these sizes (host only,
  * never fails; 0 when no split is used).  Returns 0 for invalid params. */
 size_t paged_attn_decode_workspace_size(int32_t num_seqs, int32_t max_seq_len,

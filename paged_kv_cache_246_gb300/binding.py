@@ -23,6 +23,7 @@ _DTYPES = {torch.float16: PKV_FP16, torch.bfloat16: PKV_BF16}
 
 # Every function include/pkv.h declares.
 EXPORTS = ("kv_cache_write", "paged_attn_decode", "paged_attn_decode_workspace_size",
+           "paged_attn_decode_noalloc",
            "paged_attn_prefill_varlen", "kv_copy_blocks", "kv_swap_blocks",
            "pkv_status_string", "pkv_device_error", "pkv_abi_version")
 
@@ -58,6 +59,7 @@ def lib() -> ctypes.CDLL:
             "kv_cache_write": (i32, [vp, vp, i64, vp, i64, vp, P, vp]),
             "paged_attn_decode": (i32, [vp, vp, i32, vp, i64, vp, i32, vp, i32, P, vp, sz, vp]),
             "paged_attn_decode_workspace_size": (sz, [i32, i32, P]),
+            "paged_attn_decode_noalloc": (i32, [vp, vp, i32, vp, i64, vp, i32, vp, i32, P, vp]),
             "paged_attn_prefill_varlen": (i32, [vp, vp, i64, i32, vp, vp, i32, i32, vp, i64, vp,
                                                 i32, P, vp]),
             "kv_copy_blocks": (i32, [vp, i32, i64, vp, i64, P, vp]),
@@ -171,6 +173,31 @@ def paged_attn_decode(out: torch.Tensor, query: torch.Tensor, kv_cache: torch.Te
                                    seq_lens.data_ptr(), int(max_seq_len), ctypes.byref(params),
                                    ws_ptr, ws_bytes, _stream(stream)),
            "paged_attn_decode")
+
+
+def paged_attn_decode_noalloc(out: torch.Tensor, query: torch.Tensor, kv_cache: torch.Tensor,
+                              block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                              max_seq_len: int, params: AttnParams, stream=None) -> None:
+    """paged_attn_decode without a workspace, for callers that may not
+    allocate device memory: the split partials go to the library's static
+    device scratch (PKV_DECODE_STATIC_SCRATCH_BYTES per GPU, shared by all
+    calls; calls that overlap on the GPU race on it).  Sizes that need more
+    scratch raise PkvError with PKV_ERR_UNSUPPORTED."""
+    for t, n in ((out, "out"), (query, "query"), (kv_cache, "kv_cache")):
+        _need(t, n)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    nb = _cache_blocks(kv_cache, params)
+    B = seq_lens.numel()
+    hd = params.num_heads * params.head_size
+    if query.numel() != B * hd or out.numel() != B * hd or block_tables.shape[0] != B:
+        raise ValueError("query/out/block_tables sizes disagree with seq_lens")
+    _check(lib().paged_attn_decode_noalloc(out.data_ptr(), query.data_ptr(), B,
+                                           kv_cache.data_ptr(), nb, block_tables.data_ptr(),
+                                           int(block_tables.shape[1]), seq_lens.data_ptr(),
+                                           int(max_seq_len), ctypes.byref(params),
+                                           _stream(stream)),
+           "paged_attn_decode_noalloc")
 
 
 def paged_attn_prefill_varlen(out: torch.Tensor, query: torch.Tensor, cu_seqlens_q: torch.Tensor,

@@ -196,6 +196,31 @@ pkv_status paged_attn_decode(void *out, const void *query, int32_t num_seqs, con
                                  seq_lens, max_seq_len, g, plan, workspace, s));
 }
 
+pkv_status paged_attn_decode_noalloc(void *out, const void *query, int32_t num_seqs,
+                                     const void *kv_cache, int64_t num_blocks,
+                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t *seq_lens, int32_t max_seq_len,
+                                     const pkv_attn_params *params, pkv_stream_t stream) {
+  Geometry g;
+  pkv_status st = make_geometry(params, num_blocks, &g);
+  if (st != PKV_OK) return st;
+  if (!decode_qpk_supported(g.QPK)) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || num_seqs > 65535 || max_seq_len < 0 || max_blocks_per_seq <= 0)
+    return PKV_ERR_INVALID;
+  if (num_seqs == 0) return PKV_OK;
+  cudaError_t e = select_device(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  if (paged_attn_decode_workspace_size(num_seqs, max_seq_len, params) >
+      PKV_DECODE_STATIC_SCRATCH_BYTES)
+    return PKV_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  size_t scratch_bytes = 0;
+  if (static_decode_scratch(&scratch, &scratch_bytes) != cudaSuccess) return PKV_ERR_CUDA;
+  return paged_attn_decode(out, query, num_seqs, kv_cache, num_blocks, block_tables,
+                           max_blocks_per_seq, seq_lens, max_seq_len, params, scratch,
+                           scratch_bytes, stream);
+}
+
 pkv_status paged_attn_prefill_varlen(void *out, const void *query, int64_t num_query_tokens,
                                      int32_t num_seqs,
                                      const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,

@@ -27,6 +27,7 @@
 //    several splits write (o, m, l) partials that decode_combine_kernel
 //    merges (flash-decoding).
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -566,6 +567,44 @@ cudaError_t launch_decode(void *out, const void *query, int num_seqs, const void
   }
 #undef PKV_DEC
   return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// Static decode scratch for callers that cannot allocate device memory.
+//
+// The split partials of paged_attn_decode_noalloc live in this file-scope
+// array instead of a caller workspace.  The array belongs to the module, so
+// every GPU that loads this library holds it until the process exits.  In
+// host code its name is only a host-side stand-in: the device address must be
+// looked up (once per device, with that device current) and passed to the
+// kernels.  All calls share the array and it keeps the last call's contents;
+// nothing in it has to start at zero, because the combine pass only reads
+// partials the split pass of the same call has just written.  Calls whose
+// work overlaps on the GPU (different streams, or before the previous call
+// has finished) race on it.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_decode_scratch[PKV_DECODE_STATIC_SCRATCH_BYTES];
+
+static void *g_scratch_addr[64];
+static bool g_scratch_known[64];
+static std::mutex g_scratch_mu;
+
+cudaError_t static_decode_scratch(void **ptr, size_t *bytes) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_known[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+    g_scratch_known[dev] = true;
+  }
+  *ptr = g_scratch_addr[dev];
+  *bytes = sizeof(g_decode_scratch);
+  return cudaSuccess;
 }
 
 cudaError_t read_device_error_decode(unsigned long long *out) {

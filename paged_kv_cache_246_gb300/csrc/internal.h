@@ -57,6 +57,9 @@ cudaError_t launch_decode(void *out, const void *query, int num_seqs, const void
                           const int32_t *seq_lens, int max_seq_len, const Geometry &g,
                           const DecodePlan &plan, void *workspace, cudaStream_t stream);
 cudaError_t read_device_error_decode(unsigned long long *out);
+// Device address and size of the static decode scratch of the current device
+// (looked up on the first call per device).
+cudaError_t static_decode_scratch(void **ptr, size_t *bytes);
 
 // prefill.cu
 cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, int num_seqs,
