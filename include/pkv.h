@@ -73,7 +73,7 @@ typedef enum pkv_dtype { PKV_FP16 = 0, PKV_BF16 = 1 } pkv_dtype;
  *   num_heads % num_kv_heads == 0 (xformers.py XFormersImpl.__init__);
  *     query head h reads KV head h / (num_heads / num_kv_heads).
  *   head_size: 64 or 128.  block_size: 8, 16, 32 or 64.
- *   scale: multiplies q.k before the softmax.
+ *   scale: > 0, multiplies q.k before the softmax.
  *   alibi_slopes: device fp32[num_heads] or NULL; adds slope_h * (j - i) to
  *     the score of key position j for query position i
  *     (xformers.py _make_alibi_bias).

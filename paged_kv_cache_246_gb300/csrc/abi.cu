@@ -94,7 +94,7 @@ static pkv_status make_geometry(const pkv_attn_params *p, int64_t num_blocks, Ge
   if (p->dtype != PKV_FP16 && p->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
   if (p->head_size != 64 && p->head_size != 128) return PKV_ERR_UNSUPPORTED;
   if (p->block_size != 16 && p->block_size != 32) return PKV_ERR_UNSUPPORTED;
-  if (!std::isfinite(p->scale)) return PKV_ERR_INVALID;
+  if (!std::isfinite(p->scale) || p->scale <= 0.f) return PKV_ERR_INVALID;
   if (num_blocks <= 0) return PKV_ERR_INVALID;
   if (num_blocks * p->block_size > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
   if (p->alibi_slopes && !aligned(p->alibi_slopes, 4)) return PKV_ERR_INVALID;

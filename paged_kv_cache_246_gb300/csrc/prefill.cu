@@ -709,6 +709,451 @@ cudaError_t launch(const PrefillArgs &a, int max_query_len, const CUtensorMap &q
 
 }  // namespace tc_path
 
+// ===========================================================================
+// tcgen05 / TMEM kernel, two query tiles per CTA (ping-pong).
+//
+// CTA = two 128-row query tiles sharing every K/V tile: two query heads of one
+// KV group on the same rows when the group has an even number of heads
+// (grouped-query reuse), else the same head on two consecutive row tiles.
+// 12 warps:
+//   warp 0      TMA producer (the two Q tiles once; per 128-key tile the K and
+//               V rows of the KV head, one box per cache block and 64-dim
+//               half; blocks outside the visible range come from an
+//               out-of-range coordinate, which the TMA unit zero-fills).
+//   warp 1      MMA issuer (one thread), in the order
+//                 QK_A(0) QK_B(0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...
+//               so the tensor core works on one tile while the other tile's
+//               softmax runs.  S = Q K^T lands in the tile's TMEM score
+//               buffer; O += P V reads P from TMEM (the "TS" form) and V as an
+//               MN-major 128-byte-swizzled shared-memory operand.
+//   warps 4-7   softmax of tile A, warps 8-11 of tile B: thread r owns TMEM
+//               lane r = query row r; scores are loaded 128 at a time, masked
+//               (causal, window, range) only on tiles that need it, the
+//               running max is moved (and O rescaled in TMEM) only when it
+//               grows by more than 2^8, and P is written back as bf16/fp16
+//               pairs over the first 64 columns of the score buffer, 16
+//               columns at a time.
+//   warps 2-3   idle.
+// TMEM: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [384, 384+D).
+// Every wait is bounded; a timeout raises a CTA-wide abort flag, the roles
+// stop, in-flight copies and MMAs are drained, TMEM is freed.
+// ===========================================================================
+namespace tc2 {
+
+constexpr int BM = 128, BN = 128, NST = 2;
+constexpr int kThreads = 384;
+
+template <int D>
+struct Lay {
+  static constexpr int REG = 128 * 128;
+  static constexpr int NREG = D / 64;
+  static constexpr int TILE = REG * NREG;
+  static constexpr int OFF_Q = 0;  // two Q tiles
+  static constexpr int OFF_K = 2 * TILE;
+  static constexpr int OFF_V = OFF_K + NST * TILE;
+  static constexpr int OFF_BAR = OFF_V + NST * TILE;
+  static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NST, B_EMPTY = B_VF + NST,
+                       B_SF = B_EMPTY + NST, B_PF = B_SF + 2, B_O = B_PF + 2, B_FIN = B_O + 2,
+                       NBAR = B_FIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 32;
+  static constexpr int ALLOC = (BYTES + 1024) > 118 * 1024 ? (BYTES + 1024) : 118 * 1024;
+};
+
+// One query tile of the CTA: head, first row within the sequence, rows,
+// and the half-open range of the CTA's key tiles it needs.
+struct QTile {
+  int head, q0, rows, j0, j1;
+};
+
+template <class T, int D, bool ALIBI>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc2_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
+                   const __grid_constant__ CUtensorMap kvmap, int pair_heads) {
+  using L = Lay<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+  volatile uint32_t *abort_flag = misc + 1;
+
+  // ---- which two tiles, and the key-tile range they span (CTA-uniform) ----
+  const int b = blockIdx.y;
+  const int zt = gridDim.z - 1 - blockIdx.z;  // heaviest tiles first
+  QTile qt[2];
+  if (pair_heads) {
+    qt[0].head = 2 * blockIdx.x;
+    qt[1].head = 2 * blockIdx.x + 1;
+    qt[0].q0 = qt[1].q0 = zt * BM;
+  } else {
+    qt[0].head = qt[1].head = blockIdx.x;
+    qt[0].q0 = zt * 2 * BM;
+    qt[1].q0 = qt[0].q0 + BM;
+  }
+  const int qs = __ldg(a.cu_q + b), qe = __ldg(a.cu_q + b + 1);
+  const int qb = qe - qs;
+  const int Lb = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
+  if (qt[0].q0 >= qb) return;
+  if (qs < 0 || qe > a.num_q_tokens || qb > Lb ||
+      static_cast<int64_t>(Lb) > static_cast<int64_t>(a.max_blocks_per_seq) * a.BS) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) record_error(PKV_ERR_BOUNDS, b);
+    return;
+  }
+  const int cb = Lb - qb;
+  int kv_lo = 0x7fffffff, kv_end = 0;
+  int lo_t[2], end_t[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    qt[x].rows = max(0, min(BM, qb - qt[x].q0));
+    if (qt[x].rows > 0) {
+      const int i_first = cb + qt[x].q0, i_last = i_first + qt[x].rows - 1;
+      lo_t[x] = a.window > 0 ? max(0, i_first - a.window + 1) : 0;
+      end_t[x] = i_last + 1;
+      kv_lo = min(kv_lo, lo_t[x]);
+      kv_end = max(kv_end, end_t[x]);
+    }
+  }
+  const int kv_start = kv_lo / BN * BN;
+  const int ntiles = (kv_end - kv_start + BN - 1) / BN;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    if (qt[x].rows > 0) {
+      qt[x].j0 = (lo_t[x] / BN * BN - kv_start) / BN;
+      qt[x].j1 = (end_t[x] - kv_start + BN - 1) / BN;
+    } else {
+      qt[x].j0 = qt[x].j1 = 0;
+    }
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = qt[0].head / a.QPK;
+  const int BS = a.BS;
+  const int TB = BN / BS;
+  const int64_t where = static_cast<int64_t>(b) * a.H + qt[0].head;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::NBAR; ++i)
+      mbar_init(&bars[i], (i == L::B_PF || i == L::B_PF + 1) ? 128 : 1);
+    misc[1] = 0;
+    misc[2] = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&qmap);
+    prefetch_tensormap(&kvmap);
+  }
+  if (warp == 1) tc5::tmem_alloc<512>(misc);
+  tc5::fence_before_sync();
+  __syncthreads();
+  tc5::fence_after_sync();
+  const uint32_t tmem = misc[0];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const int32_t *trow = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+    if (lane == 0) {
+      const int nq = qt[1].rows > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(&bars[L::B_Q], nq * L::TILE);
+      for (int x = 0; x < nq; ++x)
+        for (int r = 0; r < L::NREG; ++r)
+          tc5::tma_load_3d(smem + L::OFF_Q + x * L::TILE + r * L::REG, &qmap, &bars[L::B_Q],
+                           64 * r, qt[x].head, qs + qt[x].q0);
+    }
+    int j = 0;
+    for (; j < ntiles; ++j) {
+      const int s = j % NST;
+      if (j >= NST && !tc_path::warp_wait(&bars[L::B_EMPTY + s], ((j / NST) - 1) & 1, abort_flag,
+                                          where))
+        break;
+      const int kv0 = kv_start + j * BN;
+      int coord = -BS;  // out of range: zero fill
+      if (lane < TB) {
+        const int lb = kv0 / BS + lane;
+        const int p0 = lb * BS;
+        if (p0 < kv_end && p0 + BS > kv_lo) {
+          const int pb = __ldg(trow + lb);
+          if (pb < 0 || pb >= a.num_blocks)
+            record_error(PKV_ERR_BOUNDS, static_cast<int64_t>(b) * a.max_blocks_per_seq + lb);
+          else
+            coord = pb * BS;
+        }
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[L::B_KF + s], L::TILE);
+        mbar_arrive_expect_tx(&bars[L::B_VF + s], L::TILE);
+      }
+      __syncwarp();
+      if (lane < TB) {
+        uint8_t *kd = smem + L::OFF_K + s * L::TILE + lane * BS * 128;
+        uint8_t *vd = smem + L::OFF_V + s * L::TILE + lane * BS * 128;
+        for (int r = 0; r < L::NREG; ++r) {
+          tma_load_4d(kd + r * L::REG, &kvmap, &bars[L::B_KF + s], 64 * r, g, coord, 0);
+          tma_load_4d(vd + r * L::REG, &kvmap, &bars[L::B_VF + s], 64 * r, g, coord, 1);
+        }
+      }
+    }
+    if (lane == 0) misc[2] = static_cast<uint32_t>(j);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t ID_QK = tc5::idesc_f16(tc_path::AB<T>::v, 0, BM, BN);
+    constexpr uint32_t ID_PV = tc5::idesc_f16(tc_path::AB<T>::v, 1, BM, D);
+    bool ok = tc_path::warp_wait(&bars[L::B_Q], 0, abort_flag, where);
+    int k_ready = -1;  // highest key tile known to have landed
+    auto need_k = [&](int j) -> bool {
+      if (j <= k_ready) return true;
+      if (!tc_path::warp_wait(&bars[L::B_KF + j % NST], (j / NST) & 1, abort_flag, where))
+        return false;
+      tc5::fence_after_sync();
+      k_ready = j;
+      return true;
+    };
+    auto qk = [&](int x, int j) {
+      if (lane == 0) {
+        const int s = j % NST;
+        const uint32_t sb = tmem + x * 128;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const int r = k / 4, kk = k % 4;
+          const uint64_t qd =
+              tc5::sdesc_sw128(sbase + L::OFF_Q + x * L::TILE + r * L::REG + kk * 32, 16, 1024);
+          const uint64_t kd =
+              tc5::sdesc_sw128(sbase + L::OFF_K + s * L::TILE + r * L::REG + kk * 32, 16, 1024);
+          tc5::mma_ss(sb, qd, kd, ID_QK, k > 0 ? 1u : 0u);
+        }
+        tc5::commit(&bars[L::B_SF + x]);
+      }
+      __syncwarp();
+    };
+    const int j0A = qt[0].j0, j1A = qt[0].j1, j0B = qt[1].j0, j1B = qt[1].j1;
+    auto active = [&](int x, int j) {
+      return x == 0 ? (j >= j0A && j < j1A) : (j >= j0B && j < j1B);
+    };
+    if (ok && ntiles > 0) {
+      ok = need_k(0);
+      if (ok) {
+        if (active(0, 0)) qk(0, 0);
+        if (active(1, 0)) qk(1, 0);
+      }
+    }
+    int pf_a = 0, pf_b = 0;  // P tiles consumed per query tile
+    // PV of tile x for key tile j, then the look-ahead QK of tile x
+    auto step = [&](int x, int j, int s, int &pf) -> bool {
+      if (active(x, j)) {
+        if (!tc_path::warp_wait(&bars[L::B_PF + x], pf & 1, abort_flag, where)) return false;
+        tc5::fence_after_sync();
+        if (lane == 0) {
+          const uint32_t pb = tmem + x * 128;
+          const uint32_t ob = tmem + 256 + x * 128;
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k) {
+            const uint64_t vd =
+                tc5::sdesc_sw128(sbase + L::OFF_V + s * L::TILE + k * 2048, L::REG, 1024);
+            tc5::mma_ts(ob, pb + k * 8, vd, ID_PV, (pf > 0 || k > 0) ? 1u : 0u);
+          }
+          tc5::commit(&bars[L::B_O + x]);
+        }
+        __syncwarp();
+        ++pf;
+      }
+      if (j + 1 < ntiles && active(x, j + 1)) {
+        if (!need_k(j + 1)) return false;
+        qk(x, j + 1);
+      }
+      return true;
+    };
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const int s = j % NST;
+      if (!tc_path::warp_wait(&bars[L::B_VF + s], (j / NST) & 1, abort_flag, where)) break;
+      // rows past the sequence end: P there is exactly 0, but the cache may
+      // hold non-finite values and 0 * NaN is NaN, so zero those V rows
+      const int kv0 = kv_start + j * BN;
+      const int zr = max(0, Lb - kv0);
+      if (zr < BN) {
+        uint8_t *vt = smem + L::OFF_V + s * L::TILE;
+        const int n16 = (BN - zr) * 8;
+        for (int r = 0; r < L::NREG; ++r)
+          for (int c = lane; c < n16; c += 32)
+            *reinterpret_cast<uint4 *>(vt + r * L::REG + zr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (!step(0, j, s, pf_a) || !step(1, j, s, pf_b)) break;
+      if (lane == 0) tc5::commit(&bars[L::B_EMPTY + s]);
+      __syncwarp();
+    }
+    if (lane == 0) tc5::commit(&bars[L::B_FIN]);
+    __syncwarp();
+    mbar_wait_bounded(&bars[L::B_FIN], 0, where);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int x = warp >= 8 ? 1 : 0;
+    const QTile t = x ? qt[1] : qt[0];
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t sb = tmem + lane_base + x * 128;
+    const uint32_t ob = tmem + lane_base + 256 + x * 128;
+    const int pos = cb + t.q0 + row;
+    const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
+    const float sl2 = a.scale_log2;
+    const float slope = ALIBI ? __ldg(a.alibi + t.head) * kLog2e : 0.f;
+    // running max m: in the log2 domain with ALiBi; in raw-score units
+    // without (then scores are scaled inside the exponent's FMA)
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    const int n = t.j1 - t.j0;
+    for (int k = 0; k < n; ++k) {
+      const int j = t.j0 + k;
+      if (!tc_path::warp_wait(&bars[L::B_SF + x], k & 1, abort_flag, where)) {
+        ok = false;
+        break;
+      }
+      tc5::fence_after_sync();
+      uint32_t raw[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+        tc5::tmem_ld32(sb + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
+      tc5::tmem_ld_wait();
+      const int kv0 = kv_start + j * BN;
+      const bool full = (kv0 + BN - 1 <= pos) && (kv0 >= lo);
+      float mx = -INFINITY;
+      if constexpr (ALIBI) {
+        const float b0 = slope * static_cast<float>(kv0 - pos);
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          float v = fmaf(__uint_as_float(raw[e]), sl2, fmaf(slope, static_cast<float>(e), b0));
+          if (!full && (kv0 + e > pos || kv0 + e < lo)) v = -INFINITY;
+          raw[e] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+      } else {
+        if (!full) {
+#pragma unroll
+          for (int e = 0; e < BN; ++e)
+            if (kv0 + e > pos || kv0 + e < lo) raw[e] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int e = 0; e < BN; ++e) mx = fmaxf(mx, __uint_as_float(raw[e]));
+      }
+      // move the max only when it grows by more than 8 (2^8 in p)
+      float alpha = 1.f;
+      bool resc = false;
+      const float unit = ALIBI ? 1.f : sl2;  // log2 units per unit of m
+      if (m == -INFINITY) {
+        m = mx;
+      } else if ((mx - m) * unit > 8.f) {
+        alpha = fast_exp2((m - mx) * unit);
+        m = mx;
+        resc = true;
+      }
+      const float mu = m == -INFINITY ? 0.f : m * unit;
+      float ps = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p0, p1;
+          if constexpr (ALIBI) {
+            p0 = fast_exp2(__uint_as_float(raw[32 * c + e]) - mu);
+            p1 = fast_exp2(__uint_as_float(raw[32 * c + e + 1]) - mu);
+          } else {
+            p0 = fast_exp2(fmaf(__uint_as_float(raw[32 * c + e]), sl2, -mu));
+            p1 = fast_exp2(fmaf(__uint_as_float(raw[32 * c + e + 1]), sl2, -mu));
+          }
+          ps += p0 + p1;
+          pk[e / 2] = T::from_f2(p0, p1);
+        }
+        tc5::tmem_st16(sb + 16 * c, pk);
+      }
+      l = l * alpha + ps;
+      if (__any_sync(0xffffffffu, resc)) {
+        // O_x holds PV of the previous key tile once it has completed
+        if (!tc_path::warp_wait(&bars[L::B_O + x], (k - 1) & 1, abort_flag, where)) {
+          ok = false;
+          break;
+        }
+        tc5::fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tc5::tmem_ld32(ob + 32 * c, o);
+          tc5::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc5::tmem_st32(ob + 32 * c, o);
+        }
+      }
+      tc5::tmem_st_wait();
+      tc5::fence_before_sync();
+      mbar_arrive(&bars[L::B_PF + x]);
+    }
+    if (ok && n > 0 && tc_path::warp_wait(&bars[L::B_O + x], (n - 1) & 1, abort_flag, where)) {
+      tc5::fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool valid = row < t.rows;
+      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) +
+                                             (static_cast<int64_t>(qs + t.q0 + row) * a.H + t.head) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tc5::tmem_ld32(ob + 32 * c, o);
+        tc5::tmem_ld_wait();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = T::from_f2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[c * 4 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+      }
+    }
+    tc5::fence_before_sync();
+  }
+
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) {
+    mbar_wait_bounded(&bars[L::B_Q], 0, where);
+    const int issued = static_cast<int>(misc[2]);
+    for (int s = 0; s < NST; ++s) {
+      const int t_last = issued - 1 - ((issued - 1 - s) % NST + NST) % NST;
+      if (t_last >= 0 && t_last % NST == s) {
+        mbar_wait_bounded(&bars[L::B_KF + s], (t_last / NST) & 1, where);
+        mbar_wait_bounded(&bars[L::B_VF + s], (t_last / NST) & 1, where);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc5::fence_after_sync();
+    tc5::tmem_dealloc<512>(tmem);
+  }
+}
+
+template <class T, int D, bool ALIBI>
+cudaError_t launch(const PrefillArgs &a, int max_query_len, const CUtensorMap &qmap,
+                   const CUtensorMap &kvmap, cudaStream_t stream) {
+  const size_t smem = Lay<D>::ALLOC;
+  auto kern = prefill_tc2_kernel<T, D, ALIBI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int pair = (a.QPK % 2 == 0) ? 1 : 0;
+  const int tiles = (max_query_len + BM - 1) / BM;
+  dim3 grid(pair ? a.H / 2 : a.H, a.num_seqs, pair ? tiles : (tiles + 1) / 2);
+  kern<<<grid, kThreads, smem, stream>>>(a, qmap, kvmap, pair);
+  return cudaGetLastError();
+}
+
+template <class T, int D>
+cudaError_t launch_any(const PrefillArgs &a, int max_query_len, const CUtensorMap &qmap,
+                       const CUtensorMap &kvmap, cudaStream_t stream) {
+  return a.alibi ? launch<T, D, true>(a, max_query_len, qmap, kvmap, stream)
+                 : launch<T, D, false>(a, max_query_len, qmap, kvmap, stream);
+}
+
+}  // namespace tc2
+
 cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, int num_seqs,
                            const int32_t *cu_q, const int32_t *cu_k, int max_query_len,
                            int max_seq_len, const void *kv_cache, const int32_t *block_tables,
@@ -767,10 +1212,17 @@ cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, i
                           CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+#ifdef PKV_PREFILL_TC1
   if (g.D == 128) return bf ? tc_path::launch<BF16, 128>(a, max_query_len, qmap, kvmap, stream)
                             : tc_path::launch<FP16, 128>(a, max_query_len, qmap, kvmap, stream);
   if (g.D == 64) return bf ? tc_path::launch<BF16, 64>(a, max_query_len, qmap, kvmap, stream)
                            : tc_path::launch<FP16, 64>(a, max_query_len, qmap, kvmap, stream);
+#else
+  if (g.D == 128) return bf ? tc2::launch_any<BF16, 128>(a, max_query_len, qmap, kvmap, stream)
+                            : tc2::launch_any<FP16, 128>(a, max_query_len, qmap, kvmap, stream);
+  if (g.D == 64) return bf ? tc2::launch_any<BF16, 64>(a, max_query_len, qmap, kvmap, stream)
+                           : tc2::launch_any<FP16, 64>(a, max_query_len, qmap, kvmap, stream);
+#endif
   return cudaErrorInvalidValue;
 #endif
 }

@@ -63,6 +63,7 @@ def test_params_validation(lib):
     assert write(_p(block_size=24)) == B.PKV_ERR_UNSUPPORTED
     assert write(_p(dtype=7)) == B.PKV_ERR_UNSUPPORTED
     assert write(_p(scale=float("nan"))) == B.PKV_ERR_INVALID
+    assert write(_p(scale=0.0)) == B.PKV_ERR_INVALID
     assert write(_p(), nb=0) == B.PKV_ERR_INVALID
     assert write(_p(), n=-1) == B.PKV_ERR_INVALID
     assert write(_p(), n=1) == B.PKV_ERR_INVALID      # null pointers
