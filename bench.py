@@ -186,6 +186,25 @@ def algorithmic(w: W.Workload):
     return dec_bytes, flops
 
 
+def profiled_traffic(kernel_src: str, summary: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source has changed since the capture."""
+    import hashlib
+    try:
+        src = os.path.join(HERE, "paged_kv_cache_246_gb300", "csrc", kernel_src)
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        fields = {}
+        for line in open(os.path.join(HERE, "profiles", summary)):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.split()[0] if v.split() else ""
+        if fields.get("source_sha256_16") != digest:
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def step_io_bytes(st: Step):
     h2d = sum(t.numel() * t.element_size() for t in
               (st.query, st.key, st.value, st.slots, st.tables, st.seq_lens))
@@ -378,7 +397,10 @@ def run_ours(args, world, rank, local):
         e2e_value = units / (e2e_ms * 1e-3)
         achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": None,
+                "frac": achieved / hbm,
+                "traffic": profiled_traffic("decode.cu",
+                                            "decode_split_kernel_llama3_8b_decode.md")
+                if cfg == 2 and args.scale_down == 1 else None,
                 "kernel": "paged_attn_decode (split-KV pass + combine)",
                 "peak_kind": peak_kind, "algorithmic_bytes_per_launch": dec_bytes,
                 "avg_launch_ms": dec_ms}
