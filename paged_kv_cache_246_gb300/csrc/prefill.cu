@@ -125,6 +125,34 @@ struct AB<FP16> {
   static constexpr int v = 0;
 };
 
+// Packed fp32 pairs (Blackwell f32x2 FMA/ADD) and the 3-input max: the
+// softmax warps are instruction-bound, and these halve the per-score
+// arithmetic of the scale, offset, max and row-sum steps.
+__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // One query tile of the CTA: head, first row within the sequence, rows,
 // and the half-open range of the CTA's key tiles it needs.
 struct QTile {
@@ -404,25 +432,38 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       tc5::tmem_ld_wait();
       const int kv0 = kv_start + j * BN;
       const bool full = (kv0 + BN - 1 <= pos) && (kv0 >= lo);
-      float mx = -INFINITY;
       if constexpr (ALIBI) {
+        // x = s * scale * log2e + slope * log2e * (j - i), in pairs
         const float b0 = slope * static_cast<float>(kv0 - pos);
+        const unsigned long long sl2x2 = f2pack(sl2, sl2), slope2 = f2pack(slope, slope),
+                                 b0x2 = f2pack(b0, b0);
 #pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          float v = fmaf(__uint_as_float(raw[e]), sl2, fmaf(slope, static_cast<float>(e), b0));
-          if (!full && (kv0 + e > pos || kv0 + e < lo)) v = -INFINITY;
-          raw[e] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+        for (int e = 0; e < BN; e += 2) {
+          const unsigned long long bias =
+              ffma2(slope2, f2pack(static_cast<float>(e), static_cast<float>(e + 1)), b0x2);
+          float v0, v1;
+          f2unpack(ffma2(f2pack(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1])), sl2x2,
+                         bias),
+                   v0, v1);
+          raw[e] = __float_as_uint(v0);
+          raw[e + 1] = __float_as_uint(v1);
         }
-      } else {
-        if (!full) {
-#pragma unroll
-          for (int e = 0; e < BN; ++e)
-            if (kv0 + e > pos || kv0 + e < lo) raw[e] = __float_as_uint(-INFINITY);
-        }
-#pragma unroll
-        for (int e = 0; e < BN; ++e) mx = fmaxf(mx, __uint_as_float(raw[e]));
       }
+      if (!full) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e)
+          if (kv0 + e > pos || kv0 + e < lo) raw[e] = __float_as_uint(-INFINITY);
+      }
+      // 8 independent 3-input max chains, then a small tree
+      float pm[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) pm[q] = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < BN; e += 2)
+        pm[(e / 2) & 7] =
+            fmax3(pm[(e / 2) & 7], __uint_as_float(raw[e]), __uint_as_float(raw[e + 1]));
+      const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                             fmaxf(pm[6], pm[7]));
       // move the max only when it grows by more than 8 (2^8 in p)
       float alpha = 1.f;
       bool resc = false;
@@ -435,26 +476,30 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
         resc = true;
       }
       const float mu = m == -INFINITY ? 0.f : m * unit;
-      float ps = 0.f;
+      // p = 2^(x - mu): with ALiBi x is already scaled; without, the scale is
+      // folded into the pair FMA
+      const unsigned long long mul2 = ALIBI ? f2pack(1.f, 1.f) : f2pack(sl2, sl2);
+      const unsigned long long negmu2 = f2pack(-mu, -mu);
+      unsigned long long ps2[4] = {0ull, 0ull, 0ull, 0ull};  // packed partial sums
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0, p1;
-          if constexpr (ALIBI) {
-            p0 = fast_exp2(__uint_as_float(raw[32 * c + e]) - mu);
-            p1 = fast_exp2(__uint_as_float(raw[32 * c + e + 1]) - mu);
-          } else {
-            p0 = fast_exp2(fmaf(__uint_as_float(raw[32 * c + e]), sl2, -mu));
-            p1 = fast_exp2(fmaf(__uint_as_float(raw[32 * c + e + 1]), sl2, -mu));
-          }
-          ps += p0 + p1;
+          float x0, x1;
+          f2unpack(ffma2(f2pack(__uint_as_float(raw[32 * c + e]),
+                                __uint_as_float(raw[32 * c + e + 1])),
+                         mul2, negmu2),
+                   x0, x1);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          ps2[(e / 2) & 3] = fadd2(ps2[(e / 2) & 3], f2pack(p0, p1));
           pk[e / 2] = T::from_f2(p0, p1);
         }
         tc5::tmem_st16(sb + 16 * c, pk);
       }
-      l = l * alpha + ps;
+      float ps0, ps1;
+      f2unpack(fadd2(fadd2(ps2[0], ps2[1]), fadd2(ps2[2], ps2[3])), ps0, ps1);
+      l = l * alpha + (ps0 + ps1);
       if (__any_sync(0xffffffffu, resc)) {
         // O_x holds PV of the previous key tile once it has completed
         if (!warp_wait(&bars[L::B_O + x], (k - 1) & 1, abort_flag, where)) {
