@@ -29,8 +29,10 @@
 //               softmax runs.  S = Q K^T lands in the tile's TMEM score
 //               buffer; O += P V reads P from TMEM (the "TS" form) and V as an
 //               MN-major 128-byte-swizzled shared-memory operand.  Operand
-//               descriptors are built once and advanced by constants, so the
-//               single issuing thread stays ahead of the tensor core.
+//               descriptors are built once and advanced by constants, and
+//               the role runs on one lane with scalar waits, so the issuing
+//               thread spends as few cycles as possible outside MMAs (the
+//               tensor core's instruction queue is shallow).
 //   warps 4-7   softmax of tile A, warps 8-11 of tile B: thread r owns TMEM
 //               lane r = query row r; scores are loaded 128 at a time, masked
 //               (causal, window, range) only on tiles that need it, the
@@ -302,70 +304,66 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       misc[2] = static_cast<uint32_t>(jk);
       misc[3] = static_cast<uint32_t>(jv);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread: the tensor core's instruction queue is shallow, so every
+    // cycle this thread spends outside an MMA is a cycle the tensor core may
+    // idle.  Waits are scalar; there is no warp-wide synchronisation here.
     constexpr uint32_t ID_QK = tc5::idesc_f16(AB<T>::v, 0, BM, BN);
     constexpr uint32_t ID_PV = tc5::idesc_f16(AB<T>::v, 1, BM, D);
-    bool ok = warp_wait(&bars[L::B_Q], 0, abort_flag, where);
-    int k_ready = -1;  // highest key tile known to have landed
-    auto need_k = [&](int j) -> bool {
-      if (j <= k_ready) return true;
-      if (!warp_wait(&bars[L::B_KF + j % NSTK], (j / NSTK) & 1, abort_flag, where)) return false;
-      tc5::fence_after_sync();
-      k_ready = j;
-      return true;
-    };
     // Operand descriptors are built once; an MMA only adds a compile-time
-    // offset (in 16-byte units) to a base, which keeps this single issuing
-    // thread ahead of the tensor core (a 128x128x16 MMA takes 64 cycles).
+    // offset (in 16-byte units) to a base.
     const uint64_t q_desc = tc5::sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
     const uint64_t k_desc = tc5::sdesc_sw128(sbase + L::OFF_K, 16, 1024);
     const uint64_t v_desc = tc5::sdesc_sw128(sbase + L::OFF_V, L::REG, 1024);
-    auto qk = [&](int x, int j) {
-      if (lane == 0) {
-        const uint64_t qb = q_desc + static_cast<uint64_t>((x * L::TILE) >> 4);
-        const uint64_t kb = k_desc + static_cast<uint64_t>(((j % NSTK) * L::TILE) >> 4);
-        const uint32_t sb = tmem + x * 128;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint64_t off = static_cast<uint64_t>(((k / 4) * L::REG + (k % 4) * 32) >> 4);
-          tc5::mma_ss(sb, qb + off, kb + off, ID_QK, k > 0 ? 1u : 0u);
-        }
-        tc5::commit(&bars[L::B_SF + x]);
-      }
-      __syncwarp();
-    };
     const int j0A = qt[0].j0, j1A = qt[0].j1, j0B = qt[1].j0, j1B = qt[1].j1;
     auto active = [&](int x, int j) {
       return x == 0 ? (j >= j0A && j < j1A) : (j >= j0B && j < j1B);
     };
+    int k_ready = -1;  // highest key tile known to have landed
+    auto need_k = [&](int j) -> bool {
+      if (j <= k_ready) return true;
+      if (!wait_or_abort(&bars[L::B_KF + j % NSTK], (j / NSTK) & 1, abort_flag, where))
+        return false;
+      tc5::fence_after_sync();
+      k_ready = j;
+      return true;
+    };
+    auto qk = [&](int x, int j) {
+      const uint64_t qb = q_desc + static_cast<uint64_t>((x * L::TILE) >> 4);
+      const uint64_t kb = k_desc + static_cast<uint64_t>(((j % NSTK) * L::TILE) >> 4);
+      const uint32_t sb = tmem + x * 128;
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint64_t off = static_cast<uint64_t>(((k / 4) * L::REG + (k % 4) * 32) >> 4);
+        tc5::mma_ss(sb, qb + off, kb + off, ID_QK, k > 0 ? 1u : 0u);
+      }
+      tc5::commit(&bars[L::B_SF + x]);
+    };
+    bool ok = wait_or_abort(&bars[L::B_Q], 0, abort_flag, where);
     if (ok && ntiles > 0) {
       ok = need_k(0);
       if (ok) {
         if (active(0, 0)) qk(0, 0);
         if (active(1, 0)) qk(1, 0);
-        if (lane == 0) tc5::commit(&bars[L::B_EK + 0]);  // K(0) free once its QKs finish
-        __syncwarp();
+        tc5::commit(&bars[L::B_EK + 0]);  // K(0) free once its QKs finish
       }
     }
     int pf_a = 0, pf_b = 0;  // P tiles consumed per query tile
     // PV of tile x for key tile j, then the look-ahead QK of tile x
     auto step = [&](int x, int j, int sv, int &pf) -> bool {
       if (active(x, j)) {
-        if (!warp_wait(&bars[L::B_PF + x], pf & 1, abort_flag, where)) return false;
+        if (!wait_or_abort(&bars[L::B_PF + x], pf & 1, abort_flag, where)) return false;
         tc5::fence_after_sync();
-        if (lane == 0) {
-          const uint32_t pb = tmem + x * 128;
-          const uint32_t ob = tmem + 256 + x * 128;
-          const uint64_t vb = v_desc + static_cast<uint64_t>((sv * L::TILE) >> 4);
-          const uint32_t acc0 = pf > 0 ? 1u : 0u;
+        const uint32_t pb = tmem + x * 128;
+        const uint32_t ob = tmem + 256 + x * 128;
+        const uint64_t vb = v_desc + static_cast<uint64_t>((sv * L::TILE) >> 4);
+        const uint32_t acc0 = pf > 0 ? 1u : 0u;
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k)  // 16 keys = 2048 bytes of V per step
-            tc5::mma_ts(ob, pb + k * 8, vb + static_cast<uint64_t>(k * 128), ID_PV,
-                        k > 0 ? 1u : acc0);
-          tc5::commit(&bars[L::B_O + x]);
-        }
-        __syncwarp();
+        for (int k = 0; k < BN / 16; ++k)  // 16 keys = 2048 bytes of V per step
+          tc5::mma_ts(ob, pb + k * 8, vb + static_cast<uint64_t>(k * 128), ID_PV,
+                      k > 0 ? 1u : acc0);
+        tc5::commit(&bars[L::B_O + x]);
         ++pf;
       }
       if (j + 1 < ntiles && active(x, j + 1)) {
@@ -376,30 +374,27 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     };
     for (int j = 0; ok && j < ntiles; ++j) {
       const int sv = j % NSTV;
-      if (!warp_wait(&bars[L::B_VF + sv], (j / NSTV) & 1, abort_flag, where)) break;
-      // rows past the sequence end: P there is exactly 0, but the cache may
-      // hold non-finite values and 0 * NaN is NaN, so zero those V rows
+      if (!wait_or_abort(&bars[L::B_VF + sv], (j / NSTV) & 1, abort_flag, where)) break;
+      // Positions past the sequence end inside its last cache block hold
+      // whatever the cache holds there (possibly non-finite); their P is
+      // exactly 0, but 0 * NaN is NaN, so those V rows are zeroed before the
+      // PV product reads them.  Whole blocks past the end came in as zeros.
       const int kv0 = kv_start + j * BN;
-      const int zr = max(0, Lb - kv0);
-      if (zr < BN) {
+      const int zr = Lb - kv0;
+      if (zr > 0 && zr < BN && zr % BS != 0) {
+        const int ze = min(BN, (zr / BS + 1) * BS);
         uint8_t *vt = smem + L::OFF_V + sv * L::TILE;
-        const int n16 = (BN - zr) * 8;
         for (int r = 0; r < L::NREG; ++r)
-          for (int c = lane; c < n16; c += 32)
-            *reinterpret_cast<uint4 *>(vt + r * L::REG + zr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          for (int c = zr * 8; c < ze * 8; ++c)
+            *reinterpret_cast<uint4 *>(vt + r * L::REG + c * 16) = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
       }
-      __syncwarp();
       if (!step(0, j, sv, pf_a) || !step(1, j, sv, pf_b)) break;
-      if (lane == 0) {
-        tc5::commit(&bars[L::B_EV + sv]);                              // V(j) free after its PVs
-        if (j + 1 < ntiles) tc5::commit(&bars[L::B_EK + (j + 1) % NSTK]);  // K(j+1) after its QKs
-      }
-      __syncwarp();
+      tc5::commit(&bars[L::B_EV + sv]);                                  // V(j) after its PVs
+      if (j + 1 < ntiles) tc5::commit(&bars[L::B_EK + (j + 1) % NSTK]);  // K(j+1) after its QKs
     }
     // every MMA this thread issued has completed before TMEM is released
-    if (lane == 0) tc5::commit(&bars[L::B_FIN]);
-    __syncwarp();
+    tc5::commit(&bars[L::B_FIN]);
     mbar_wait_bounded(&bars[L::B_FIN], 0, where);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
