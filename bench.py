@@ -410,7 +410,10 @@ def run_ours(args, world, rank, local):
         e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
         achieved = flops / (pre_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_burst, "unit": "TFLOP/s",
-                "frac": achieved / bf16_burst, "traffic": None,
+                "frac": achieved / bf16_burst,
+                "traffic": profiled_traffic("prefill.cu",
+                                            "prefill_tc_kernel_varlen_prefill.md")
+                if cfg == 3 and args.scale_down == 1 else None,
                 "kernel": "paged_attn_prefill_varlen", "peak_kind": peak_kind,
                 "algorithmic_flops_per_launch": flops, "avg_launch_ms": pre_ms,
                 "frac_of_sustained": achieved / bf16_sust}
