@@ -214,6 +214,52 @@ def step_io_bytes(st: Step):
     return h2d, d2h
 
 
+def time_block_moves(st: Step, w: W.Workload, B, args, hbm: float):
+    """kv_copy_blocks and kv_swap_blocks of the workload, timed apart from the
+    step with CUDA events: copy against the HBM roofline (read + write
+    bytes), swap out / in against a same-size contiguous pinned copy in the
+    same direction (the host link), measured here."""
+    stream = torch.cuda.current_stream()
+    block_bytes = 2 * w.kv_cache.shape[2] * w.kv_cache.element_size()   # K and V of one block
+    n_copy, n_swap = int(w.copy_pairs.shape[0]), int(w.swap_pairs.shape[0])
+    pairs_dev = w.copy_pairs.to(st.dev)
+    host = torch.empty((2, n_swap, w.kv_cache.shape[2]), dtype=w.dtype).pin_memory()
+    out_pairs = w.swap_pairs.contiguous()
+    in_pairs = w.swap_pairs[:, [1, 0]].contiguous()
+    flat_dev = torch.empty(n_swap * block_bytes, dtype=torch.uint8, device=st.dev)
+    flat_host = torch.empty(n_swap * block_bytes, dtype=torch.uint8).pin_memory()
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    reps = max(5, min(args.steps, 50))
+    copy_ms = timed(lambda: B.kv_copy_blocks([st.cache], pairs_dev, st.p), reps)
+    out_ms = timed(lambda: B.kv_swap_blocks(st.cache, host, out_pairs, st.p), reps)
+    in_ms = timed(lambda: B.kv_swap_blocks(host, st.cache, in_pairs, st.p), reps)
+    link_out_ms = timed(lambda: flat_host.copy_(flat_dev, non_blocking=True), reps)
+    link_in_ms = timed(lambda: flat_dev.copy_(flat_host, non_blocking=True), reps)
+    B.check_device_error("block moves")
+    copy_gbs = 2 * n_copy * block_bytes / (copy_ms * 1e-3) / 1e9
+    swap_bytes = n_swap * block_bytes
+    gbs = lambda ms: swap_bytes / (ms * 1e-3) / 1e9
+    return {"copy_blocks": {"pairs": n_copy, "ms": copy_ms, "gbs": copy_gbs,
+                            "frac_of_hbm": copy_gbs / hbm},
+            "swap_out": {"blocks": n_swap, "ms": out_ms, "gbs": gbs(out_ms),
+                         "link_gbs": gbs(link_out_ms), "frac_of_link": link_out_ms / out_ms},
+            "swap_in": {"blocks": n_swap, "ms": in_ms, "gbs": gbs(in_ms),
+                        "link_gbs": gbs(link_in_ms), "frac_of_link": link_in_ms / in_ms}}
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -424,6 +470,8 @@ def run_ours(args, world, rank, local):
                  "decode_gbs": dec_bytes / (dec_ms * 1e-3) / 1e9,
                  "decode_frac_of_hbm": dec_bytes / (dec_ms * 1e-3) / 1e9 / hbm}
 
+    block_moves = time_block_moves(st, w, B, args, hbm) if w.copy_pairs.numel() else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r = oracle_rate(w, budget_s=args.cpu_budget)
@@ -448,6 +496,8 @@ def run_ours(args, world, rank, local):
                 "gpu_launches": st.launches_per_step() * args.steps,
                 "cpu_baseline": cpu}
         line.update(extra)
+        if block_moves:
+            line["block_moves"] = block_moves
         print(json.dumps(line), flush=True)
 
 
