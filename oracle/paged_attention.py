@@ -59,7 +59,9 @@ class AttnParams:
 
     Mirrors the constructor arguments of ``XFormersImpl`` (xformers.py) and
     ``TorchSDPABackendImpl`` (cpu_attn): num_heads, head_size, scale,
-    num_kv_heads, alibi_slopes, sliding_window; plus the cache block size.
+    num_kv_heads, alibi_slopes, sliding_window; plus the cache block size and
+    ``causal`` (cpu_attn ``_run_sdpa_forward`` is causal only for decoder
+    attention; encoder and encoder-only attention see the whole sequence).
     """
     num_heads: int
     num_kv_heads: int
@@ -68,6 +70,7 @@ class AttnParams:
     scale: float
     alibi_slopes: Optional[Sequence[float]] = None
     sliding_window: int = 0
+    causal: bool = True
 
     @property
     def queries_per_kv(self) -> int:
@@ -209,28 +212,34 @@ def gather_kv(kv_cache: torch.Tensor, table_row: torch.Tensor, n_tokens: int,
 
 def attend_rows(q: torch.Tensor, positions: Sequence[int], K: torch.Tensor,
                 V: torch.Tensor, scale: float, slope: Optional[float],
-                window: int) -> torch.Tensor:
+                window: int, causal: bool = True) -> torch.Tensor:
     """softmax(scale * q K^T + alibi + mask) V for a set of query rows.
 
     q: [n, D] fp64; positions: query position i of each row; K, V: [L, D]
     fp64 holding positions 0..L-1 of one KV head.  Row r sees keys
     ``window_lo(i) <= j <= i`` (causal; xformers.py BlockDiagonalCausalMask,
     cpu_attn is_causal SDPA), scores ``scale * q.k_j`` (plus
-    ``alibi_bias``), then a softmax and the weighted sum of V.
+    ``alibi_bias``), then a softmax and the weighted sum of V.  With
+    ``causal=False`` (encoder attention, cpu_attn ``_run_sdpa_forward``) every
+    row sees all keys 0..L-1; a window is not defined there.
     """
     n = q.shape[0]
     out = torch.zeros(n, V.shape[1], dtype=F64)
     for r in range(n):
         i = int(positions[r])
-        lo = window_lo(i, window)
-        if i < lo:
+        if causal:
+            lo, hi = window_lo(i, window), i
+        else:
+            assert window <= 0, "a sliding window is only defined for causal attention"
+            lo, hi = 0, K.shape[0] - 1
+        if hi < lo:
             continue  # no key visible: zeros
-        j = torch.arange(lo, i + 1, dtype=F64)
-        s = scale * (K[lo:i + 1] @ q[r])
+        j = torch.arange(lo, hi + 1, dtype=F64)
+        s = scale * (K[lo:hi + 1] @ q[r])
         if slope is not None:
             s = s + alibi_bias(slope, j, i)
         e = torch.exp(s - s.max())
-        out[r] = (e / e.sum()) @ V[lo:i + 1]
+        out[r] = (e / e.sum()) @ V[lo:hi + 1]
     return out
 
 
@@ -341,6 +350,8 @@ def paged_attn_prefill_varlen(query: torch.Tensor, cu_seqlens_q: torch.Tensor,
     forward_prefix).  With c_b = 0 this is the block-diagonal causal prefill
     of _run_memory_efficient_xformers_forward and the per-sequence causal SDPA
     of cpu_attn _run_sdpa_forward.
+    With ``p.causal`` False (encoder / encoder-only attention, cpu_attn
+    ``_run_sdpa_forward`` with is_causal off) row t sees all L_b keys.
     Returns fp64 [num_query_tokens, num_heads * head_size]; rows not listed in
     ``rows`` (if given) are left NaN.
     """
@@ -365,7 +376,7 @@ def paged_attn_prefill_varlen(query: torch.Tensor, cu_seqlens_q: torch.Tensor,
         for h in range(H):
             g = kv_head_of(h, qpk)
             o = attend_rows(q_all[idx, h], pos, K[:, g], V[:, g], p.scale,
-                            _slope(p, h), window)
+                            _slope(p, h), window, p.causal)
             out[idx, h * D:(h + 1) * D] = o
     return out
 

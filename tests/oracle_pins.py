@@ -38,11 +38,11 @@ GOLDEN = os.path.join(HERE, "golden")
 # oracle's own (separately pinned) cache write
 # ---------------------------------------------------------------------------
 
-def _params(H, KVH, D, bs, scale=None, slopes=None, window=0):
+def _params(H, KVH, D, bs, scale=None, slopes=None, window=0, causal=True):
     return O.AttnParams(num_heads=H, num_kv_heads=KVH, head_size=D,
                         block_size=bs,
                         scale=(1.0 / math.sqrt(D)) if scale is None else scale,
-                        alibi_slopes=slopes, sliding_window=window)
+                        alibi_slopes=slopes, sliding_window=window, causal=causal)
 
 
 def paged_from_contiguous(Ks, Vs, p, g, extra_blocks=3, dtype=torch.bfloat16):
@@ -89,6 +89,16 @@ def _prefill(Q, Ks, Vs, qlens, p, g, rows=None):
     lens = [K.shape[0] for K in Ks]
     return O.paged_attn_prefill_varlen(Q, _cu(qlens), _cu(lens), cache, tables,
                                        p, rows=rows)
+
+
+def _sdpa(q, K, V, p, causal):
+    """torch CPU fp64 SDPA with GQA by repeat_interleave; [L, H*D]."""
+    qpk = p.num_heads // p.num_kv_heads
+    qq = q.to(F64).permute(1, 0, 2)[None]
+    kk = K.to(F64).repeat_interleave(qpk, dim=1).permute(1, 0, 2)[None]
+    vv = V.to(F64).repeat_interleave(qpk, dim=1).permute(1, 0, 2)[None]
+    o = F.scaled_dot_product_attention(qq, kk, vv, is_causal=causal, scale=p.scale)
+    return o[0].permute(1, 0, 2).reshape(q.shape[0], -1)
 
 
 def _sdpa_causal(q, K, V, p):
@@ -184,6 +194,25 @@ def pin_prefill_equals_sdpa_causal():
         ref = _sdpa_causal(Q[a:a + L].view(L, p.num_heads, p.head_size), K, V, p)
         _close(out[a:a + L], ref, what=f"prefill L={L}")
         a += L
+
+
+def pin_noncausal_prefill_equals_sdpa():
+    """Encoder attention (cpu_attn _run_sdpa_forward with is_causal off):
+    every row sees the whole sequence."""
+    g = torch.Generator().manual_seed(16)
+    p = _params(H=4, KVH=2, D=16, bs=4, scale=0.3, causal=False)
+    lens = [1, 6, 13]
+    Ks, Vs = _rand_seqs(g, lens, p.num_kv_heads, p.head_size)
+    Q = torch.randn(sum(lens), p.num_heads * p.head_size, generator=g).to(torch.bfloat16)
+    out = _prefill(Q, Ks, Vs, lens, p, g)
+    a = 0
+    for L, K, V in zip(lens, Ks, Vs):
+        ref = _sdpa(Q[a:a + L].view(L, p.num_heads, p.head_size), K, V, p, causal=False)
+        _close(out[a:a + L], ref, what=f"non-causal L={L}")
+        a += L
+    # a chunk of the last rows sees the same full sequence
+    chunk = _prefill(Q[a - 4:a], [Ks[-1]], [Vs[-1]], [4], p, g)
+    _close(chunk, out[a - 4:a], tol=1e-13, what="non-causal chunk")
 
 
 def pin_decode_equals_sdpa_last_row():

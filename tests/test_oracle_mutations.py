@@ -16,13 +16,13 @@ _orig_attend = OP.attend_rows
 
 
 def _attend_variant(drop_scale=False, drop_causal=False, swap_kv=False):
-    def attend(q, positions, K, V, scale, slope, window):
+    def attend(q, positions, K, V, scale, slope, window, causal=True):
         if swap_kv:
             K, V = V, K
         if drop_scale:
             scale = 1.0
         if not drop_causal:
-            return _orig_attend(q, positions, K, V, scale, slope, window)
+            return _orig_attend(q, positions, K, V, scale, slope, window, causal)
         n = q.shape[0]
         out = torch.zeros(n, V.shape[1], dtype=torch.float64)
         for r in range(n):
@@ -68,6 +68,14 @@ def _gather_wrong_block(kv_cache, table_row, n_tokens, p):
 
 _orig_gather = OP.gather_kv
 MUTATIONS["block_table_rotated"] = ("gather_kv", _gather_wrong_block)
+
+
+def _attend_always_causal(q, positions, K, V, scale, slope, window, causal=True):
+    # the non-causal flag ignored: encoder attention would lose its future keys
+    return _orig_attend(q, positions, K, V, scale, slope, window, True)
+
+
+MUTATIONS["noncausal_ignored"] = ("attend_rows", _attend_always_causal)
 
 
 @pytest.mark.parametrize("mutation", sorted(MUTATIONS))
