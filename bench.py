@@ -35,7 +35,7 @@ if HERE not in sys.path:
 from paged_kv_cache_246_gb300 import workloads as W  # noqa: E402
 
 METRIC = ("decode tokens/s and HBM GB/s (%peak); prefill TFLOP/s (%bf16 peak), 1×GB300")
-CFG_OF = {"decode": 2, "prefill": 3, "mixed": 4, "swa": 5}
+CFG_OF = {"decode": 2, "prefill": 3, "mixed": 4, "swa": 5, "encoder": 6}
 
 
 def peaks():
@@ -110,7 +110,7 @@ class Step:
         self.w, self.B, self.dev = w, B, dev
         self.slopes = None if w.alibi_slopes is None else w.alibi_slopes.to(dev)
         self.p = B.make_params(w.num_heads, w.num_kv_heads, w.head_size, w.block_size, w.dtype,
-                               w.scale, self.slopes, w.sliding_window)
+                               w.scale, self.slopes, w.sliding_window, not w.causal)
         self.cache = w.kv_cache.to(dev)
         self.key, self.value = w.key.to(dev), w.value.to(dev)
         self.slots = w.slot_mapping.to(dev)
@@ -180,6 +180,9 @@ def algorithmic(w: W.Workload):
         pairs = 0
         for t in range(q):      # keys visible to query row t
             i = c + t
+            if not w.causal:
+                pairs += L      # encoder attention: the whole sequence
+                continue
             lo = max(0, i - w.sliding_window + 1) if w.sliding_window > 0 else 0
             pairs += i - lo + 1
         flops += 4 * w.num_heads * w.head_size * pairs   # q.k and p.V
@@ -298,7 +301,7 @@ def oracle_rate(w: W.Workload, budget_s: float):
     import oracle as O
     op = O.AttnParams(w.num_heads, w.num_kv_heads, w.head_size, w.block_size, w.scale,
                       None if w.alibi_slopes is None else w.alibi_slopes.tolist(),
-                      w.sliding_window)
+                      w.sliding_window, w.causal)
     ref = w.kv_cache.clone()
     P = w.num_prefill_seqs
     t0 = time.perf_counter()

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 2
 
 typedef struct CUstream_st *pkv_stream_t; /* == cudaStream_t */
 
@@ -79,6 +79,12 @@ typedef enum pkv_dtype { PKV_FP16 = 0, PKV_BF16 = 1 } pkv_dtype;
  *     (xformers.py _make_alibi_bias).
  *   sliding_window: W > 0 keeps keys i - W < j <= i; W <= 0 means none.
  *     It applies together with ALiBi when both are given.
+ *   non_causal: 0 for decoder self-attention (causal); 1 for encoder /
+ *     encoder-only attention, where every query row of a sequence sees all
+ *     of its keys 0 .. L-1 (cpu_attn _run_sdpa_forward runs SDPA causally
+ *     only for decoder attention).  Affects the prefill call; a decode query
+ *     is the last position, so it sees the same keys either way.  A window
+ *     together with non_causal is PKV_ERR_UNSUPPORTED.
  */
 typedef struct pkv_attn_params {
   int32_t num_heads;
@@ -89,6 +95,7 @@ typedef struct pkv_attn_params {
   float scale;
   const float *alibi_slopes;
   int32_t sliding_window;
+  int32_t non_causal;
 } pkv_attn_params;
 
 /*

@@ -39,7 +39,8 @@ class AttnParams(ctypes.Structure):
     _fields_ = [("num_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_size", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("alibi_slopes", ctypes.c_void_p), ("sliding_window", ctypes.c_int32)]
+                ("alibi_slopes", ctypes.c_void_p), ("sliding_window", ctypes.c_int32),
+                ("non_causal", ctypes.c_int32)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -105,7 +106,7 @@ def _need(t: torch.Tensor, name: str, dtype=None, ndim=None, cuda=True) -> None:
 
 def make_params(num_heads: int, num_kv_heads: int, head_size: int, block_size: int,
                 dtype: torch.dtype, scale: float, alibi_slopes: Optional[torch.Tensor] = None,
-                sliding_window: int = 0) -> AttnParams:
+                sliding_window: int = 0, non_causal: bool = False) -> AttnParams:
     """pkv_attn_params; alibi_slopes is a CUDA fp32 tensor [num_heads] or None.
 
     The caller keeps alibi_slopes alive while the params are in use."""
@@ -118,7 +119,7 @@ def make_params(num_heads: int, num_kv_heads: int, head_size: int, block_size: i
             raise ValueError("alibi_slopes must have num_heads entries")
         ptr = alibi_slopes.data_ptr()
     return AttnParams(num_heads, num_kv_heads, head_size, block_size, _DTYPES[dtype],
-                      float(scale), ptr, int(sliding_window or 0))
+                      float(scale), ptr, int(sliding_window or 0), int(bool(non_causal)))
 
 
 def _cache_blocks(kv_cache: torch.Tensor, p: AttnParams) -> int:

@@ -98,6 +98,8 @@ static pkv_status make_geometry(const pkv_attn_params *p, int64_t num_blocks, Ge
   if (num_blocks <= 0) return PKV_ERR_INVALID;
   if (num_blocks * p->block_size > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
   if (p->alibi_slopes && !aligned(p->alibi_slopes, 4)) return PKV_ERR_INVALID;
+  if (p->non_causal != 0 && p->non_causal != 1) return PKV_ERR_INVALID;
+  if (p->non_causal && p->sliding_window > 0) return PKV_ERR_UNSUPPORTED;
   g->H = p->num_heads;
   g->KVH = p->num_kv_heads;
   g->QPK = p->num_heads / p->num_kv_heads;
@@ -107,6 +109,7 @@ static pkv_status make_geometry(const pkv_attn_params *p, int64_t num_blocks, Ge
   g->scale = p->scale;
   g->alibi = p->alibi_slopes;
   g->window = p->sliding_window > 0 ? p->sliding_window : 0;
+  g->non_causal = p->non_causal;
   g->num_blocks = num_blocks;
   g->row_elems = static_cast<int64_t>(g->KVH) * g->D;
   g->block_elems = g->row_elems * g->BS;

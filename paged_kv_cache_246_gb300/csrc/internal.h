@@ -17,6 +17,7 @@ struct Geometry {
   float scale;
   const float *alibi;
   int window;            // <= 0: none
+  int non_causal;        // 1: every query row sees its whole sequence
   int64_t num_blocks;    // blocks per cache half
   int64_t row_elems;     // KVH * D
   int64_t block_elems;   // BS * KVH * D

@@ -5,8 +5,9 @@
 // _run_memory_efficient_xformers_forward; cpu_attn flash_attn_varlen_func):
 // sequence b has L_b = cu_k[b+1] - cu_k[b] tokens of which the last
 // q_b = cu_q[b+1] - cu_q[b] are query rows; row t sits at position
-// i = (L_b - q_b) + t and attends to keys lo(i) <= j <= i of its sequence,
-// all read through the block table:
+// i = (L_b - q_b) + t and attends to keys lo(i) <= j <= i of its sequence
+// (every key 0 <= j < L_b for encoder attention, non_causal), all read
+// through the block table:
 //     s_j = scale * q.k_j + slope_h * (j - i),   out = softmax(s) . V.
 //
 // Design: CTA = two 128-row query tiles sharing every K/V tile: two query
@@ -64,7 +65,7 @@ struct PrefillArgs {
   int64_t num_blocks;
   int64_t num_q_tokens;  // rows of query / out
   int num_seqs, max_blocks_per_seq;
-  int H, KVH, QPK, BS, window;
+  int H, KVH, QPK, BS, window, non_causal;
   float scale_log2;
 };
 
@@ -205,7 +206,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     if (qt[x].rows > 0) {
       const int i_first = cb + qt[x].q0, i_last = i_first + qt[x].rows - 1;
       lo_t[x] = a.window > 0 ? max(0, i_first - a.window + 1) : 0;
-      end_t[x] = i_last + 1;
+      end_t[x] = a.non_causal ? Lb : i_last + 1;  // non-causal: every key
       kv_lo = min(kv_lo, lo_t[x]);
       kv_end = max(kv_end, end_t[x]);
     }
@@ -406,6 +407,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     const uint32_t ob = tmem + lane_base + 256 + x * 128;
     const int pos = cb + t.q0 + row;
     const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
+    const int hi = a.non_causal ? Lb - 1 : pos;  // last visible key
     const float sl2 = a.scale_log2;
     const float slope = ALIBI ? __ldg(a.alibi + t.head) * kLog2e : 0.f;
     // running max m: in the log2 domain with ALiBi; in raw-score units
@@ -426,7 +428,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
         tc5::tmem_ld32(sb + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
       tc5::tmem_ld_wait();
       const int kv0 = kv_start + j * BN;
-      const bool full = (kv0 + BN - 1 <= pos) && (kv0 >= lo);
+      const bool full = (kv0 + BN - 1 <= hi) && (kv0 >= lo);
       if constexpr (ALIBI) {
         // x = s * scale * log2e + slope * log2e * (j - i), in pairs
         const float b0 = slope * static_cast<float>(kv0 - pos);
@@ -447,7 +449,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       if (!full) {
 #pragma unroll
         for (int e = 0; e < BN; ++e)
-          if (kv0 + e > pos || kv0 + e < lo) raw[e] = __float_as_uint(-INFINITY);
+          if (kv0 + e > hi || kv0 + e < lo) raw[e] = __float_as_uint(-INFINITY);
       }
       // 8 independent 3-input max chains, then a small tree
       float pm[8];
@@ -607,6 +609,7 @@ cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, i
   a.QPK = g.QPK;
   a.BS = g.BS;
   a.window = g.window;
+  a.non_causal = g.non_causal;
   a.scale_log2 = g.scale * kLog2e;
   const bool bf = g.dtype == PKV_BF16;
   // Q: (D, H, tokens); cache: (D, KVH, NB * BS tokens, 2 halves); 64-element

@@ -22,6 +22,8 @@ The five named workloads follow the attention-backend pages' metadata
 5. ``swa_long_decode``: bf16, 64 seqs, seq_len in U[16384,32768], window
    4096, then 2048 block copies and a 4096-block swap out to pinned host
    memory and back.
+6. ``encoder_varlen_prefill``: the shape of 3 with non-causal (encoder)
+   attention: every query row sees its whole prompt.
 """
 from __future__ import annotations
 
@@ -60,6 +62,7 @@ class Workload:
     slot_mapping: torch.Tensor               # int64 [T]
     copy_pairs: torch.Tensor = field(default_factory=lambda: torch.empty(0, 2, dtype=torch.int64))
     swap_pairs: torch.Tensor = field(default_factory=lambda: torch.empty(0, 2, dtype=torch.int64))
+    causal: bool = True                      # False: encoder attention
 
     # -- views used by the calls --------------------------------------------
     @property
@@ -131,8 +134,8 @@ def build(*, name: str, g: torch.Generator, dtype: torch.dtype,
           seq_lens, query_lens, num_prefill_seqs: int,
           num_blocks: Optional[int] = None, pool_extra: float = 0.10,
           alibi: bool = False, sliding_window: int = 0,
-          n_copy: int = 0, n_swap: int = 0, fill_cache: bool = True
-          ) -> Workload:
+          n_copy: int = 0, n_swap: int = 0, fill_cache: bool = True,
+          causal: bool = True) -> Workload:
     """Lay out a batch in a paged pool and draw its tensors.
 
     Block placement: the N = sum ceil(seq_len / block_size) blocks the batch
@@ -210,7 +213,8 @@ def build(*, name: str, g: torch.Generator, dtype: torch.dtype,
         seq_lens=seq_lens.to(torch.int32), query_lens=query_lens.to(torch.int32),
         num_prefill_seqs=num_prefill_seqs, block_tables=tables,
         kv_cache=kv_cache, query=query, key=key, value=value,
-        slot_mapping=slots, copy_pairs=copy_pairs, swap_pairs=swap_pairs)
+        slot_mapping=slots, copy_pairs=copy_pairs, swap_pairs=swap_pairs,
+        causal=causal)
 
 
 # ---------------------------------------------------------------------------
@@ -268,17 +272,26 @@ def _swa_long_decode(g, scale_down=1):
                  n_swap=max(1, 4096 // scale_down))
 
 
+def _encoder_varlen_prefill(g, scale_down=1):
+    B = max(1, 16 // scale_down)
+    L = _log_uniform_int(g, B, 128, 8192)
+    return build(name="encoder_varlen_prefill", g=g, dtype=torch.bfloat16,
+                 num_heads=32, num_kv_heads=8, head_size=128, block_size=16,
+                 seq_lens=L, query_lens=L, num_prefill_seqs=B, causal=False)
+
+
 CONFIGS = {
     1: _tiny_decode,
     2: _llama3_8b_decode,
     3: _varlen_prefill,
     4: _mixed_chunked_alibi,
     5: _swa_long_decode,
+    6: _encoder_varlen_prefill,
 }
 
 
 def make_config(index: int, scale_down: int = 1) -> Workload:
-    """Workload ``index`` (1..5) drawn from generator seed 1000 + index.
+    """Workload ``index`` (1..6) drawn from generator seed 1000 + index.
 
     ``scale_down`` > 1 divides the batch counts (not the lengths), for tests
     that want the shape of a workload at a fraction of its size.

@@ -40,7 +40,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pkv_abi_version() == 1
+    assert lib.pkv_abi_version() == 2
+    assert ctypes.sizeof(B.AttnParams) == 40
     for s in range(6):
         assert B.status_string(s)
     assert B.status_string(99) == "unknown status"
@@ -48,7 +49,7 @@ def test_abi_version_and_status_strings(lib):
 
 def _p(**kw):
     base = dict(num_heads=32, num_kv_heads=8, head_size=128, block_size=16, dtype=B.PKV_BF16,
-                scale=0.088, alibi_slopes=None, sliding_window=0)
+                scale=0.088, alibi_slopes=None, sliding_window=0, non_causal=0)
     base.update(kw)
     return B.AttnParams(**base)
 
@@ -64,6 +65,8 @@ def test_params_validation(lib):
     assert write(_p(dtype=7)) == B.PKV_ERR_UNSUPPORTED
     assert write(_p(scale=float("nan"))) == B.PKV_ERR_INVALID
     assert write(_p(scale=0.0)) == B.PKV_ERR_INVALID
+    assert write(_p(non_causal=1, sliding_window=8)) == B.PKV_ERR_UNSUPPORTED
+    assert write(_p(non_causal=2)) == B.PKV_ERR_INVALID
     assert write(_p(), nb=0) == B.PKV_ERR_INVALID
     assert write(_p(), n=-1) == B.PKV_ERR_INVALID
     assert write(_p(), n=1) == B.PKV_ERR_INVALID      # null pointers

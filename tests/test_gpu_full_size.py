@@ -70,6 +70,18 @@ def test_varlen_prefill_full():
     assert_close(out[rows], ref[rows], "varlen_prefill")
 
 
+def test_encoder_varlen_prefill_full():
+    w = W.make_config(6)
+    r = GpuRun(w)
+    ref_cache = _write_and_check(w, r)
+    out = r.prefill()
+    assert_no_device_error("encoder prefill")
+    q, cuq, cuk, bt, _, _ = w.prefill_slices()
+    rows = _sample_rows(cuq, per_seq=2)
+    ref = O.paged_attn_prefill_varlen(q, cuq, cuk, ref_cache, bt, oracle_params(w), rows=rows)
+    assert_close(out[rows], ref[rows], "encoder_varlen_prefill")
+
+
 def test_mixed_chunked_alibi_full():
     w = W.make_config(4)
     r = GpuRun(w)

@@ -19,13 +19,14 @@ if torch.cuda.is_available():
 
 
 def small(seed, *, dtype=torch.bfloat16, H=8, KVH=2, D=128, bs=16, seq_lens, query_lens=None,
-          P=0, alibi=False, window=0, num_blocks=None):
+          P=0, alibi=False, window=0, num_blocks=None, causal=True):
     g = torch.Generator().manual_seed(seed)
     if query_lens is None:
         query_lens = [1] * len(seq_lens)
     return W.build(name=f"case{seed}", g=g, dtype=dtype, num_heads=H, num_kv_heads=KVH,
                    head_size=D, block_size=bs, seq_lens=seq_lens, query_lens=query_lens,
-                   num_prefill_seqs=P, alibi=alibi, sliding_window=window, num_blocks=num_blocks)
+                   num_prefill_seqs=P, alibi=alibi, sliding_window=window, num_blocks=num_blocks,
+                   causal=causal)
 
 
 def rand_lens(seed, n, lo, hi):
@@ -152,6 +153,12 @@ PREFILL_CASES = {
     "block32_qpk1": lambda: chunked(47, [40, 0], [90, 200], bs=32, H=4, KVH=4),
     "qpk8": lambda: chunked(48, [10, 300], [257, 3], H=16, KVH=2),
     "single_row_chunks": lambda: chunked(49, [0, 10, 99, 500], [1, 1, 1, 1]),
+    "noncausal_varlen": lambda: small(51, H=32, KVH=8, causal=False, seq_lens=[1, 17, 129, 300],
+                                      query_lens=[1, 17, 129, 300], P=4),
+    "noncausal_chunked_alibi": lambda: chunked(52, [0, 70, 200], [150, 33, 257], causal=False,
+                                               alibi=True),
+    "noncausal_rowpair_fp16_d64": lambda: chunked(53, [5, 0], [300, 140], causal=False,
+                                                  dtype=torch.float16, D=64, H=3, KVH=3),
 }
 
 
