@@ -36,6 +36,7 @@ Readings taken where the pages are silent (each is listed in the design doc):
 """
 from __future__ import annotations
 
+import bisect
 import math
 from dataclasses import dataclass
 from typing import Optional, Sequence
@@ -50,6 +51,7 @@ __all__ = [
     "lengths_from_cu", "gather_kv", "attend_rows", "paged_attn_decode",
     "paged_attn_prefill_varlen", "decode_split_partials",
     "combine_split_partials", "kv_copy_blocks", "kv_swap_blocks",
+    "e4m3_decode", "e4m3_encode", "fp8_quantize",
 ]
 
 
@@ -71,6 +73,9 @@ class AttnParams:
     alibi_slopes: Optional[Sequence[float]] = None
     sliding_window: int = 0
     causal: bool = True
+    kv_cache_dtype: str = "auto"   # "auto" (model dtype) or "fp8_e4m3"
+    k_scale: float = 1.0           # fp8 cache: key = code * k_scale
+    v_scale: float = 1.0           #            value = code * v_scale
 
     @property
     def queries_per_kv(self) -> int:
@@ -82,6 +87,61 @@ class AttnParams:
     @property
     def row_elems(self) -> int:
         return self.num_kv_heads * self.head_size
+
+
+# ---------------------------------------------------------------------------
+# fp8 cache codes (the kv_cache_dtype / k_scale / v_scale of xformers.py
+# write_to_paged_cache and cpu_attn forward_decode).  Reading taken: the
+# 8-bit format is E4M3 in its "fn" form (sign, 4 exponent bits with bias 7,
+# 3 mantissa bits, no infinities, S.1111.111 is NaN, largest finite 448);
+# a value is stored as the code nearest to x / scale (ties to the even
+# code), saturating at +-448, with x / scale taken in fp32.
+# ---------------------------------------------------------------------------
+
+def e4m3_decode(code: int) -> float:
+    """Value of an E4M3 code, from its bit fields."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** (1 - 7)   # subnormal
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+_E4M3_POS = [e4m3_decode(c) for c in range(0x7F)]   # codes 0x00..0x7E, increasing
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest E4M3 code to x, ties to the even code, saturating at +-448."""
+    if x != x:
+        return 0x7F
+    sign = 0x80 if math.copysign(1.0, x) < 0 else 0x00
+    a = abs(x)
+    if a >= _E4M3_POS[-1]:
+        return sign | 0x7E                        # saturate at 448
+    hi = bisect.bisect_left(_E4M3_POS, a)        # first code with value >= a
+    if _E4M3_POS[hi] == a:
+        return sign | hi
+    lo = hi - 1                                  # value(lo) < a < value(hi)
+    d_lo, d_hi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    if d_lo < d_hi or (d_lo == d_hi and lo % 2 == 0):
+        return sign | lo
+    return sign | hi
+
+
+def fp8_quantize(x: torch.Tensor, scale: float) -> torch.Tensor:
+    """uint8 codes of x / scale (quotient in fp32, then nearest code)."""
+    q = (x.to(torch.float32) / torch.tensor(scale, dtype=torch.float32)).reshape(-1)
+    return torch.tensor([e4m3_encode(float(v)) for v in q.tolist()],
+                        dtype=torch.uint8).view(x.shape)
+
+
+_E4M3_TABLE = torch.tensor([e4m3_decode(c) for c in range(256)], dtype=F64)
+
+
+def _dequant(codes: torch.Tensor, scale: float) -> torch.Tensor:
+    return _E4M3_TABLE[codes.to(torch.int64)] * scale
 
 
 # ---------------------------------------------------------------------------
@@ -120,7 +180,18 @@ def kv_cache_write(key: torch.Tensor, value: torch.Tensor,
     the new key and value are written into the paged cache through
     slot_mapping before any attention runs.  The copy is bitwise (done on
     16-bit integer views).  Negative slots are padding and are skipped.
+    With an fp8 cache (uint8 tensor) the row is stored as E4M3 codes of
+    key / k_scale and value / v_scale.
     """
+    if p.kv_cache_dtype == "fp8_e4m3":
+        for t in range(key.shape[0]):
+            s = int(slot_mapping[t])
+            if s < 0:
+                continue
+            blk, off = slot_location(s, p.block_size)
+            cache_row(kv_cache, 0, blk, off, p).copy_(fp8_quantize(key[t].reshape(-1), p.k_scale))
+            cache_row(kv_cache, 1, blk, off, p).copy_(fp8_quantize(value[t].reshape(-1), p.v_scale))
+        return
     kc = kv_cache.view(torch.int16)
     kb = key.reshape(key.shape[0], -1).view(torch.int16)
     vb = value.reshape(value.shape[0], -1).view(torch.int16)
@@ -205,8 +276,11 @@ def gather_kv(kv_cache: torch.Tensor, table_row: torch.Tensor, n_tokens: int,
         blk = int(table_row[k])
         j0, j1 = k * bs, min((k + 1) * bs, n_tokens)
         for half, dst in ((0, K), (1, V)):
-            rows = kv_cache[half, blk].view(bs, p.num_kv_heads, p.head_size)
-            dst[j0:j1] = rows[:j1 - j0].to(F64)
+            rows = kv_cache[half, blk].view(bs, p.num_kv_heads, p.head_size)[:j1 - j0]
+            if p.kv_cache_dtype == "fp8_e4m3":   # code * scale
+                dst[j0:j1] = _dequant(rows, p.k_scale if half == 0 else p.v_scale)
+            else:
+                dst[j0:j1] = rows.to(F64)
     return K, V
 
 

@@ -437,6 +437,68 @@ def pin_copy_and_swap_round_trip():
         assert torch.equal(back[:, s].view(torch.int16), dev[:, s].view(torch.int16))
 
 
+# ---------------------------------------------------------------------------
+# pins: the fp8 (E4M3) cache codes
+# ---------------------------------------------------------------------------
+
+def pin_e4m3_decode_matches_library():
+    """Every code's value against torch's float8_e4m3fn widening."""
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(F64)
+    mine = torch.tensor([O.e4m3_decode(c) for c in range(256)], dtype=F64)
+    nan = torch.isnan(lib)
+    assert torch.equal(torch.isnan(mine), nan)
+    assert torch.equal(mine[~nan], lib[~nan])
+
+
+def pin_e4m3_encode_matches_library_in_range():
+    """Nearest-even rounding against torch's float8_e4m3fn narrowing, on every
+    code value, every midpoint between neighbours (the ties) and a sweep, all
+    inside +-464 (torch returns NaN beyond; saturation is pinned below)."""
+    vals = sorted({O.e4m3_decode(c) for c in range(0x7F)})
+    mids = [(a + b) / 2 for a, b in zip(vals, vals[1:])]
+    pts = torch.tensor(vals + mids + [464.0], dtype=torch.float32)
+    pts = torch.cat([pts, -pts, torch.linspace(-464, 464, 20001)])
+    lib = pts.to(torch.float8_e4m3fn).view(torch.uint8)
+    mine = torch.tensor([O.e4m3_encode(float(v)) for v in pts.tolist()], dtype=torch.uint8)
+    assert torch.equal(mine, lib)
+
+
+def pin_e4m3_saturation_and_specials():
+    assert O.e4m3_encode(1000.0) == 0x7E and O.e4m3_encode(-1e6) == 0xFE   # +-448
+    assert O.e4m3_encode(float("nan")) == 0x7F
+    assert O.e4m3_encode(-0.0) == 0x80 and O.e4m3_encode(2.0 ** -10) == 0x00
+    assert O.e4m3_decode(0x7E) == 448.0 and O.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def pin_fp8_cache_equals_bf16_cache_of_its_values():
+    """Attention over an fp8 cache (code * scale) equals attention over a bf16
+    cache holding the same, exactly representable, values."""
+    g = torch.Generator().manual_seed(17)
+    H, KVH, D, bs = 4, 2, 16, 4
+    p8 = O.AttnParams(H, KVH, D, bs, 0.25, [0.5, 0.25, 0.1, 0.02], 0, True,
+                      "fp8_e4m3", 0.125, 0.5)
+    pb = O.AttnParams(H, KVH, D, bs, 0.25, [0.5, 0.25, 0.1, 0.02])
+    L = 11
+    tables = torch.tensor([[2, 0, 5]], dtype=torch.int32)
+    slots = torch.tensor([int(tables[0, j // bs]) * bs + j % bs for j in range(L)])
+    key = torch.randn(L, KVH * D, generator=g).to(torch.bfloat16)
+    val = torch.randn(L, KVH * D, generator=g).to(torch.bfloat16)
+    c8 = torch.zeros(2, 6, bs * KVH * D, dtype=torch.uint8)
+    O.kv_cache_write(key, val, c8, slots, p8)
+    # the bf16 cache holds code * scale, computed from the codes' bit fields
+    cb = torch.zeros(2, 6, bs * KVH * D, dtype=torch.bfloat16)
+    for half, sc in ((0, 0.125), (1, 0.5)):
+        vals = torch.tensor([O.e4m3_decode(int(c)) * sc for c in c8[half].reshape(-1)])
+        cb[half] = vals.view(6, -1).to(torch.bfloat16)
+    q = torch.randn(1, H * D, generator=g).to(torch.bfloat16)
+    sl = torch.tensor([L], dtype=torch.int32)
+    a = O.paged_attn_decode(q, c8, tables, sl, p8)
+    b = O.paged_attn_decode(q, cb, tables, sl, pb)
+    _close(a, b, tol=1e-13, what="fp8 vs bf16 cache")
+    # and the codes are the nearest codes of key / k_scale
+    assert int(c8[0].view(6, bs, KVH * D)[2, 0, 0]) == O.e4m3_encode(float(key[0, 0]) / 0.125)
+
+
 def pin_empty_decode_row_is_zero():
     p = _params(H=2, KVH=1, D=4, bs=4)
     cache = torch.randn(2, 2, 16).to(torch.bfloat16)

@@ -78,6 +78,23 @@ def _attend_always_causal(q, positions, K, V, scale, slope, window, causal=True)
 MUTATIONS["noncausal_ignored"] = ("attend_rows", _attend_always_causal)
 
 
+def _encode_truncating(x):
+    # rounds toward zero instead of to nearest
+    if x != x:
+        return 0x7F
+    sign = 0x80 if math.copysign(1.0, x) < 0 else 0
+    a = min(abs(x), 448.0)
+    best = 0
+    for c, v in enumerate(OP._E4M3_POS):
+        if v <= a:
+            best = c
+    return sign | best
+
+
+MUTATIONS["fp8_truncating"] = ("e4m3_encode", _encode_truncating)
+MUTATIONS["fp8_scale_ignored"] = ("_dequant", lambda codes, scale: OP._E4M3_TABLE[codes.to(torch.int64)])
+
+
 @pytest.mark.parametrize("mutation", sorted(MUTATIONS))
 def test_mutation_is_caught(mutation, monkeypatch):
     attr, fn = MUTATIONS[mutation]
