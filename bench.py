@@ -35,7 +35,7 @@ if HERE not in sys.path:
 from paged_kv_cache_246_gb300 import workloads as W  # noqa: E402
 
 METRIC = ("decode tokens/s and HBM GB/s (%peak); prefill TFLOP/s (%bf16 peak), 1×GB300")
-CFG_OF = {"decode": 2, "prefill": 3, "mixed": 4, "swa": 5, "encoder": 6}
+CFG_OF = {"decode": 2, "prefill": 3, "mixed": 4, "swa": 5, "encoder": 6, "decode_fp8": 7}
 
 
 def peaks():
@@ -110,7 +110,8 @@ class Step:
         self.w, self.B, self.dev = w, B, dev
         self.slopes = None if w.alibi_slopes is None else w.alibi_slopes.to(dev)
         self.p = B.make_params(w.num_heads, w.num_kv_heads, w.head_size, w.block_size, w.dtype,
-                               w.scale, self.slopes, w.sliding_window, not w.causal)
+                               w.scale, self.slopes, w.sliding_window, not w.causal,
+                               w.kv_cache_dtype, w.k_scale, w.v_scale)
         self.cache = w.kv_cache.to(dev)
         self.key, self.value = w.key.to(dev), w.value.to(dev)
         self.slots = w.slot_mapping.to(dev)
@@ -167,11 +168,12 @@ def algorithmic(w: W.Workload):
     """Bytes read+written by the decode call and flops of the prefill call."""
     P = w.num_prefill_seqs
     el = 2
+    kv_el = 1 if w.kv_cache_dtype == "fp8_e4m3" else 2   # cache bytes per element
     row = w.num_kv_heads * w.head_size
     dec_bytes = 0
     for L in w.seq_lens[P:].tolist():
         keys = min(L, w.sliding_window) if w.sliding_window > 0 else L
-        dec_bytes += keys * row * el * 2          # K and V of every visible token
+        dec_bytes += keys * row * kv_el * 2       # K and V of every visible token
     nd = w.num_seqs - P
     dec_bytes += nd * w.num_heads * w.head_size * el * 2   # query in, output out
     flops = 0
@@ -301,7 +303,7 @@ def oracle_rate(w: W.Workload, budget_s: float):
     import oracle as O
     op = O.AttnParams(w.num_heads, w.num_kv_heads, w.head_size, w.block_size, w.scale,
                       None if w.alibi_slopes is None else w.alibi_slopes.tolist(),
-                      w.sliding_window, w.causal)
+                      w.sliding_window, w.causal, w.kv_cache_dtype, w.k_scale, w.v_scale)
     ref = w.kv_cache.clone()
     P = w.num_prefill_seqs
     t0 = time.perf_counter()

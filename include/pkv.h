@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 2
+#define PKV_ABI_VERSION 3
 
 typedef struct CUstream_st *pkv_stream_t; /* == cudaStream_t */
 
@@ -64,6 +64,16 @@ typedef enum pkv_status {
 } pkv_status;
 
 typedef enum pkv_dtype { PKV_FP16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Element type of the KV cache: the model dtype, or 8-bit E4M3 codes with a
+ * per-layer scale for keys and one for values (the kv_cache_dtype, k_scale
+ * and v_scale of xformers.py write_to_paged_cache / forward_decode and
+ * cpu_attn forward_decode).  E4M3 is the "fn" form: sign, 4 exponent bits
+ * (bias 7), 3 mantissa bits, no infinities, largest finite 448.  A key x is
+ * stored as the code nearest to x / k_scale (quotient in fp32, ties to the
+ * even code, saturating at +-448) and read back as code * k_scale; values
+ * likewise with v_scale. */
+typedef enum pkv_cache_dtype { PKV_CACHE_AUTO = 0, PKV_CACHE_FP8_E4M3 = 1 } pkv_cache_dtype;
 
 /*
  * Per-layer attention constants: the constructor arguments of
@@ -85,6 +95,11 @@ typedef enum pkv_dtype { PKV_FP16 = 0, PKV_BF16 = 1 } pkv_dtype;
  *     only for decoder attention).  Affects the prefill call; a decode query
  *     is the last position, so it sees the same keys either way.  A window
  *     together with non_causal is PKV_ERR_UNSUPPORTED.
+ *   kv_cache_dtype: pkv_cache_dtype.  With PKV_CACHE_FP8_E4M3 the cache holds
+ *     one byte per element ([2][num_blocks][block_size * num_kv_heads *
+ *     head_size] codes) and k_scale, v_scale (finite, > 0) apply; the write,
+ *     decode, copy and swap calls support it; prefill over an fp8 cache
+ *     returns PKV_ERR_UNSUPPORTED.
  */
 typedef struct pkv_attn_params {
   int32_t num_heads;
@@ -96,6 +111,9 @@ typedef struct pkv_attn_params {
   const float *alibi_slopes;
   int32_t sliding_window;
   int32_t non_causal;
+  int32_t kv_cache_dtype; /* pkv_cache_dtype */
+  float k_scale;
+  float v_scale;
 } pkv_attn_params;
 
 /*

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
 
 PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_BOUNDS, PKV_ERR_TIMEOUT = range(6)
 PKV_FP16, PKV_BF16 = 0, 1
+PKV_CACHE_AUTO, PKV_CACHE_FP8_E4M3 = 0, 1
 _DTYPES = {torch.float16: PKV_FP16, torch.bfloat16: PKV_BF16}
 
 # Every function include/pkv.h declares.
@@ -40,7 +41,8 @@ class AttnParams(ctypes.Structure):
                 ("head_size", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("alibi_slopes", ctypes.c_void_p), ("sliding_window", ctypes.c_int32),
-                ("non_causal", ctypes.c_int32)]
+                ("non_causal", ctypes.c_int32), ("kv_cache_dtype", ctypes.c_int32),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -106,10 +108,16 @@ def _need(t: torch.Tensor, name: str, dtype=None, ndim=None, cuda=True) -> None:
 
 def make_params(num_heads: int, num_kv_heads: int, head_size: int, block_size: int,
                 dtype: torch.dtype, scale: float, alibi_slopes: Optional[torch.Tensor] = None,
-                sliding_window: int = 0, non_causal: bool = False) -> AttnParams:
+                sliding_window: int = 0, non_causal: bool = False,
+                kv_cache_dtype: str = "auto", k_scale: float = 1.0,
+                v_scale: float = 1.0) -> AttnParams:
     """pkv_attn_params; alibi_slopes is a CUDA fp32 tensor [num_heads] or None.
+    kv_cache_dtype "auto" (the model dtype) or "fp8_e4m3" (uint8 cache of
+    E4M3 codes with k_scale / v_scale).
 
     The caller keeps alibi_slopes alive while the params are in use."""
+    if kv_cache_dtype not in ("auto", "fp8_e4m3"):
+        raise ValueError(f"unsupported kv_cache_dtype {kv_cache_dtype}")
     if dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {dtype}")
     ptr = None
@@ -119,7 +127,9 @@ def make_params(num_heads: int, num_kv_heads: int, head_size: int, block_size: i
             raise ValueError("alibi_slopes must have num_heads entries")
         ptr = alibi_slopes.data_ptr()
     return AttnParams(num_heads, num_kv_heads, head_size, block_size, _DTYPES[dtype],
-                      float(scale), ptr, int(sliding_window or 0), int(bool(non_causal)))
+                      float(scale), ptr, int(sliding_window or 0), int(bool(non_causal)),
+                      PKV_CACHE_FP8_E4M3 if kv_cache_dtype == "fp8_e4m3" else PKV_CACHE_AUTO,
+                      float(k_scale), float(v_scale))
 
 
 def _cache_blocks(kv_cache: torch.Tensor, p: AttnParams) -> int:
@@ -127,6 +137,8 @@ def _cache_blocks(kv_cache: torch.Tensor, p: AttnParams) -> int:
         raise ValueError("kv_cache must be [2, num_blocks, block_size*num_kv_heads*head_size]")
     if kv_cache.shape[2] != p.block_size * p.num_kv_heads * p.head_size:
         raise ValueError("kv_cache block size does not match params")
+    if kv_cache.element_size() != (1 if p.kv_cache_dtype == PKV_CACHE_FP8_E4M3 else 2):
+        raise ValueError("kv_cache element size does not match kv_cache_dtype")
     return int(kv_cache.shape[1])
 
 
@@ -140,8 +152,9 @@ def kv_cache_write(key: torch.Tensor, value: torch.Tensor, kv_cache: torch.Tenso
     row = params.num_kv_heads * params.head_size
     if key.numel() != T * row or value.numel() != T * row or slot_mapping.numel() != T:
         raise ValueError("key/value/slot_mapping sizes disagree")
-    if key.dtype != kv_cache.dtype or value.dtype != kv_cache.dtype:
-        raise ValueError("key/value dtype must match the cache")
+    cache_dtype = torch.uint8 if params.kv_cache_dtype == PKV_CACHE_FP8_E4M3 else key.dtype
+    if value.dtype != key.dtype or kv_cache.dtype != cache_dtype:
+        raise ValueError("key/value dtype must match each other and the cache")
     _check(lib().kv_cache_write(key.data_ptr(), value.data_ptr(), T, kv_cache.data_ptr(), nb,
                                 slot_mapping.data_ptr(), ctypes.byref(params), _stream(stream)),
            "kv_cache_write")

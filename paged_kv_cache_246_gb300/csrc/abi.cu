@@ -100,6 +100,12 @@ static pkv_status make_geometry(const pkv_attn_params *p, int64_t num_blocks, Ge
   if (p->alibi_slopes && !aligned(p->alibi_slopes, 4)) return PKV_ERR_INVALID;
   if (p->non_causal != 0 && p->non_causal != 1) return PKV_ERR_INVALID;
   if (p->non_causal && p->sliding_window > 0) return PKV_ERR_UNSUPPORTED;
+  if (p->kv_cache_dtype != PKV_CACHE_AUTO && p->kv_cache_dtype != PKV_CACHE_FP8_E4M3)
+    return PKV_ERR_UNSUPPORTED;
+  const bool fp8 = p->kv_cache_dtype == PKV_CACHE_FP8_E4M3;
+  if (fp8 && (!std::isfinite(p->k_scale) || !std::isfinite(p->v_scale) || p->k_scale <= 0.f ||
+              p->v_scale <= 0.f))
+    return PKV_ERR_INVALID;
   g->H = p->num_heads;
   g->KVH = p->num_kv_heads;
   g->QPK = p->num_heads / p->num_kv_heads;
@@ -113,6 +119,12 @@ static pkv_status make_geometry(const pkv_attn_params *p, int64_t num_blocks, Ge
   g->num_blocks = num_blocks;
   g->row_elems = static_cast<int64_t>(g->KVH) * g->D;
   g->block_elems = g->row_elems * g->BS;
+  g->fp8 = fp8;
+  g->k_scale = fp8 ? p->k_scale : 1.f;
+  g->v_scale = fp8 ? p->v_scale : 1.f;
+  g->elem_bytes = fp8 ? 1 : 2;
+  g->row_bytes = g->row_elems * g->elem_bytes;
+  g->block_bytes = g->block_elems * g->elem_bytes;
   return PKV_OK;
 }
 
@@ -234,6 +246,7 @@ pkv_status paged_attn_prefill_varlen(void *out, const void *query, int64_t num_q
   Geometry g;
   pkv_status st = make_geometry(params, num_blocks, &g);
   if (st != PKV_OK) return st;
+  if (g.fp8) return PKV_ERR_UNSUPPORTED;
   if (num_seqs < 0 || num_seqs > 65535 || max_query_len < 0 || max_seq_len < 0 ||
       max_blocks_per_seq <= 0 || num_query_tokens < 0 || num_query_tokens > 0x7fffffffLL)
     return PKV_ERR_INVALID;

@@ -26,6 +26,8 @@
 //  * Warps merge through shared memory; a single split writes the output,
 //    several splits write (o, m, l) partials that decode_combine_kernel
 //    merges (flash-decoding).
+#include <cuda_fp8.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -50,7 +52,8 @@ struct DecodeArgs {
   int num_seqs, max_blocks_per_seq;
   int H, QPK, head_groups;  // head_groups = QPK / QT
   int BS, window, split_blocks, max_splits, stages;
-  float scale_log2;
+  float scale_log2;  // scale * log2(e) (* k_scale for an fp8 cache)
+  float v_scale;     // 1, or the fp8 cache's value scale
 };
 
 struct SeqSpan {
@@ -129,8 +132,24 @@ __device__ __forceinline__ void reduce_over_dg(float *v, int lane) {
   halve<(NV >= 4 ? NV / 4 : 1), 1>(v, lane);
 }
 
-// T: element type; D: head size; QT: query heads per CTA (<= 4).
-template <class T, int D, int QT>
+// Eight / four / two E4M3 cache codes (low byte first) widened to fp32.
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+      static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+__device__ __forceinline__ void load_chunk8_f32(const uint2 &u, float (&f)[8]) {
+  float2 t;
+  t = e4m3x2_to_f2(u.x); f[0] = t.x; f[1] = t.y;
+  t = e4m3x2_to_f2(u.x >> 16); f[2] = t.x; f[3] = t.y;
+  t = e4m3x2_to_f2(u.y); f[4] = t.x; f[5] = t.y;
+  t = e4m3x2_to_f2(u.y >> 16); f[6] = t.x; f[7] = t.y;
+}
+
+// T: element type of queries / outputs; D: head size; QT: query heads per
+// CTA (<= 4); KV8: the cache holds E4M3 codes (k_scale is folded into the
+// query scale, v_scale applied to the merged output).
+template <class T, int D, int QT, bool KV8>
 __global__ void __launch_bounds__(kDecThreads, 3)
 decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
   constexpr int CPL = D / 64;  // 8-element chunks per lane per token (q.k)
@@ -147,7 +166,8 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
   const int BS = a.BS;
   const int nst = a.stages;
   const int tile_elems = BS * D;
-  const uint32_t tile_bytes = static_cast<uint32_t>(tile_elems) * 2u;
+  constexpr int EB = KV8 ? 1 : 2;  // cache bytes per element
+  const uint32_t tile_bytes = static_cast<uint32_t>(tile_elems) * EB;
 
   const SeqSpan sp = seq_span(a, b, split == 0 && blockIdx.y == 0 && threadIdx.x == 0);
   const int H = a.H;
@@ -164,7 +184,7 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
   const int nb_split = blk_end - blk_begin;
 
   // ---- shared memory carve-up -------------------------------------------
-  uint16_t *tiles = reinterpret_cast<uint16_t *>(smem);  // [warp][stage][K,V][tile]
+  uint8_t *tiles = smem;  // [warp][stage][K,V][tile]
   float *sP = reinterpret_cast<float *>(smem + static_cast<size_t>(kDecWarps) * nst * 2 * tile_bytes);
   int32_t *sTable = reinterpret_cast<int32_t *>(sP + kDecWarps * kSub * QT);
   uint64_t *bars = reinterpret_cast<uint64_t *>(
@@ -190,14 +210,14 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 
   // ---- this warp's blocks: k-th is split block warp + 4k -------------------
   const int my_count = nb_split > warp ? (nb_split - warp + kDecWarps - 1) / kDecWarps : 0;
-  uint16_t *wtiles = tiles + static_cast<size_t>(warp) * nst * 2 * tile_elems;
+  uint8_t *wtiles = tiles + static_cast<size_t>(warp) * nst * 2 * tile_bytes;
   auto issue = [&](int k) {
     const int st = k % nst;
     const int pb = sTable[warp + k * kDecWarps];
     mbar_arrive_expect_tx(&wbar[st], 2u * tile_bytes);
-    uint16_t *kt = wtiles + static_cast<size_t>(st) * 2 * tile_elems;
+    uint8_t *kt = wtiles + static_cast<size_t>(st) * 2 * tile_bytes;
     tma_load_4d(kt, &tmap, &wbar[st], 0, kvh, pb * BS, 0);
-    tma_load_4d(kt + tile_elems, &tmap, &wbar[st], 0, kvh, pb * BS, 1);
+    tma_load_4d(kt + tile_bytes, &tmap, &wbar[st], 0, kvh, pb * BS, 1);
   };
   int issued = 0;
   if (lane == 0) {
@@ -255,8 +275,8 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
       break;
     }
     consumed = k + 1;
-    const uint16_t *kt = wtiles + static_cast<size_t>(st) * 2 * tile_elems;
-    const uint16_t *vt = kt + tile_elems;
+    const uint8_t *kt = wtiles + static_cast<size_t>(st) * 2 * tile_bytes;
+    const uint8_t *vt = kt + tile_bytes;
     const int blk = blk_begin + warp + k * kDecWarps;  // logical block
     for (int sub = 0; sub < BS; sub += kSub) {
       const int j0 = blk * BS + sub;  // position of the sub-tile's token 0
@@ -267,7 +287,8 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
       // tokens it*4 + ts over its dims, index it * QT + h ---------------------
       constexpr int NV = (kSub / 4) * QT;  // partial dots per lane
       float v[NV];
-      const uint4 *k4 = reinterpret_cast<const uint4 *>(kt + sub * D);
+      const uint4 *k4 = reinterpret_cast<const uint4 *>(kt + sub * D * EB);
+      const uint2 *k2 = reinterpret_cast<const uint2 *>(kt + sub * D * EB);
 #pragma unroll
       for (int it = 0; it < kSub / 4; ++it) {
         const int tok = it * 4 + ts;
@@ -276,7 +297,10 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           float f[8];
-          load_chunk_f32<T>(k4[tok * ROWC + c * 8 + dg], f);
+          if constexpr (KV8)
+            load_chunk8_f32(k2[tok * ROWC + c * 8 + dg], f);
+          else
+            load_chunk_f32<T>(k4[tok * ROWC + c * 8 + dg], f);
 #pragma unroll
           for (int h = 0; h < QT; ++h)
 #pragma unroll
@@ -336,15 +360,23 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
         for (int e = 0; e < DPL; ++e) o[h][e] *= alpha[h];
       __syncwarp();
       // ---- p.V over the valid tokens ---------------------------------------
-      const uint16_t *vrow = vt + sub * D + lane * DPL;
+      const uint8_t *vrow = vt + (sub * D + lane * DPL) * EB;
       for (int tok = t_lo; tok < t_hi; ++tok) {
         float vf[DPL];
-        if constexpr (DPL == 4) {
-          const uint2 u = *reinterpret_cast<const uint2 *>(vrow + tok * D);
+        if constexpr (KV8 && DPL == 4) {
+          const uint32_t u = *reinterpret_cast<const uint32_t *>(vrow + tok * D);
+          float2 t0 = e4m3x2_to_f2(u), t1 = e4m3x2_to_f2(u >> 16);
+          vf[0] = t0.x; vf[1] = t0.y; vf[2] = t1.x; vf[3] = t1.y;
+        } else if constexpr (KV8) {
+          const uint32_t u = *reinterpret_cast<const uint16_t *>(vrow + tok * D);
+          float2 t0 = e4m3x2_to_f2(u);
+          vf[0] = t0.x; vf[1] = t0.y;
+        } else if constexpr (DPL == 4) {
+          const uint2 u = *reinterpret_cast<const uint2 *>(vrow + tok * D * 2);
           float2 t0 = T::to_f2(u.x), t1 = T::to_f2(u.y);
           vf[0] = t0.x; vf[1] = t0.y; vf[2] = t1.x; vf[3] = t1.y;
         } else {
-          const uint32_t u = *reinterpret_cast<const uint32_t *>(vrow + tok * D);
+          const uint32_t u = *reinterpret_cast<const uint32_t *>(vrow + tok * D * 2);
           float2 t0 = T::to_f2(u);
           vf[0] = t0.x; vf[1] = t0.y;
         }
@@ -411,7 +443,7 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
       num = fmaf(e, sO[(w * QT + h) * D + d], num);
       den = fmaf(e, sL[w * QT + h], den);
     }
-    const float val = num / den;
+    const float val = num / den * a.v_scale;
     const int64_t hh = static_cast<int64_t>(b) * H + head0 + h;
     if (single) {
       uint16_t *o16 = static_cast<uint16_t *>(a.out);
@@ -456,8 +488,8 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
 // ---------------------------------------------------------------------------
 static int stages_for(int BS) { return BS <= 16 ? 2 : 1; }
 
-static size_t split_smem_bytes(int BS, int D, int QT, int split_blocks) {
-  const size_t tiles = static_cast<size_t>(kDecWarps) * stages_for(BS) * 2 * BS * D * 2;
+static size_t split_smem_bytes(int BS, int D, int QT, int split_blocks, int eb) {
+  const size_t tiles = static_cast<size_t>(kDecWarps) * stages_for(BS) * 2 * BS * D * eb;
   const size_t p = static_cast<size_t>(kDecWarps) * kSub * QT * 4;
   const size_t table = ((split_blocks * 4 + 15) / 16) * 16;
   const size_t bars = static_cast<size_t>(kDecWarps) * stages_for(BS) * 8;
@@ -496,11 +528,11 @@ DecodePlan plan_decode(int num_seqs, int max_seq_len, const Geometry &g, int sms
   return p;
 }
 
-template <class T, int D, int QT>
+template <class T, int D, int QT, bool KV8>
 static cudaError_t launch_typed(const DecodeArgs &a, const CUtensorMap &tmap, int KVH, int num_seqs,
                                 cudaStream_t stream) {
-  const size_t smem = split_smem_bytes(a.BS, D, QT, a.split_blocks);
-  auto kern = decode_split_kernel<T, D, QT>;
+  const size_t smem = split_smem_bytes(a.BS, D, QT, a.split_blocks, KV8 ? 1 : 2);
+  auto kern = decode_split_kernel<T, D, QT, KV8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -521,12 +553,15 @@ cudaError_t launch_decode(void *out, const void *query, int num_seqs, const void
   CUtensorMap tmap;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.D), static_cast<cuuint64_t>(g.KVH),
                               static_cast<cuuint64_t>(g.num_blocks * g.BS), 2};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.D) * 2,
-                                 static_cast<cuuint64_t>(g.row_elems) * 2,
-                                 static_cast<cuuint64_t>(g.num_blocks * g.block_elems) * 2};
+  const cuuint64_t eb = static_cast<cuuint64_t>(g.elem_bytes);
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.D) * eb,
+                                 static_cast<cuuint64_t>(g.row_elems) * eb,
+                                 static_cast<cuuint64_t>(g.num_blocks * g.block_elems) * eb};
   const cuuint32_t box[4] = {static_cast<cuuint32_t>(g.D), 1, static_cast<cuuint32_t>(g.BS), 1};
   const CUtensorMapDataType dt =
-      g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      g.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+            : (g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   if (encode_tensor_map(&tmap, dt, 4, const_cast<void *>(kv_cache), dims, strides, box,
                         CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
@@ -552,12 +587,14 @@ cudaError_t launch_decode(void *out, const void *query, int num_seqs, const void
   a.split_blocks = plan.split_blocks;
   a.max_splits = plan.max_splits;
   a.stages = stages_for(g.BS);
-  a.scale_log2 = g.scale * kLog2e;
+  a.scale_log2 = g.scale * kLog2e * g.k_scale;
+  a.v_scale = g.v_scale;
 
   const bool bf = g.dtype == PKV_BF16;
-#define PKV_DEC(TT, DD, QQ)                                              \
-  if (g.D == DD && QT == QQ)                                             \
-    return launch_typed<TT, DD, QQ>(a, tmap, g.KVH, num_seqs, stream);
+#define PKV_DEC(TT, DD, QQ)                                                    \
+  if (g.D == DD && QT == QQ)                                                   \
+    return g.fp8 ? launch_typed<TT, DD, QQ, true>(a, tmap, g.KVH, num_seqs, stream) \
+                 : launch_typed<TT, DD, QQ, false>(a, tmap, g.KVH, num_seqs, stream);
   if (bf) {
     PKV_DEC(BF16, 128, 4) PKV_DEC(BF16, 128, 2) PKV_DEC(BF16, 128, 1)
     PKV_DEC(BF16, 64, 4) PKV_DEC(BF16, 64, 2) PKV_DEC(BF16, 64, 1)

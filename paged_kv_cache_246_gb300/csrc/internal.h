@@ -21,6 +21,11 @@ struct Geometry {
   int64_t num_blocks;    // blocks per cache half
   int64_t row_elems;     // KVH * D
   int64_t block_elems;   // BS * KVH * D
+  bool fp8;              // cache holds E4M3 codes (1 byte per element)
+  float k_scale, v_scale;
+  int64_t elem_bytes;    // of the cache: 2, or 1 for fp8
+  int64_t row_bytes;     // one token row of the cache
+  int64_t block_bytes;   // one block of one cache half
 };
 
 // Streams/devices: the SM count and opt-in shared memory of the current device.

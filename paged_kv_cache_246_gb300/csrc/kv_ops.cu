@@ -4,6 +4,8 @@
 // All three are pure 16-byte vector copies.  Rows (KVH * D elements) and
 // blocks (BS * KVH * D elements) are multiples of 16 bytes for every
 // supported head size, so every access is an aligned uint4.
+#include <cuda_fp8.h>
+
 #include <algorithm>
 #include <vector>
 
@@ -39,11 +41,66 @@ kv_write_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value, 
   }
 }
 
+// fp8 cache: thread i produces 16-byte chunk (i % row_chunks) of codes of
+// token (i / row_chunks), from 16 input elements: code = nearest E4M3 to
+// x / scale (IEEE fp32 division, round to nearest even, saturating at 448).
+template <class T>
+__device__ __forceinline__ uint32_t quant4(uint2 in, float scale) {
+  float2 a = T::to_f2(in.x), b = T::to_f2(in.y);
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+      make_float2(__fdiv_rn(a.x, scale), __fdiv_rn(a.y, scale)), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+      make_float2(__fdiv_rn(b.x, scale), __fdiv_rn(b.y, scale)), __NV_SATFINITE, __NV_E4M3);
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+template <class T>
+__global__ void __launch_bounds__(256)
+kv_write_fp8_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                    int64_t num_tokens, uint4 *__restrict__ k_half, uint4 *__restrict__ v_half,
+                    const int64_t *__restrict__ slots, int64_t num_slots, int row_chunks,
+                    float k_scale, float v_scale) {
+  const int64_t total = num_tokens * row_chunks;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int64_t t = i / row_chunks;
+    const int64_t c = i - t * row_chunks;
+    const int64_t s = __ldg(slots + t);
+    if (s < 0) continue;  // padding token
+    if (s >= num_slots) {
+      record_error(PKV_ERR_BOUNDS, t);
+      continue;
+    }
+    const uint4 k0 = __ldg(key + 2 * i), k1 = __ldg(key + 2 * i + 1);
+    const uint4 v0 = __ldg(value + 2 * i), v1 = __ldg(value + 2 * i + 1);
+    k_half[s * row_chunks + c] =
+        make_uint4(quant4<T>(make_uint2(k0.x, k0.y), k_scale), quant4<T>(make_uint2(k0.z, k0.w), k_scale),
+                   quant4<T>(make_uint2(k1.x, k1.y), k_scale), quant4<T>(make_uint2(k1.z, k1.w), k_scale));
+    v_half[s * row_chunks + c] =
+        make_uint4(quant4<T>(make_uint2(v0.x, v0.y), v_scale), quant4<T>(make_uint2(v0.z, v0.w), v_scale),
+                   quant4<T>(make_uint2(v1.x, v1.y), v_scale), quant4<T>(make_uint2(v1.z, v1.w), v_scale));
+  }
+}
+
 cudaError_t launch_kv_write(const void *key, const void *value, int64_t num_tokens, void *kv_cache,
                             const int64_t *slot_mapping, const Geometry &g, cudaStream_t stream) {
   DeviceInfo dev;
   cudaError_t e = current_device_info(&dev);
   if (e != cudaSuccess) return e;
+  if (g.fp8) {
+    const int row_chunks = static_cast<int>(g.row_bytes / 16);  // 16 codes per chunk
+    const int64_t num_slots = g.num_blocks * g.BS;
+    uint4 *k_half = static_cast<uint4 *>(kv_cache);
+    uint4 *v_half = k_half + num_slots * row_chunks;
+    const int64_t total = num_tokens * row_chunks;
+    const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, int64_t(dev.sms) * 8));
+    auto kern = g.dtype == PKV_BF16 ? kv_write_fp8_kernel<BF16> : kv_write_fp8_kernel<FP16>;
+    kern<<<blocks, 256, 0, stream>>>(static_cast<const uint4 *>(key),
+                                     static_cast<const uint4 *>(value), num_tokens, k_half, v_half,
+                                     slot_mapping, num_slots, row_chunks, g.k_scale, g.v_scale);
+    return cudaGetLastError();
+  }
   const int row_chunks = static_cast<int>(g.row_elems * 2 / 16);
   const int64_t num_slots = g.num_blocks * g.BS;
   uint4 *k_half = static_cast<uint4 *>(kv_cache);
@@ -102,7 +159,7 @@ cudaError_t launch_kv_copy(void *const *caches, int num_layers, const int64_t *p
   LayerPtrs lp;
   for (int l = 0; l < kMaxLayers; ++l)
     lp.p[l] = l < num_layers ? static_cast<uint4 *>(caches[l]) : nullptr;
-  const int64_t block_chunks = g.block_elems * 2 / 16;
+  const int64_t block_chunks = g.block_bytes / 16;
   // grid.x may go up to 2^31-1: pairs beyond that are split over launches
   const int64_t max_x = 0x7fffffff;
   for (int64_t a = 0; a < num_pairs; a += max_x) {
@@ -143,7 +200,7 @@ kv_swap_kernel(const uint4 *__restrict__ src, int64_t src_half, uint4 *__restric
 cudaError_t launch_kv_swap(const void *src, int64_t src_blocks, void *dst, int64_t dst_blocks,
                            const int64_t *pairs_host, int64_t num_pairs, const Geometry &g,
                            cudaStream_t stream) {
-  const int64_t block_chunks = g.block_elems * 2 / 16;
+  const int64_t block_chunks = g.block_bytes / 16;
   SwapPairs pp;
   for (int64_t a = 0; a < num_pairs; a += kSwapChunk) {
     const int n = static_cast<int>(std::min<int64_t>(kSwapChunk, num_pairs - a));

@@ -24,6 +24,9 @@ The five named workloads follow the attention-backend pages' metadata
    memory and back.
 6. ``encoder_varlen_prefill``: the shape of 3 with non-causal (encoder)
    attention: every query row sees its whole prompt.
+7. ``llama3_8b_decode_fp8``: the shape of 2 with an fp8 (E4M3) cache,
+   k_scale = v_scale = 0.02 (N(0,1) keys and values map to codes of up to
+   about +-250, inside E4M3's +-448).
 """
 from __future__ import annotations
 
@@ -63,6 +66,9 @@ class Workload:
     copy_pairs: torch.Tensor = field(default_factory=lambda: torch.empty(0, 2, dtype=torch.int64))
     swap_pairs: torch.Tensor = field(default_factory=lambda: torch.empty(0, 2, dtype=torch.int64))
     causal: bool = True                      # False: encoder attention
+    kv_cache_dtype: str = "auto"             # or "fp8_e4m3" (uint8 cache)
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     # -- views used by the calls --------------------------------------------
     @property
@@ -135,7 +141,8 @@ def build(*, name: str, g: torch.Generator, dtype: torch.dtype,
           num_blocks: Optional[int] = None, pool_extra: float = 0.10,
           alibi: bool = False, sliding_window: int = 0,
           n_copy: int = 0, n_swap: int = 0, fill_cache: bool = True,
-          causal: bool = True) -> Workload:
+          causal: bool = True, kv_cache_dtype: str = "auto", k_scale: float = 1.0,
+          v_scale: float = 1.0) -> Workload:
     """Lay out a batch in a paged pool and draw its tensors.
 
     Block placement: the N = sum ceil(seq_len / block_size) blocks the batch
@@ -169,9 +176,21 @@ def build(*, name: str, g: torch.Generator, dtype: torch.dtype,
     free = [int(x) for x in perm[need:]]
 
     row = num_kv_heads * head_size
-    kv_cache = torch.zeros(2, num_blocks, bs * row, dtype=dtype)
-    if fill_cache:
-        fill_normal(kv_cache.numel(), dtype, g, out=kv_cache.view(-1))
+    if kv_cache_dtype == "fp8_e4m3":
+        # cached context as 8-bit codes: N(0,1) / scale narrowed by torch's
+        # float8_e4m3fn conversion (input drawing only; values stay in range)
+        kv_cache = torch.zeros(2, num_blocks, bs * row, dtype=torch.uint8)
+        if fill_cache:
+            for half, sc in ((0, k_scale), (1, v_scale)):
+                flat = kv_cache[half].view(-1)
+                for a in range(0, flat.numel(), 1 << 26):
+                    b = min(flat.numel(), a + (1 << 26))
+                    x = torch.randn(b - a, generator=g, dtype=torch.float32) / sc
+                    flat[a:b] = x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    else:
+        kv_cache = torch.zeros(2, num_blocks, bs * row, dtype=dtype)
+        if fill_cache:
+            fill_normal(kv_cache.numel(), dtype, g, out=kv_cache.view(-1))
 
     T = int(query_lens.sum())
     query = fill_normal(T * num_heads * head_size, dtype, g).view(T, -1)
@@ -214,7 +233,7 @@ def build(*, name: str, g: torch.Generator, dtype: torch.dtype,
         num_prefill_seqs=num_prefill_seqs, block_tables=tables,
         kv_cache=kv_cache, query=query, key=key, value=value,
         slot_mapping=slots, copy_pairs=copy_pairs, swap_pairs=swap_pairs,
-        causal=causal)
+        causal=causal, kv_cache_dtype=kv_cache_dtype, k_scale=k_scale, v_scale=v_scale)
 
 
 # ---------------------------------------------------------------------------
@@ -280,6 +299,16 @@ def _encoder_varlen_prefill(g, scale_down=1):
                  seq_lens=L, query_lens=L, num_prefill_seqs=B, causal=False)
 
 
+def _llama3_8b_decode_fp8(g, scale_down=1):
+    B = max(1, 256 // scale_down)
+    L = _uniform_int(g, B, 512, 4096)
+    return build(name="llama3_8b_decode_fp8", g=g, dtype=torch.bfloat16,
+                 num_heads=32, num_kv_heads=8, head_size=128, block_size=16,
+                 seq_lens=L, query_lens=torch.ones(B, dtype=torch.int64),
+                 num_prefill_seqs=0, kv_cache_dtype="fp8_e4m3", k_scale=0.02,
+                 v_scale=0.02)
+
+
 CONFIGS = {
     1: _tiny_decode,
     2: _llama3_8b_decode,
@@ -287,11 +316,12 @@ CONFIGS = {
     4: _mixed_chunked_alibi,
     5: _swa_long_decode,
     6: _encoder_varlen_prefill,
+    7: _llama3_8b_decode_fp8,
 }
 
 
 def make_config(index: int, scale_down: int = 1) -> Workload:
-    """Workload ``index`` (1..6) drawn from generator seed 1000 + index.
+    """Workload ``index`` (1..7) drawn from generator seed 1000 + index.
 
     ``scale_down`` > 1 divides the batch counts (not the lengths), for tests
     that want the shape of a workload at a fraction of its size.

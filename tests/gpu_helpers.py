@@ -18,7 +18,7 @@ DEV = torch.device("cuda:0")
 def oracle_params(w: W.Workload) -> O.AttnParams:
     return O.AttnParams(w.num_heads, w.num_kv_heads, w.head_size, w.block_size, w.scale,
                         None if w.alibi_slopes is None else w.alibi_slopes.tolist(),
-                        w.sliding_window, w.causal)
+                        w.sliding_window, w.causal, w.kv_cache_dtype, w.k_scale, w.v_scale)
 
 
 class GpuRun:
@@ -28,7 +28,8 @@ class GpuRun:
         self.w = w
         self.slopes = None if w.alibi_slopes is None else w.alibi_slopes.to(DEV)
         self.p = B.make_params(w.num_heads, w.num_kv_heads, w.head_size, w.block_size, w.dtype,
-                               w.scale, self.slopes, w.sliding_window, not w.causal)
+                               w.scale, self.slopes, w.sliding_window, not w.causal,
+                               w.kv_cache_dtype, w.k_scale, w.v_scale)
         self.cache = w.kv_cache.to(DEV)
         self.key = w.key.to(DEV)
         self.value = w.value.to(DEV)

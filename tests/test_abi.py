@@ -40,8 +40,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pkv_abi_version() == 2
-    assert ctypes.sizeof(B.AttnParams) == 40
+    assert lib.pkv_abi_version() == 3
+    assert ctypes.sizeof(B.AttnParams) == 56
     for s in range(6):
         assert B.status_string(s)
     assert B.status_string(99) == "unknown status"
@@ -49,7 +49,8 @@ def test_abi_version_and_status_strings(lib):
 
 def _p(**kw):
     base = dict(num_heads=32, num_kv_heads=8, head_size=128, block_size=16, dtype=B.PKV_BF16,
-                scale=0.088, alibi_slopes=None, sliding_window=0, non_causal=0)
+                scale=0.088, alibi_slopes=None, sliding_window=0, non_causal=0,
+                kv_cache_dtype=B.PKV_CACHE_AUTO, k_scale=1.0, v_scale=1.0)
     base.update(kw)
     return B.AttnParams(**base)
 
@@ -67,6 +68,13 @@ def test_params_validation(lib):
     assert write(_p(scale=0.0)) == B.PKV_ERR_INVALID
     assert write(_p(non_causal=1, sliding_window=8)) == B.PKV_ERR_UNSUPPORTED
     assert write(_p(non_causal=2)) == B.PKV_ERR_INVALID
+    assert write(_p(kv_cache_dtype=2)) == B.PKV_ERR_UNSUPPORTED
+    fp8 = dict(kv_cache_dtype=B.PKV_CACHE_FP8_E4M3)
+    assert write(_p(k_scale=0.0, **fp8)) == B.PKV_ERR_INVALID
+    assert write(_p(v_scale=-1.0, **fp8)) == B.PKV_ERR_INVALID
+    assert write(_p(k_scale=float("inf"), **fp8)) == B.PKV_ERR_INVALID
+    assert write(_p(k_scale=0.0), n=0) == B.PKV_OK   # scales unused by an "auto" cache
+    assert write(_p(**fp8), n=0) == B.PKV_OK
     assert write(_p(), nb=0) == B.PKV_ERR_INVALID
     assert write(_p(), n=-1) == B.PKV_ERR_INVALID
     assert write(_p(), n=1) == B.PKV_ERR_INVALID      # null pointers
@@ -91,6 +99,9 @@ def test_decode_and_prefill_validation(lib):
                                          ctypes.byref(p), nul) == B.PKV_ERR_INVALID
     assert lib.paged_attn_prefill_varlen(nul, nul, -1, 3, nul, nul, 5, 5, nul, 4, nul, 1,
                                          ctypes.byref(p), nul) == B.PKV_ERR_INVALID
+    p8 = _p(kv_cache_dtype=B.PKV_CACHE_FP8_E4M3, k_scale=0.02, v_scale=0.02)
+    assert lib.paged_attn_prefill_varlen(nul, nul, 10, 3, nul, nul, 5, 5, nul, 4, nul, 1,
+                                         ctypes.byref(p8), nul) == B.PKV_ERR_UNSUPPORTED
 
 
 def test_workspace_size_is_host_only(lib):

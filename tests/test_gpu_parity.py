@@ -274,3 +274,105 @@ def test_bad_block_table_entry_is_reported():
     r2.prefill()
     torch.cuda.synchronize()
     assert B.device_error()[0] == B.PKV_ERR_BOUNDS
+
+
+# ---------------------------------------------------------------------------
+# fp8 (E4M3) cache: write is bit-exact, decode and block moves over codes
+# ---------------------------------------------------------------------------
+
+def fp8(w, k_scale=0.02, v_scale=0.03):
+    """The same workload over an fp8 cache: codes of its context drawn as in
+    workload 7, new keys/values quantised by the write."""
+    g = torch.Generator().manual_seed(len(w.name) * 7919 + int(w.seq_lens.sum()))
+    cache = torch.zeros(w.kv_cache.shape, dtype=torch.uint8)
+    for half, sc in ((0, k_scale), (1, v_scale)):
+        x = torch.randn(cache[half].numel(), generator=g) / sc
+        cache[half].view(-1).copy_(x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8))
+    w.kv_cache = cache
+    w.kv_cache_dtype, w.k_scale, w.v_scale = "fp8_e4m3", k_scale, v_scale
+    return w
+
+
+FP8_WRITE_CASES = {
+    "cfg7": lambda: W.make_config(7, scale_down=32),
+    "prefill_bf16": lambda: fp8(small(81, seq_lens=[5, 9, 33], query_lens=[5, 9, 33], P=3)),
+    "fp16_d64_bs32": lambda: fp8(small(82, dtype=torch.float16, D=64, bs=32, H=4, KVH=2,
+                                       seq_lens=[40, 70], query_lens=[40, 70], P=2)),
+    # scales small enough that a few percent of the quotients pass 448
+    "saturating": lambda: fp8(small(83, seq_lens=[64, 17], query_lens=[64, 17], P=2),
+                              k_scale=0.005, v_scale=0.004),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FP8_WRITE_CASES))
+def test_kv_cache_write_fp8_bit_exact(case):
+    w = FP8_WRITE_CASES[case]()
+    if case == "prefill_bf16":
+        w.slot_mapping[::4] = -1
+    r = GpuRun(w)
+    r.write()
+    assert_no_device_error(case)
+    ref = oracle_cache_after_write(w)
+    got = r.cache.cpu()
+    assert got.dtype == torch.uint8
+    assert torch.equal(got, ref), int((got != ref).sum())
+    if case == "saturating":   # the case does reach the saturated codes
+        assert ((ref == 0x7E) | (ref == 0xFE)).any()
+
+
+FP8_DECODE_CASES = {
+    "cfg7": lambda: W.make_config(7, scale_down=16),
+    "qpk4_multi_split": lambda: fp8(small(91, H=32, KVH=8, seq_lens=rand_lens(21, 12, 1, 900))),
+    "qpk1": lambda: fp8(small(92, H=4, KVH=4, seq_lens=rand_lens(22, 7, 1, 300))),
+    "qpk2_d64": lambda: fp8(small(93, H=4, KVH=2, D=64, seq_lens=rand_lens(23, 9, 1, 600))),
+    "qpk8_fp16": lambda: fp8(small(94, dtype=torch.float16, H=16, KVH=2,
+                                   seq_lens=rand_lens(24, 5, 1, 700))),
+    "block32_alibi": lambda: fp8(small(95, bs=32, alibi=True, seq_lens=rand_lens(25, 6, 1, 900))),
+    "window": lambda: fp8(small(96, window=100, seq_lens=rand_lens(26, 8, 1, 900))),
+    "long_single": lambda: fp8(small(97, H=32, KVH=8, seq_lens=[5000])),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FP8_DECODE_CASES))
+def test_decode_fp8_parity(case):
+    w = FP8_DECODE_CASES[case]()
+    r = GpuRun(w)
+    r.write()
+    out = r.decode()
+    assert_no_device_error(case)
+    ref_cache = oracle_cache_after_write(w)
+    assert torch.equal(r.cache.cpu(), ref_cache)
+    q, bt, sl, _ = w.decode_slices()
+    ref = O.paged_attn_decode(q, ref_cache, bt, sl, oracle_params(w))
+    assert_close(out, ref, case)
+
+
+def test_fp8_copy_and_swap_move_codes():
+    w = fp8(small(98, seq_lens=[300, 200], num_blocks=64))
+    r = GpuRun(w)
+    pairs = torch.tensor([[3, 20], [7, 30], [0, 63]], dtype=torch.int64)
+    B.kv_copy_blocks([r.cache], pairs.to(DEV), r.p)
+    ref = w.kv_cache.clone()
+    O.kv_copy_blocks([ref], pairs.tolist())
+    assert torch.equal(r.cache.cpu(), ref)
+    host = torch.zeros((2, 8, w.kv_cache.shape[2]), dtype=torch.uint8).pin_memory()
+    out_pairs = torch.tensor([[5, 0], [40, 7]], dtype=torch.int64)
+    B.kv_swap_blocks(r.cache, host, out_pairs, r.p)
+    assert_no_device_error("fp8 moves")
+    ref_host = torch.zeros_like(host)
+    O.kv_swap_blocks(ref, ref_host, out_pairs.tolist())
+    assert torch.equal(host, ref_host)
+
+
+def test_fp8_prefill_and_dtype_mismatch_rejected():
+    w = fp8(small(99, seq_lens=[40], query_lens=[40], P=1))
+    r = GpuRun(w)
+    with pytest.raises(B.PkvError) as e:
+        r.prefill()
+    assert e.value.status == B.PKV_ERR_UNSUPPORTED
+    wide = torch.zeros(w.kv_cache.shape, dtype=w.dtype, device=DEV)
+    with pytest.raises(ValueError):   # a 2-byte cache under fp8 params
+        B.kv_cache_write(r.key, r.value, wide, r.slots, r.p)
+    with pytest.raises(ValueError):
+        r.p.kv_cache_dtype = B.PKV_CACHE_AUTO
+        B.kv_cache_write(r.key, r.value, r.cache, r.slots, r.p)
