@@ -39,6 +39,7 @@ namespace pkv {
 constexpr int kDecWarps = 4;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kSub = 16;  // tokens per compute sub-tile
+constexpr float kLazy = 8.f;  // reference-max slack (log2 units) before a rescale
 
 struct DecodeArgs {
   void *out;
@@ -150,7 +151,7 @@ __device__ __forceinline__ void load_chunk8_f32(const uint2 &u, float (&f)[8]) {
 // CTA (<= 4); KV8: the cache holds E4M3 codes (k_scale is folded into the
 // query scale, v_scale applied to the merged output).
 template <class T, int D, int QT, bool KV8>
-__global__ void __launch_bounds__(kDecThreads, 3)
+__global__ void __launch_bounds__(kDecThreads, KV8 ? 4 : 3)
 decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
   constexpr int CPL = D / 64;  // 8-element chunks per lane per token (q.k)
   constexpr int DPL = D / 32;  // output dims per lane (p.V)
@@ -226,7 +227,7 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 
   // ---- query registers (pre-scaled into the log2 domain) ------------------
   const int dg = lane & 7, ts = lane >> 3;
-  float q[QT][CPL * 8];
+  unsigned long long q2[QT][CPL * 4];  // packed dim pairs
   {
     const uint4 *qrow = reinterpret_cast<const uint4 *>(a.query + (static_cast<int64_t>(b) * H + head0) * D);
 #pragma unroll
@@ -236,7 +237,8 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
         float f[8];
         load_chunk_f32<T>(__ldg(qrow + h * ROWC + c * 8 + dg), f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[h][c * 8 + e] = f[e] * a.scale_log2;
+        for (int e = 0; e < 8; e += 2)
+          q2[h][c * 4 + e / 2] = f2pack(f[e] * a.scale_log2, f[e + 1] * a.scale_log2);
       }
   }
   float slope[QT];
@@ -251,7 +253,8 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
     else if constexpr (QT == 2) slope_own[f] = (dg & 1) ? slope[1] : slope[0];
     else slope_own[f] = slope[0];
   }
-  float m[NF], l[NF], o[QT][DPL];
+  float m[NF], l[NF];
+  unsigned long long o2[QT][DPL / 2];  // packed output dim pairs
 #pragma unroll
   for (int f = 0; f < NF; ++f) {
     m[f] = -INFINITY;
@@ -260,7 +263,7 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
   for (int h = 0; h < QT; ++h)
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) o[h][e] = 0.f;
+    for (int e = 0; e < DPL / 2; ++e) o2[h][e] = 0ull;  // (+0, +0)
   float *wP = sP + warp * kSub * QT;
   const int qpos = sp.L - 1;
   bool ok = true;
@@ -292,8 +295,9 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
       for (int it = 0; it < kSub / 4; ++it) {
         const int tok = it * 4 + ts;
+        unsigned long long acc[QT];  // even / odd dim partial sums
 #pragma unroll
-        for (int h = 0; h < QT; ++h) v[it * QT + h] = 0.f;
+        for (int h = 0; h < QT; ++h) acc[h] = 0ull;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           float f[8];
@@ -302,9 +306,17 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
           else
             load_chunk_f32<T>(k4[tok * ROWC + c * 8 + dg], f);
 #pragma unroll
-          for (int h = 0; h < QT; ++h)
+          for (int e = 0; e < 8; e += 2) {
+            const unsigned long long kk = f2pack(f[e], f[e + 1]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[it * QT + h] = fmaf(q[h][c * 8 + e], f[e], v[it * QT + h]);
+            for (int h = 0; h < QT; ++h) acc[h] = ffma2(q2[h][c * 4 + e / 2], kk, acc[h]);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < QT; ++h) {
+          float x, y;
+          f2unpack(acc[h], x, y);
+          v[it * QT + h] = x + y;
         }
       }
       // Recursive halving over the 8 dg lanes (xor 4, 2, 1): each level a lane
@@ -320,45 +332,63 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
       for (int f = 0; f < NF; ++f)
         sc[f] = valid ? v[f] + slope_own[f] * static_cast<float>(j - qpos) : -INFINITY;
-      // ---- online softmax: max over the 16 lanes holding the same head ----
-      float alpha_own[NF];
+      // ---- online softmax with a lazy reference max: while no score exceeds
+      // the head's reference m by more than kLazy (log2 units) the weights
+      // 2^(s - m) stay <= 2^kLazy and nothing is rescaled; otherwise the
+      // reference moves to the true running max (the 16 lanes of a head) --
+      bool grow = false;
 #pragma unroll
-      for (int f = 0; f < NF; ++f) {
-        float bm = sc[f];
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-        const float mn = fmaxf(m[f], bm);
-        alpha_own[f] = fast_exp2(m[f] - mn);
-        m[f] = mn;
-        const float p = fast_exp2(sc[f] - mn);
-        l[f] = l[f] * alpha_own[f] + p;  // per-lane partial, summed at the end
-        if (QT > 1 || (dg & 1) == 0) wP[tk * QT + head_of<QT>(dg, f)] = p;
-      }
-      // every lane needs every head's rescale factor for its p.V accumulators
-      float alpha[QT];
-      if constexpr (QT == 4) {
-        const float x0 = __shfl_xor_sync(0xffffffffu, alpha_own[0], 1);
-        const float x1 = __shfl_xor_sync(0xffffffffu, alpha_own[1], 1);
-        const bool hi = dg & 1;
-        alpha[0] = hi ? x0 : alpha_own[0];
-        alpha[1] = hi ? x1 : alpha_own[1];
-        alpha[2] = hi ? alpha_own[0] : x0;
-        alpha[3] = hi ? alpha_own[1] : x1;
-      } else if constexpr (QT == 2) {
-        const float x0 = __shfl_xor_sync(0xffffffffu, alpha_own[0], 1);
-        const bool hi = dg & 1;
-        alpha[0] = hi ? x0 : alpha_own[0];
-        alpha[1] = hi ? alpha_own[0] : x0;
+      for (int f = 0; f < NF; ++f) grow |= sc[f] > m[f] + kLazy;
+      if (!__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int f = 0; f < NF; ++f) {
+          const float p = fast_exp2(sc[f] - m[f]);
+          l[f] += p;
+          if (QT > 1 || (dg & 1) == 0) wP[tk * QT + head_of<QT>(dg, f)] = p;
+        }
+        __syncwarp();
       } else {
-        alpha[0] = alpha_own[0];
+        float alpha_own[NF];
+#pragma unroll
+        for (int f = 0; f < NF; ++f) {
+          float bm = sc[f];
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+          const float mn = fmaxf(m[f], bm);
+          alpha_own[f] = fast_exp2(m[f] - mn);
+          m[f] = mn;
+          const float p = fast_exp2(sc[f] - mn);
+          l[f] = l[f] * alpha_own[f] + p;  // per-lane partial, summed at the end
+          if (QT > 1 || (dg & 1) == 0) wP[tk * QT + head_of<QT>(dg, f)] = p;
+        }
+        // every lane needs every head's rescale factor for its p.V accumulators
+        float alpha[QT];
+        if constexpr (QT == 4) {
+          const float x0 = __shfl_xor_sync(0xffffffffu, alpha_own[0], 1);
+          const float x1 = __shfl_xor_sync(0xffffffffu, alpha_own[1], 1);
+          const bool hi = dg & 1;
+          alpha[0] = hi ? x0 : alpha_own[0];
+          alpha[1] = hi ? x1 : alpha_own[1];
+          alpha[2] = hi ? alpha_own[0] : x0;
+          alpha[3] = hi ? alpha_own[1] : x1;
+        } else if constexpr (QT == 2) {
+          const float x0 = __shfl_xor_sync(0xffffffffu, alpha_own[0], 1);
+          const bool hi = dg & 1;
+          alpha[0] = hi ? x0 : alpha_own[0];
+          alpha[1] = hi ? alpha_own[0] : x0;
+        } else {
+          alpha[0] = alpha_own[0];
+        }
+#pragma unroll
+        for (int h = 0; h < QT; ++h) {
+          const unsigned long long a2 = f2pack(alpha[h], alpha[h]);
+#pragma unroll
+          for (int e = 0; e < DPL / 2; ++e) o2[h][e] = fmul2(o2[h][e], a2);
+        }
+        __syncwarp();
       }
-#pragma unroll
-      for (int h = 0; h < QT; ++h)
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) o[h][e] *= alpha[h];
-      __syncwarp();
       // ---- p.V over the valid tokens ---------------------------------------
       const uint8_t *vrow = vt + (sub * D + lane * DPL) * EB;
       for (int tok = t_lo; tok < t_hi; ++tok) {
@@ -388,10 +418,15 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
           for (int h = 0; h < QT; ++h) pp[h] = wP[tok * QT + h];
         }
+        unsigned long long vv[DPL / 2];
 #pragma unroll
-        for (int h = 0; h < QT; ++h)
+        for (int e = 0; e < DPL / 2; ++e) vv[e] = f2pack(vf[2 * e], vf[2 * e + 1]);
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pp[h], vf[e], o[h][e]);
+        for (int h = 0; h < QT; ++h) {
+          const unsigned long long p2 = f2pack(pp[h], pp[h]);
+#pragma unroll
+          for (int e = 0; e < DPL / 2; ++e) o2[h][e] = ffma2(p2, vv[e], o2[h][e]);
+        }
       }
       __syncwarp();
     }
@@ -415,7 +450,12 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
   for (int h = 0; h < QT; ++h)
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) sO[(warp * QT + h) * D + lane * DPL + e] = o[h][e];
+    for (int e = 0; e < DPL / 2; ++e) {
+      float x, y;
+      f2unpack(o2[h][e], x, y);
+      sO[(warp * QT + h) * D + lane * DPL + 2 * e] = x;
+      sO[(warp * QT + h) * D + lane * DPL + 2 * e + 1] = y;
+    }
 #pragma unroll
   for (int f = 0; f < NF; ++f) {
     float lt = l[f];
