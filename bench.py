@@ -35,7 +35,8 @@ if HERE not in sys.path:
 from paged_kv_cache_246_gb300 import workloads as W  # noqa: E402
 
 METRIC = ("decode tokens/s and HBM GB/s (%peak); prefill TFLOP/s (%bf16 peak), 1×GB300")
-CFG_OF = {"decode": 2, "prefill": 3, "mixed": 4, "swa": 5, "encoder": 6, "decode_fp8": 7}
+CFG_OF = {"decode": 2, "prefill": 3, "mixed": 4, "swa": 5, "encoder": 6, "decode_fp8": 7,
+          "prefill_fp8": 8}
 
 
 def peaks():

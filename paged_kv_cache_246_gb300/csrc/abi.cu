@@ -246,7 +246,6 @@ pkv_status paged_attn_prefill_varlen(void *out, const void *query, int64_t num_q
   Geometry g;
   pkv_status st = make_geometry(params, num_blocks, &g);
   if (st != PKV_OK) return st;
-  if (g.fp8) return PKV_ERR_UNSUPPORTED;
   if (num_seqs < 0 || num_seqs > 65535 || max_query_len < 0 || max_seq_len < 0 ||
       max_blocks_per_seq <= 0 || num_query_tokens < 0 || num_query_tokens > 0x7fffffffLL)
     return PKV_ERR_INVALID;

@@ -41,13 +41,29 @@
 //               grows by more than 2^8, and P is written back as bf16/fp16
 //               pairs over the first 64 columns of the score buffer, 16
 //               columns at a time; at the end O is normalised and stored.
-//   warps 2-3   idle.
+//   warps 2-3   idle, except over an fp8 (E4M3) cache: there the producer
+//               loads each tile's 8-bit codes (one plain box of D bytes x
+//               block_size rows per cache block), and these two warps widen
+//               them to fp16 in the 128-byte-swizzled layout the MMA reads
+//               (E4M3 is a subset of fp16, so the codes are exact), then
+//               release the stage to the MMA thread.  The MMAs then run on
+//               fp16 operands: bf16 queries are rewritten in place as fp16
+//               times a CTA-wide power of two 2^-e chosen from their largest
+//               magnitude (exact scaling, no overflow), and k_scale * 2^e
+//               joins the softmax scale; P is written as fp16 and v_scale
+//               multiplies the output.  With D = 128 the codes land in the
+//               stage's upper 64-column region and are widened in place, row
+//               by row (a row is read completely before it is rewritten);
+//               with D = 64 they have their own staging area.
 // TMEM: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [384, 384+D).
 // Causal tile skipping: each query tile only visits the key tiles its rows
 // can see; CTAs are ordered so the tiles with the most keys start first.
 // Every wait is bounded; a timeout raises a CTA-wide abort flag, the roles
 // stop, in-flight copies and MMAs are drained, TMEM is freed.
+#include <cuda_fp8.h>
+
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -66,7 +82,8 @@ struct PrefillArgs {
   int64_t num_q_tokens;  // rows of query / out
   int num_seqs, max_blocks_per_seq;
   int H, KVH, QPK, BS, window, non_causal;
-  float scale_log2;
+  float scale_log2;  // scale * log2(e) (* k_scale over an fp8 cache)
+  float v_scale;     // 1, or the fp8 cache's value scale
 };
 
 namespace pf {
@@ -75,18 +92,28 @@ constexpr int BM = 128, BN = 128;
 constexpr int NSTK = 3, NSTV = 2;  // K and V pipeline stages
 constexpr int kThreads = 384;
 
-template <int D>
+template <int D, bool KV8 = false>
 struct Lay {
   static constexpr int REG = 128 * 128;  // one 64-column region of 128 rows
   static constexpr int NREG = D / 64;
   static constexpr int TILE = REG * NREG;
+  static constexpr int TILE8 = BN * D;  // one key tile of 8-bit codes
+  static constexpr bool STG_SEP = KV8 && D == 64;  // codes get their own area
   static constexpr int OFF_Q = 0;  // two Q tiles
   static constexpr int OFF_K = 2 * TILE;
   static constexpr int OFF_V = OFF_K + NSTK * TILE;
-  static constexpr int OFF_BAR = OFF_V + NSTV * TILE;
+  static constexpr int OFF_STG = OFF_V + NSTV * TILE;
+  static constexpr int OFF_BAR = OFF_STG + (STG_SEP ? (NSTK + NSTV) * TILE8 : 0);
+  // B_KF / B_VF: stage ready for the MMA; B_K8F / B_V8F: codes landed (fp8)
   static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NSTK, B_EK = B_VF + NSTV,
                        B_EV = B_EK + NSTK, B_SF = B_EV + NSTV, B_PF = B_SF + 2, B_O = B_PF + 2,
-                       B_FIN = B_O + 2, NBAR = B_FIN + 1;
+                       B_FIN = B_O + 2, B_Q2 = B_FIN + 1, B_K8F = B_Q2 + 1,
+                       B_V8F = B_K8F + NSTK, NBAR = B_V8F + NSTV;
+  // 8-bit codes of stage s of K (kv = 0) or V (kv = 1)
+  static __device__ __forceinline__ uint8_t *codes(uint8_t *smem, int kv, int s) {
+    if constexpr (STG_SEP) return smem + OFF_STG + (kv ? NSTK + s : s) * TILE8;
+    else return smem + (kv ? OFF_V : OFF_K) + s * TILE + REG;
+  }
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 32;
   // + alignment slack; at least ~118 KB so that one CTA owns an SM (and all
@@ -128,17 +155,30 @@ struct AB<FP16> {
   static constexpr int v = 0;
 };
 
+// Four E4M3 codes (low byte first) -> two fp16 pairs, exactly.
+__device__ __forceinline__ uint2 e4m3x4_to_h4(uint32_t u) {
+  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+      static_cast<__nv_fp8x2_storage_t>(u & 0xffffu), __NV_E4M3);
+  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+      static_cast<__nv_fp8x2_storage_t>(u >> 16), __NV_E4M3);
+  return make_uint2(static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16),
+                    static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16));
+}
+
 // One query tile of the CTA: head, first row within the sequence, rows,
 // and the half-open range of the CTA's key tiles it needs.
 struct QTile {
   int head, q0, rows, j0, j1;
 };
 
-template <class T, int D, bool ALIBI>
+template <class T, int D, bool ALIBI, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
                   const __grid_constant__ CUtensorMap kvmap, int pair_heads) {
-  using L = Lay<D>;
+  using L = Lay<D, KV8>;
+  using OPT = std::conditional_t<KV8, FP16, T>;  // MMA operand type (and P)
+  constexpr int KFT = KV8 ? L::B_K8F : L::B_KF;   // barrier the K copies complete on
+  constexpr int VFT = KV8 ? L::B_V8F : L::B_VF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -201,8 +241,14 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
   const int64_t where = static_cast<int64_t>(b) * a.H + qt[0].head;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < L::NBAR; ++i)
-      mbar_init(&bars[i], (i == L::B_PF || i == L::B_PF + 1) ? 128 : 1);
+    for (int i = 0; i < L::NBAR; ++i) {
+      uint32_t count = (i == L::B_PF || i == L::B_PF + 1) ? 128 : 1;
+      // over an fp8 cache the converter warps release Q (warp 2) and the
+      // stages (warps 2 and 3)
+      if (KV8 && i == L::B_Q2) count = 32;
+      if (KV8 && i >= L::B_KF && i < L::B_VF + NSTV) count = 64;
+      mbar_init(&bars[i], count);
+    }
     misc[1] = 0;  // abort flag
     misc[2] = 0;  // K tiles issued
     misc[3] = 0;  // V tiles issued
@@ -253,23 +299,33 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       const int sk = j % NSTK;
       if (j >= NSTK && !warp_wait(&bars[L::B_EK + sk], ((j / NSTK) - 1) & 1, abort_flag, where))
         break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[L::B_KF + sk], L::TILE);
+      if (lane == 0) mbar_arrive_expect_tx(&bars[KFT + sk], KV8 ? L::TILE8 : L::TILE);
       __syncwarp();
       if (lane < TB) {
-        uint8_t *kd = smem + L::OFF_K + sk * L::TILE + lane * BS * 128;
-        for (int r = 0; r < L::NREG; ++r)
-          tma_load_4d(kd + r * L::REG, &kvmap, &bars[L::B_KF + sk], 64 * r, g, coord, 0);
+        if constexpr (KV8) {
+          tma_load_4d(L::codes(smem, 0, sk) + lane * BS * D, &kvmap, &bars[KFT + sk], 0, g, coord,
+                      0);
+        } else {
+          uint8_t *kd = smem + L::OFF_K + sk * L::TILE + lane * BS * 128;
+          for (int r = 0; r < L::NREG; ++r)
+            tma_load_4d(kd + r * L::REG, &kvmap, &bars[KFT + sk], 64 * r, g, coord, 0);
+        }
       }
       jk = j + 1;
       const int sv = j % NSTV;
       if (j >= NSTV && !warp_wait(&bars[L::B_EV + sv], ((j / NSTV) - 1) & 1, abort_flag, where))
         break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[L::B_VF + sv], L::TILE);
+      if (lane == 0) mbar_arrive_expect_tx(&bars[VFT + sv], KV8 ? L::TILE8 : L::TILE);
       __syncwarp();
       if (lane < TB) {
-        uint8_t *vd = smem + L::OFF_V + sv * L::TILE + lane * BS * 128;
-        for (int r = 0; r < L::NREG; ++r)
-          tma_load_4d(vd + r * L::REG, &kvmap, &bars[L::B_VF + sv], 64 * r, g, coord, 1);
+        if constexpr (KV8) {
+          tma_load_4d(L::codes(smem, 1, sv) + lane * BS * D, &kvmap, &bars[VFT + sv], 0, g, coord,
+                      1);
+        } else {
+          uint8_t *vd = smem + L::OFF_V + sv * L::TILE + lane * BS * 128;
+          for (int r = 0; r < L::NREG; ++r)
+            tma_load_4d(vd + r * L::REG, &kvmap, &bars[VFT + sv], 64 * r, g, coord, 1);
+        }
       }
       jv = j + 1;
     }
@@ -282,8 +338,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     // One thread: the tensor core's instruction queue is shallow, so every
     // cycle this thread spends outside an MMA is a cycle the tensor core may
     // idle.  Waits are scalar; there is no warp-wide synchronisation here.
-    constexpr uint32_t ID_QK = tc5::idesc_f16(AB<T>::v, 0, BM, BN);
-    constexpr uint32_t ID_PV = tc5::idesc_f16(AB<T>::v, 1, BM, D);
+    constexpr uint32_t ID_QK = tc5::idesc_f16(AB<OPT>::v, 0, BM, BN);
+    constexpr uint32_t ID_PV = tc5::idesc_f16(AB<OPT>::v, 1, BM, D);
     // Operand descriptors are built once; an MMA only adds a compile-time
     // offset (in 16-byte units) to a base.
     const uint64_t q_desc = tc5::sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
@@ -313,7 +369,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       }
       tc5::commit(&bars[L::B_SF + x]);
     };
-    bool ok = wait_or_abort(&bars[L::B_Q], 0, abort_flag, where);
+    bool ok = wait_or_abort(&bars[KV8 ? L::B_Q2 : L::B_Q], 0, abort_flag, where);
     if (ok && ntiles > 0) {
       ok = need_k(0);
       if (ok) {
@@ -369,6 +425,67 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     // every MMA this thread issued has completed before TMEM is released
     tc5::commit(&bars[L::B_FIN]);
     mbar_wait_bounded(&bars[L::B_FIN], 0, where);
+  } else if (KV8 && (warp == 2 || warp == 3)) {
+    // ------------------------------------------------------------ fp8 widening
+    const int cw = warp - 2;
+    bool ok = true;
+    if (cw == 0) {  // queries: warp 2 alone (no cross-warp barrier to wait on)
+      ok = warp_wait(&bars[L::B_Q], 0, abort_flag, where);
+    }
+    if (cw == 0 && ok) {
+      int e = 0;  // queries become fp16 * 2^-e
+      if constexpr (std::is_same<T, BF16>::value) {
+        const int nchunk = (qt[1].rows > 0 ? 2 : 1) * L::TILE / 16;
+        uint4 *q4 = reinterpret_cast<uint4 *>(smem + L::OFF_Q);
+        uint32_t am = 0;  // per-halfword max of |bf16| bit patterns
+        for (int c = lane; c < nchunk; c += 32) {
+          const uint4 u = q4[c];
+          am = __vmaxu2(am, __vmaxu2(__vmaxu2(u.x & 0x7fff7fffu, u.y & 0x7fff7fffu),
+                                     __vmaxu2(u.z & 0x7fff7fffu, u.w & 0x7fff7fffu)));
+        }
+        am = __reduce_max_sync(0xffffffffu, max(am & 0xffffu, am >> 16));
+        const int E = static_cast<int>(am >> 7);  // bf16 exponent field of the largest |q|
+        // largest |q| * 2^-e in [2^14, 2^15): inside fp16's range, full precision
+        e = E == 0 ? 0 : min(64, max(-64, E - 141));
+        const float mul = __int_as_float((127 - e) << 23);
+        for (int c = lane; c < nchunk; c += 32) {
+          const uint4 u = q4[c];
+          uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = BF16::to_f2(w[k]);
+            w[k] = FP16::from_f2(f.x * mul, f.y * mul);
+          }
+          q4[c] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      if (lane == 0) misc[4] = static_cast<uint32_t>(e);
+      mbar_arrive(&bars[L::B_Q2]);
+    }
+    // per key tile: K then V, in the order the producer issues them
+    constexpr int LPR = D / 8, RPI = 32 / LPR;  // lanes per row, rows per pass
+    const int cc = lane % LPR, r0 = lane / LPR;
+    auto widen = [&](int kv, int s, uint32_t parity) -> bool {
+      if (!warp_wait(&bars[(kv ? L::B_V8F : L::B_K8F) + s], parity, abort_flag, where))
+        return false;
+      const uint8_t *src = L::codes(smem, kv, s);
+      uint8_t *dst = smem + (kv ? L::OFF_V : L::OFF_K) + s * L::TILE;
+#pragma unroll 4
+      for (int it = 0; it < 64 / RPI; ++it) {
+        const int row = cw * 64 + it * RPI + r0;
+        const uint2 u = *reinterpret_cast<const uint2 *>(src + row * D + cc * 8);
+        __syncwarp();  // the row's codes are read before any lane rewrites it
+        const uint2 h0 = e4m3x4_to_h4(u.x), h1 = e4m3x4_to_h4(u.y);
+        *reinterpret_cast<uint4 *>(dst + (cc / 8) * L::REG + row * 128 +
+                                   (((cc % 8) ^ (row & 7)) * 16)) = make_uint4(h0.x, h0.y, h1.x, h1.y);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[(kv ? L::B_VF : L::B_KF) + s]);
+      return true;
+    };
+    for (int j = 0; ok && j < ntiles; ++j)
+      ok = widen(0, j % NSTK, (j / NSTK) & 1) && widen(1, j % NSTV, (j / NSTV) & 1);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int x = warp >= 8 ? 1 : 0;
@@ -380,14 +497,18 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     const int pos = cb + t.q0 + row;
     const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
     const int hi = a.non_causal ? Lb - 1 : pos;  // last visible key
-    const float sl2 = a.scale_log2;
+    float sl2 = a.scale_log2;
     const float slope = ALIBI ? __ldg(a.alibi + t.head) * kLog2e : 0.f;
     // running max m: in the log2 domain with ALiBi; in raw-score units
     // without (then scores are scaled inside the exponent's FMA)
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    if constexpr (KV8) {  // the queries' power-of-two scale joins the score scale
+      ok = warp_wait(&bars[L::B_Q2], 0, abort_flag, where);
+      sl2 *= __int_as_float((127 + static_cast<int>(misc[4])) << 23);
+    }
     const int n = t.j1 - t.j0;
-    for (int k = 0; k < n; ++k) {
+    for (int k = 0; ok && k < n; ++k) {
       const int j = t.j0 + k;
       if (!warp_wait(&bars[L::B_SF + x], k & 1, abort_flag, where)) {
         ok = false;
@@ -462,7 +583,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
                    x0, x1);
           const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
           ps2[(e / 2) & 3] = fadd2(ps2[(e / 2) & 3], f2pack(p0, p1));
-          pk[e / 2] = T::from_f2(p0, p1);
+          pk[e / 2] = OPT::from_f2(p0, p1);
         }
         tc5::tmem_st16(sb + 16 * c, pk);
       }
@@ -492,7 +613,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     }
     if (ok && n > 0 && warp_wait(&bars[L::B_O + x], (n - 1) & 1, abort_flag, where)) {
       tc5::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? (KV8 ? a.v_scale : 1.f) / l : 0.f;
       const bool valid = row < t.rows;
       uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) +
                                              (static_cast<int64_t>(qs + t.q0 + row) * a.H + t.head) * D);
@@ -522,11 +643,11 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     const int nk = static_cast<int>(misc[2]), nv = static_cast<int>(misc[3]);
     for (int s = 0; s < NSTK; ++s) {
       const int t = nk - 1 - ((nk - 1 - s) % NSTK + NSTK) % NSTK;  // last K tile of stage s
-      if (t >= 0 && t % NSTK == s) mbar_wait_bounded(&bars[L::B_KF + s], (t / NSTK) & 1, where);
+      if (t >= 0 && t % NSTK == s) mbar_wait_bounded(&bars[KFT + s], (t / NSTK) & 1, where);
     }
     for (int s = 0; s < NSTV; ++s) {
       const int t = nv - 1 - ((nv - 1 - s) % NSTV + NSTV) % NSTV;
-      if (t >= 0 && t % NSTV == s) mbar_wait_bounded(&bars[L::B_VF + s], (t / NSTV) & 1, where);
+      if (t >= 0 && t % NSTV == s) mbar_wait_bounded(&bars[VFT + s], (t / NSTV) & 1, where);
     }
   }
   __syncthreads();
@@ -536,11 +657,11 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
   }
 }
 
-template <class T, int D, bool ALIBI>
+template <class T, int D, bool ALIBI, bool KV8>
 cudaError_t launch(const PrefillArgs &a, int max_query_len, const CUtensorMap &qmap,
                    const CUtensorMap &kvmap, cudaStream_t stream) {
-  const size_t smem = Lay<D>::ALLOC;
-  auto kern = prefill_tc_kernel<T, D, ALIBI>;
+  const size_t smem = Lay<D, KV8>::ALLOC;
+  auto kern = prefill_tc_kernel<T, D, ALIBI, KV8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -553,9 +674,12 @@ cudaError_t launch(const PrefillArgs &a, int max_query_len, const CUtensorMap &q
 
 template <class T, int D>
 cudaError_t launch_any(const PrefillArgs &a, int max_query_len, const CUtensorMap &qmap,
-                       const CUtensorMap &kvmap, cudaStream_t stream) {
-  return a.alibi ? launch<T, D, true>(a, max_query_len, qmap, kvmap, stream)
-                 : launch<T, D, false>(a, max_query_len, qmap, kvmap, stream);
+                       const CUtensorMap &kvmap, bool kv8, cudaStream_t stream) {
+  if (kv8)
+    return a.alibi ? launch<T, D, true, true>(a, max_query_len, qmap, kvmap, stream)
+                   : launch<T, D, false, true>(a, max_query_len, qmap, kvmap, stream);
+  return a.alibi ? launch<T, D, true, false>(a, max_query_len, qmap, kvmap, stream)
+                 : launch<T, D, false, false>(a, max_query_len, qmap, kvmap, stream);
 }
 
 }  // namespace pf
@@ -582,7 +706,8 @@ cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, i
   a.BS = g.BS;
   a.window = g.window;
   a.non_causal = g.non_causal;
-  a.scale_log2 = g.scale * kLog2e;
+  a.scale_log2 = g.scale * kLog2e * g.k_scale;
+  a.v_scale = g.v_scale;
   const bool bf = g.dtype == PKV_BF16;
   // Q: (D, H, tokens); cache: (D, KVH, NB * BS tokens, 2 halves); 64-element
   // (128-byte) inner boxes with the 128-byte swizzle the MMA descriptors use.
@@ -600,20 +725,28 @@ cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, i
       return cudaErrorInvalidValue;
   }
   {
+    // 16-bit cache: 64-element swizzled boxes; fp8 cache: one plain box of
+    // the whole D-byte row per cache block (the widening warps swizzle)
+    const cuuint64_t eb = static_cast<cuuint64_t>(g.elem_bytes);
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.D), static_cast<cuuint64_t>(g.KVH),
                                 static_cast<cuuint64_t>(g.num_blocks * g.BS), 2};
-    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.D) * 2,
-                                   static_cast<cuuint64_t>(g.row_elems) * 2,
-                                   static_cast<cuuint64_t>(g.num_blocks * g.block_elems) * 2};
-    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(g.BS), 1};
-    if (encode_tensor_map(&kvmap, dt, 4, const_cast<void *>(kv_cache), dims, strides, box,
-                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.D) * eb,
+                                   static_cast<cuuint64_t>(g.row_elems) * eb,
+                                   static_cast<cuuint64_t>(g.num_blocks * g.block_elems) * eb};
+    const cuuint32_t box[4] = {g.fp8 ? static_cast<cuuint32_t>(g.D) : 64u, 1,
+                               static_cast<cuuint32_t>(g.BS), 1};
+    if (encode_tensor_map(&kvmap, g.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : dt, 4,
+                          const_cast<void *>(kv_cache), dims, strides, box,
+                          g.fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B) !=
+        CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  if (g.D == 128) return bf ? pf::launch_any<BF16, 128>(a, max_query_len, qmap, kvmap, stream)
-                            : pf::launch_any<FP16, 128>(a, max_query_len, qmap, kvmap, stream);
-  if (g.D == 64) return bf ? pf::launch_any<BF16, 64>(a, max_query_len, qmap, kvmap, stream)
-                           : pf::launch_any<FP16, 64>(a, max_query_len, qmap, kvmap, stream);
+  if (g.D == 128)
+    return bf ? pf::launch_any<BF16, 128>(a, max_query_len, qmap, kvmap, g.fp8, stream)
+              : pf::launch_any<FP16, 128>(a, max_query_len, qmap, kvmap, g.fp8, stream);
+  if (g.D == 64)
+    return bf ? pf::launch_any<BF16, 64>(a, max_query_len, qmap, kvmap, g.fp8, stream)
+              : pf::launch_any<FP16, 64>(a, max_query_len, qmap, kvmap, g.fp8, stream);
   return cudaErrorInvalidValue;
 }
 

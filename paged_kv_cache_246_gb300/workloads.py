@@ -27,6 +27,9 @@ The five named workloads follow the attention-backend pages' metadata
 7. ``llama3_8b_decode_fp8``: the shape of 2 with an fp8 (E4M3) cache,
    k_scale = v_scale = 0.02 (N(0,1) keys and values map to codes of up to
    about +-250, inside E4M3's +-448).
+8. ``varlen_prefill_fp8``: the shape of 3 over an fp8 (E4M3) cache with the
+   same scales as 7 (the prompts' keys and values are quantised by the
+   cache write).
 """
 from __future__ import annotations
 
@@ -299,6 +302,15 @@ def _encoder_varlen_prefill(g, scale_down=1):
                  seq_lens=L, query_lens=L, num_prefill_seqs=B, causal=False)
 
 
+def _varlen_prefill_fp8(g, scale_down=1):
+    B = max(1, 16 // scale_down)
+    L = _log_uniform_int(g, B, 128, 8192)
+    return build(name="varlen_prefill_fp8", g=g, dtype=torch.bfloat16,
+                 num_heads=32, num_kv_heads=8, head_size=128, block_size=16,
+                 seq_lens=L, query_lens=L, num_prefill_seqs=B, kv_cache_dtype="fp8_e4m3",
+                 k_scale=0.02, v_scale=0.02)
+
+
 def _llama3_8b_decode_fp8(g, scale_down=1):
     B = max(1, 256 // scale_down)
     L = _uniform_int(g, B, 512, 4096)
@@ -317,11 +329,12 @@ CONFIGS = {
     5: _swa_long_decode,
     6: _encoder_varlen_prefill,
     7: _llama3_8b_decode_fp8,
+    8: _varlen_prefill_fp8,
 }
 
 
 def make_config(index: int, scale_down: int = 1) -> Workload:
-    """Workload ``index`` (1..7) drawn from generator seed 1000 + index.
+    """Workload ``index`` (1..8) drawn from generator seed 1000 + index.
 
     ``scale_down`` > 1 divides the batch counts (not the lengths), for tests
     that want the shape of a workload at a fraction of its size.

@@ -100,8 +100,10 @@ def test_decode_and_prefill_validation(lib):
     assert lib.paged_attn_prefill_varlen(nul, nul, -1, 3, nul, nul, 5, 5, nul, 4, nul, 1,
                                          ctypes.byref(p), nul) == B.PKV_ERR_INVALID
     p8 = _p(kv_cache_dtype=B.PKV_CACHE_FP8_E4M3, k_scale=0.02, v_scale=0.02)
+    assert lib.paged_attn_prefill_varlen(nul, nul, 10, 3, nul, nul, 0, 5, nul, 4, nul, 1,
+                                         ctypes.byref(p8), nul) == B.PKV_OK
     assert lib.paged_attn_prefill_varlen(nul, nul, 10, 3, nul, nul, 5, 5, nul, 4, nul, 1,
-                                         ctypes.byref(p8), nul) == B.PKV_ERR_UNSUPPORTED
+                                         ctypes.byref(p8), nul) == B.PKV_ERR_INVALID
 
 
 def test_workspace_size_is_host_only(lib):

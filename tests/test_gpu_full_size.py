@@ -82,6 +82,30 @@ def test_encoder_varlen_prefill_full():
     assert_close(out[rows], ref[rows], "encoder_varlen_prefill")
 
 
+def test_llama3_8b_decode_fp8_full():
+    w = W.make_config(7)
+    r = GpuRun(w)
+    ref_cache = _write_and_check(w, r)
+    out = r.decode()
+    assert_no_device_error("fp8 decode")
+    seqs = _sample_seqs(w.seq_lens)
+    ref = O.paged_attn_decode(w.query, ref_cache, w.block_tables, w.seq_lens,
+                              oracle_params(w), seqs=seqs)
+    assert_close(out[seqs], ref[seqs], "llama3_8b_decode_fp8")
+
+
+def test_varlen_prefill_fp8_full():
+    w = W.make_config(8)
+    r = GpuRun(w)
+    ref_cache = _write_and_check(w, r)
+    out = r.prefill()
+    assert_no_device_error("fp8 prefill")
+    q, cuq, cuk, bt, _, _ = w.prefill_slices()
+    rows = _sample_rows(cuq, per_seq=2)
+    ref = O.paged_attn_prefill_varlen(q, cuq, cuk, ref_cache, bt, oracle_params(w), rows=rows)
+    assert_close(out[rows], ref[rows], "varlen_prefill_fp8")
+
+
 def test_mixed_chunked_alibi_full():
     w = W.make_config(4)
     r = GpuRun(w)

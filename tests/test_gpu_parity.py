@@ -364,12 +364,65 @@ def test_fp8_copy_and_swap_move_codes():
     assert torch.equal(host, ref_host)
 
 
-def test_fp8_prefill_and_dtype_mismatch_rejected():
+def scaled_q(w, f):
+    """Queries times f, softmax scale divided by f: the same scores, query
+    magnitudes far outside fp16's normal range (f = 3e4 or 1e-6)."""
+    w.query = (w.query.float() * f).to(w.dtype)
+    w.scale = w.scale / f
+    return w
+
+
+FP8_PREFILL_CASES = {
+    "varlen_qpk4": lambda: fp8(small(101, H=32, KVH=8, seq_lens=[1, 17, 64, 65, 130, 300],
+                                     query_lens=[1, 17, 64, 65, 130, 300], P=6)),
+    "chunked_ctx": lambda: fp8(chunked(102, [0, 5, 64, 100, 333], [70, 1, 64, 129, 40])),
+    "chunked_alibi": lambda: fp8(chunked(103, [13, 200, 0], [150, 64, 90], alibi=True, H=8,
+                                         KVH=2)),
+    "window_chunked": lambda: fp8(chunked(104, [120, 9], [200, 33], window=64)),
+    "fp16_d64": lambda: fp8(chunked(105, [0, 31], [100, 70], dtype=torch.float16, D=64, H=4,
+                                    KVH=2)),
+    "bf16_d64_alibi": lambda: fp8(chunked(106, [40, 0], [90, 200], D=64, alibi=True)),
+    "block32_qpk1": lambda: fp8(chunked(107, [40, 0], [90, 200], bs=32, H=4, KVH=4)),
+    "noncausal_rowpair": lambda: fp8(chunked(108, [5, 0], [300, 140], causal=False, H=3,
+                                             KVH=3)),
+    "huge_queries": lambda: scaled_q(fp8(chunked(109, [0, 50], [200, 77], H=8, KVH=2)), 3e4),
+    "tiny_queries": lambda: scaled_q(fp8(chunked(110, [0, 50], [200, 77], H=8, KVH=2)), 1e-6),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FP8_PREFILL_CASES))
+def test_prefill_fp8_parity(case):
+    w = FP8_PREFILL_CASES[case]()
+    r = GpuRun(w)
+    r.write()
+    out = r.prefill()
+    assert_no_device_error(case)
+    ref_cache = oracle_cache_after_write(w)
+    assert torch.equal(r.cache.cpu(), ref_cache)
+    q, cuq, cuk, bt, _, _ = w.prefill_slices()
+    ref = O.paged_attn_prefill_varlen(q, cuq, cuk, ref_cache, bt, oracle_params(w))
+    assert_close(out, ref, case)
+
+
+def test_fp8_prefill_last_row_equals_fp8_decode():
+    lens = [33, 130, 257]
+    w = fp8(small(111, H=32, KVH=8, seq_lens=lens, query_lens=lens, P=3))
+    r = GpuRun(w)
+    r.write()
+    pre = r.prefill()
+    last = torch.tensor([sum(lens[:k + 1]) - 1 for k in range(3)]).to(DEV)
+    q = r.query[last].contiguous()
+    out = torch.empty_like(q)
+    n = B.paged_attn_decode_workspace_size(3, max(lens), r.p)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=DEV)
+    B.paged_attn_decode(out, q, r.cache, r.tables, w.seq_lens.to(DEV), max(lens), r.p, ws)
+    assert_no_device_error("fp8 cross path")
+    assert (pre[last].double() - out.double()).abs().max().item() <= 2e-2
+
+
+def test_fp8_dtype_mismatch_rejected():
     w = fp8(small(99, seq_lens=[40], query_lens=[40], P=1))
     r = GpuRun(w)
-    with pytest.raises(B.PkvError) as e:
-        r.prefill()
-    assert e.value.status == B.PKV_ERR_UNSUPPORTED
     wide = torch.zeros(w.kv_cache.shape, dtype=w.dtype, device=DEV)
     with pytest.raises(ValueError):   # a 2-byte cache under fp8 params
         B.kv_cache_write(r.key, r.value, wide, r.slots, r.p)
