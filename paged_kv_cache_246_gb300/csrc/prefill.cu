@@ -98,24 +98,27 @@ struct Lay {
   static constexpr int NREG = D / 64;
   static constexpr int TILE = REG * NREG;
   static constexpr int TILE8 = BN * D;  // one key tile of 8-bit codes
-  static constexpr bool STG_SEP = KV8 && D == 64;  // codes get their own area
+  // 16-bit K / V stages.  Over an fp8 cache fewer, plus N8K / N8V staging
+  // areas for the K / V tiles' codes, each refilled as soon as its codes have
+  // been widened; SPLIT: warp 2 widens every K tile and warp 3 every V tile
+  // (else both widen half the rows of each).
+  static constexpr int NK = KV8 ? 1 : NSTK, NV = KV8 ? 2 : NSTV;
+  static constexpr int N8K = 2, N8V = 2;
+  static constexpr bool SPLIT = false;
   static constexpr int OFF_Q = 0;  // two Q tiles
   static constexpr int OFF_K = 2 * TILE;
-  static constexpr int OFF_V = OFF_K + NSTK * TILE;
-  static constexpr int OFF_STG = OFF_V + NSTV * TILE;
-  static constexpr int OFF_BAR = OFF_STG + (STG_SEP ? (NSTK + NSTV) * TILE8 : 0);
-  // B_KF / B_VF: stage ready for the MMA; B_K8F / B_V8F: codes landed (fp8)
-  static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NSTK, B_EK = B_VF + NSTV,
-                       B_EV = B_EK + NSTK, B_SF = B_EV + NSTV, B_PF = B_SF + 2, B_O = B_PF + 2,
-                       B_FIN = B_O + 2, B_Q2 = B_FIN + 1, B_K8F = B_Q2 + 1,
-                       B_V8F = B_K8F + NSTK, NBAR = B_V8F + NSTV;
-  // 8-bit codes of stage s of K (kv = 0) or V (kv = 1)
-  static __device__ __forceinline__ uint8_t *codes(uint8_t *smem, int kv, int s) {
-    if constexpr (STG_SEP) return smem + OFF_STG + (kv ? NSTK + s : s) * TILE8;
-    else return smem + (kv ? OFF_V : OFF_K) + s * TILE + REG;
-  }
+  static constexpr int OFF_V = OFF_K + NK * TILE;
+  static constexpr int OFF_STG = OFF_V + NV * TILE;  // N8K K code tiles, then N8V V
+  static constexpr int OFF_BAR = OFF_STG + (KV8 ? (N8K + N8V) * TILE8 : 0);
+  // B_KF / B_VF: stage ready for the MMA; B_EK / B_EV: stage consumed by the
+  // MMA; B_K8F / B_V8F: codes landed; B_E8K / B_E8V: codes widened; B_QS:
+  // a query tile's largest magnitude gathered; B_Q2: its fp16 copy ready
+  static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NK, B_EK = B_VF + NV, B_EV = B_EK + NK,
+                       B_SF = B_EV + NV, B_PF = B_SF + 2, B_O = B_PF + 2, B_FIN = B_O + 2,
+                       B_Q2 = B_FIN + 1, B_QS = B_Q2 + 2, B_K8F = B_QS + 2, B_V8F = B_K8F + N8K,
+                       B_E8K = B_V8F + N8V, B_E8V = B_E8K + N8K, NBAR = B_E8V + N8V;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int BYTES = OFF_MISC + 32;
+  static constexpr int BYTES = OFF_MISC + 64;
   // + alignment slack; at least ~118 KB so that one CTA owns an SM (and all
   // of its tensor memory)
   static constexpr int ALLOC = (BYTES + 1024) > 118 * 1024 ? (BYTES + 1024) : 118 * 1024;
@@ -155,14 +158,15 @@ struct AB<FP16> {
   static constexpr int v = 0;
 };
 
-// Four E4M3 codes (low byte first) -> two fp16 pairs, exactly.
+// Four E4M3 codes (low byte first) -> two fp16 pairs (low half first),
+// exactly: every E4M3 value is an fp16 value.
 __device__ __forceinline__ uint2 e4m3x4_to_h4(uint32_t u) {
-  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(u & 0xffffu), __NV_E4M3);
-  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(u >> 16), __NV_E4M3);
-  return make_uint2(static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16),
-                    static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16));
+  uint2 r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(r.x), "=r"(r.y)
+      : "r"(u));
+  return r;
 }
 
 // One query tile of the CTA: head, first row within the sequence, rows,
@@ -177,8 +181,12 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
                   const __grid_constant__ CUtensorMap kvmap, int pair_heads) {
   using L = Lay<D, KV8>;
   using OPT = std::conditional_t<KV8, FP16, T>;  // MMA operand type (and P)
-  constexpr int KFT = KV8 ? L::B_K8F : L::B_KF;   // barrier the K copies complete on
-  constexpr int VFT = KV8 ? L::B_V8F : L::B_VF;
+  constexpr int NK = L::NK, NV = L::NV;  // 16-bit K / V stages
+  // barriers the K / V copies complete on, and how many stages they have
+  constexpr int KFT = KV8 ? L::B_K8F : L::B_KF, VFT = KV8 ? L::B_V8F : L::B_VF;
+  constexpr int NKT = KV8 ? L::N8K : NK, NVT = KV8 ? L::N8V : NV;
+  // bf16 queries over an fp8 cache are rewritten as fp16 by their softmax warps
+  constexpr bool QCONV = KV8 && std::is_same<T, BF16>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -243,10 +251,12 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::NBAR; ++i) {
       uint32_t count = (i == L::B_PF || i == L::B_PF + 1) ? 128 : 1;
-      // over an fp8 cache the converter warps release Q (warp 2) and the
-      // stages (warps 2 and 3)
-      if (KV8 && i == L::B_Q2) count = 32;
-      if (KV8 && i >= L::B_KF && i < L::B_VF + NSTV) count = 64;
+      // the softmax warps of a tile release its fp16 queries; the stages and
+      // staging areas are released by the converter warp(s) that widen them
+      if (KV8 && (i == L::B_Q2 || i == L::B_Q2 + 1 || i == L::B_QS || i == L::B_QS + 1))
+        count = 128;
+      if (KV8 && ((i >= L::B_KF && i < L::B_VF + NV) || (i >= L::B_E8K && i < L::B_E8V + L::N8V)))
+        count = L::SPLIT ? 32 : 64;
       mbar_init(&bars[i], count);
     }
     misc[1] = 0;  // abort flag
@@ -296,36 +306,50 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     for (int j = 0; j < ntiles; ++j) {
       const int coord = next;
       next = coord_of(j + 1);  // table entries of the next tile, fetched early
-      const int sk = j % NSTK;
-      if (j >= NSTK && !warp_wait(&bars[L::B_EK + sk], ((j / NSTK) - 1) & 1, abort_flag, where))
+      if constexpr (KV8) {
+        // codes into a staging area once the tile that used it was widened
+        constexpr int N8K = L::N8K, N8V = L::N8V;
+        const int sk8 = j % N8K, sv8 = j % N8V;
+        if (j >= N8K &&
+            !warp_wait(&bars[L::B_E8K + sk8], ((j / N8K) - 1) & 1, abort_flag, where))
+          break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars[L::B_K8F + sk8], L::TILE8);
+        __syncwarp();
+        if (lane < TB)
+          tma_load_4d(smem + L::OFF_STG + sk8 * L::TILE8 + lane * BS * D, &kvmap,
+                      &bars[L::B_K8F + sk8], 0, g, coord, 0);
+        jk = j + 1;
+        if (j >= N8V &&
+            !warp_wait(&bars[L::B_E8V + sv8], ((j / N8V) - 1) & 1, abort_flag, where))
+          break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars[L::B_V8F + sv8], L::TILE8);
+        __syncwarp();
+        if (lane < TB)
+          tma_load_4d(smem + L::OFF_STG + (N8K + sv8) * L::TILE8 + lane * BS * D, &kvmap,
+                      &bars[L::B_V8F + sv8], 0, g, coord, 1);
+        jv = j + 1;
+        continue;
+      }
+      const int sk = j % NK;
+      if (j >= NK && !warp_wait(&bars[L::B_EK + sk], ((j / NK) - 1) & 1, abort_flag, where))
         break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[KFT + sk], KV8 ? L::TILE8 : L::TILE);
+      if (lane == 0) mbar_arrive_expect_tx(&bars[L::B_KF + sk], L::TILE);
       __syncwarp();
       if (lane < TB) {
-        if constexpr (KV8) {
-          tma_load_4d(L::codes(smem, 0, sk) + lane * BS * D, &kvmap, &bars[KFT + sk], 0, g, coord,
-                      0);
-        } else {
-          uint8_t *kd = smem + L::OFF_K + sk * L::TILE + lane * BS * 128;
-          for (int r = 0; r < L::NREG; ++r)
-            tma_load_4d(kd + r * L::REG, &kvmap, &bars[KFT + sk], 64 * r, g, coord, 0);
-        }
+        uint8_t *kd = smem + L::OFF_K + sk * L::TILE + lane * BS * 128;
+        for (int r = 0; r < L::NREG; ++r)
+          tma_load_4d(kd + r * L::REG, &kvmap, &bars[L::B_KF + sk], 64 * r, g, coord, 0);
       }
       jk = j + 1;
-      const int sv = j % NSTV;
-      if (j >= NSTV && !warp_wait(&bars[L::B_EV + sv], ((j / NSTV) - 1) & 1, abort_flag, where))
+      const int sv = j % NV;
+      if (j >= NV && !warp_wait(&bars[L::B_EV + sv], ((j / NV) - 1) & 1, abort_flag, where))
         break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[VFT + sv], KV8 ? L::TILE8 : L::TILE);
+      if (lane == 0) mbar_arrive_expect_tx(&bars[L::B_VF + sv], L::TILE);
       __syncwarp();
       if (lane < TB) {
-        if constexpr (KV8) {
-          tma_load_4d(L::codes(smem, 1, sv) + lane * BS * D, &kvmap, &bars[VFT + sv], 0, g, coord,
-                      1);
-        } else {
-          uint8_t *vd = smem + L::OFF_V + sv * L::TILE + lane * BS * 128;
-          for (int r = 0; r < L::NREG; ++r)
-            tma_load_4d(vd + r * L::REG, &kvmap, &bars[VFT + sv], 64 * r, g, coord, 1);
-        }
+        uint8_t *vd = smem + L::OFF_V + sv * L::TILE + lane * BS * 128;
+        for (int r = 0; r < L::NREG; ++r)
+          tma_load_4d(vd + r * L::REG, &kvmap, &bars[L::B_VF + sv], 64 * r, g, coord, 1);
       }
       jv = j + 1;
     }
@@ -352,7 +376,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     int k_ready = -1;  // highest key tile known to have landed
     auto need_k = [&](int j) -> bool {
       if (j <= k_ready) return true;
-      if (!wait_or_abort(&bars[L::B_KF + j % NSTK], (j / NSTK) & 1, abort_flag, where))
+      if (!wait_or_abort(&bars[L::B_KF + j % NK], (j / NK) & 1, abort_flag, where))
         return false;
       tc5::fence_after_sync();
       k_ready = j;
@@ -360,7 +384,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     };
     auto qk = [&](int x, int j) {
       const uint64_t qb = q_desc + static_cast<uint64_t>((x * L::TILE) >> 4);
-      const uint64_t kb = k_desc + static_cast<uint64_t>(((j % NSTK) * L::TILE) >> 4);
+      const uint64_t kb = k_desc + static_cast<uint64_t>(((j % NK) * L::TILE) >> 4);
       const uint32_t sb = tmem + x * 128;
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
@@ -369,7 +393,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       }
       tc5::commit(&bars[L::B_SF + x]);
     };
-    bool ok = wait_or_abort(&bars[KV8 ? L::B_Q2 : L::B_Q], 0, abort_flag, where);
+    bool ok = wait_or_abort(&bars[QCONV ? L::B_Q2 : L::B_Q], 0, abort_flag, where);
+    if (QCONV && ok && qt[1].rows > 0) ok = wait_or_abort(&bars[L::B_Q2 + 1], 0, abort_flag, where);
     if (ok && ntiles > 0) {
       ok = need_k(0);
       if (ok) {
@@ -402,8 +427,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       return true;
     };
     for (int j = 0; ok && j < ntiles; ++j) {
-      const int sv = j % NSTV;
-      if (!wait_or_abort(&bars[L::B_VF + sv], (j / NSTV) & 1, abort_flag, where)) break;
+      const int sv = j % NV;
+      if (!wait_or_abort(&bars[L::B_VF + sv], (j / NV) & 1, abort_flag, where)) break;
       // Positions past the sequence end inside its last cache block hold
       // whatever the cache holds there (possibly non-finite); their P is
       // exactly 0, but 0 * NaN is NaN, so those V rows are zeroed before the
@@ -420,7 +445,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       }
       if (!step(0, j, sv, pf_a) || !step(1, j, sv, pf_b)) break;
       tc5::commit(&bars[L::B_EV + sv]);                                  // V(j) after its PVs
-      if (j + 1 < ntiles) tc5::commit(&bars[L::B_EK + (j + 1) % NSTK]);  // K(j+1) after its QKs
+      if (j + 1 < ntiles) tc5::commit(&bars[L::B_EK + (j + 1) % NK]);  // K(j+1) after its QKs
     }
     // every MMA this thread issued has completed before TMEM is released
     tc5::commit(&bars[L::B_FIN]);
@@ -429,63 +454,66 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     // ------------------------------------------------------------ fp8 widening
     const int cw = warp - 2;
     bool ok = true;
-    if (cw == 0) {  // queries: warp 2 alone (no cross-warp barrier to wait on)
-      ok = warp_wait(&bars[L::B_Q], 0, abort_flag, where);
-    }
-    if (cw == 0 && ok) {
-      int e = 0;  // queries become fp16 * 2^-e
-      if constexpr (std::is_same<T, BF16>::value) {
-        const int nchunk = (qt[1].rows > 0 ? 2 : 1) * L::TILE / 16;
-        uint4 *q4 = reinterpret_cast<uint4 *>(smem + L::OFF_Q);
-        uint32_t am = 0;  // per-halfword max of |bf16| bit patterns
-        for (int c = lane; c < nchunk; c += 32) {
-          const uint4 u = q4[c];
-          am = __vmaxu2(am, __vmaxu2(__vmaxu2(u.x & 0x7fff7fffu, u.y & 0x7fff7fffu),
-                                     __vmaxu2(u.z & 0x7fff7fffu, u.w & 0x7fff7fffu)));
-        }
-        am = __reduce_max_sync(0xffffffffu, max(am & 0xffffu, am >> 16));
-        const int E = static_cast<int>(am >> 7);  // bf16 exponent field of the largest |q|
-        // largest |q| * 2^-e in [2^14, 2^15): inside fp16's range, full precision
-        e = E == 0 ? 0 : min(64, max(-64, E - 141));
-        const float mul = __int_as_float((127 - e) << 23);
-        for (int c = lane; c < nchunk; c += 32) {
-          const uint4 u = q4[c];
-          uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    // Per key tile the K then the V codes are widened: with SPLIT by warp 2
+    // (K) and warp 3 (V) alone, else by both, each taking half the rows.
+    // Lane (row r0, column group cc) widens 16 codes (one 16-byte load) into
+    // two 16-byte chunks of the swizzled fp16 tile; lanes of the upper column
+    // half store their two chunks in the opposite order, so that the 8 lanes
+    // of one row never hit the same bank group in one store.
+    constexpr int LPR = D / 16, RPI = 32 / LPR;  // lanes per row, rows per pass
+    constexpr int ROWS = L::SPLIT ? BM : BM / 2;  // rows each converter warp widens
+    const int cc = lane % LPR, r0 = lane / LPR;
+    const int row_base = L::SPLIT ? 0 : cw * (BM / 2);
+    const int swap = (cc >= LPR / 2) ? 1 : 0;
+    auto widen = [&](int kv, int j) -> bool {
+      const int ns = kv ? NV : NK, n8 = kv ? L::N8V : L::N8K;
+      const int s = j % ns, s8 = j % n8;
+      if (!warp_wait(&bars[(kv ? L::B_V8F : L::B_K8F) + s8], (j / n8) & 1, abort_flag, where))
+        return false;
+      // the fp16 stage is free once the MMAs of the tile that used it are done
+      if (j >= ns &&
+          !warp_wait(&bars[(kv ? L::B_EV : L::B_EK) + s], ((j / ns) - 1) & 1, abort_flag, where))
+        return false;
+      const uint8_t *src = smem + L::OFF_STG + (kv ? L::N8K + s8 : s8) * L::TILE8;
+      uint8_t *dst = smem + (kv ? L::OFF_V : L::OFF_K) + s * L::TILE;
+      // this lane's row r = row_base + RPI * it + r0 has swizzle phase
+      // r & 7 = r0 ^ ((RPI * it) & 7); its two chunks' addresses are a
+      // lane-constant base plus a compile-time offset per pass
+      const uint8_t *ls = src + (row_base + r0) * D + cc * 16;
+      uint8_t *ld = dst + (cc / 4) * L::REG + (row_base + r0) * 128;
+      const int k0 = (2 * cc) % 8;
+      uint8_t *pa[2], *pb[2];  // [phase 0 / 4]: first, second chunk
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 f = BF16::to_f2(w[k]);
-            w[k] = FP16::from_f2(f.x * mul, f.y * mul);
-          }
-          q4[c] = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int ph = 0; ph < 2; ++ph) {
+        pa[ph] = ld + ((k0 ^ r0 ^ (4 * ph)) * 16);
+        pb[ph] = ld + (((k0 + 1) ^ r0 ^ (4 * ph)) * 16);
+        if (swap) {  // store order flipped for the upper column half
+          uint8_t *t = pa[ph];
+          pa[ph] = pb[ph];
+          pb[ph] = t;
         }
       }
-      fence_proxy_async_smem();
-      if (lane == 0) misc[4] = static_cast<uint32_t>(e);
-      mbar_arrive(&bars[L::B_Q2]);
-    }
-    // per key tile: K then V, in the order the producer issues them
-    constexpr int LPR = D / 8, RPI = 32 / LPR;  // lanes per row, rows per pass
-    const int cc = lane % LPR, r0 = lane / LPR;
-    auto widen = [&](int kv, int s, uint32_t parity) -> bool {
-      if (!warp_wait(&bars[(kv ? L::B_V8F : L::B_K8F) + s], parity, abort_flag, where))
-        return false;
-      const uint8_t *src = L::codes(smem, kv, s);
-      uint8_t *dst = smem + (kv ? L::OFF_V : L::OFF_K) + s * L::TILE;
-#pragma unroll 4
-      for (int it = 0; it < 64 / RPI; ++it) {
-        const int row = cw * 64 + it * RPI + r0;
-        const uint2 u = *reinterpret_cast<const uint2 *>(src + row * D + cc * 8);
-        __syncwarp();  // the row's codes are read before any lane rewrites it
+#pragma unroll
+      for (int it = 0; it < ROWS / RPI; ++it) {
+        const int ph = ((RPI * it) & 7) ? 1 : 0;
+        const uint4 u = *reinterpret_cast<const uint4 *>(ls + it * RPI * D);
         const uint2 h0 = e4m3x4_to_h4(u.x), h1 = e4m3x4_to_h4(u.y);
-        *reinterpret_cast<uint4 *>(dst + (cc / 8) * L::REG + row * 128 +
-                                   (((cc % 8) ^ (row & 7)) * 16)) = make_uint4(h0.x, h0.y, h1.x, h1.y);
+        const uint2 h2 = e4m3x4_to_h4(u.z), h3 = e4m3x4_to_h4(u.w);
+        // dims 16cc .. 16cc+7 and 16cc+8 .. 16cc+15 (swapped with the order)
+        const uint4 c0 = make_uint4(h0.x, h0.y, h1.x, h1.y);
+        const uint4 c1 = make_uint4(h2.x, h2.y, h3.x, h3.y);
+        *reinterpret_cast<uint4 *>(pa[ph] + it * RPI * 128) = swap ? c1 : c0;
+        *reinterpret_cast<uint4 *>(pb[ph] + it * RPI * 128) = swap ? c0 : c1;
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars[(kv ? L::B_VF : L::B_KF) + s]);
+      mbar_arrive(&bars[(kv ? L::B_E8V : L::B_E8K) + s8]);  // staging area free again
       return true;
     };
-    for (int j = 0; ok && j < ntiles; ++j)
-      ok = widen(0, j % NSTK, (j / NSTK) & 1) && widen(1, j % NSTV, (j / NSTV) & 1);
+    for (int j = 0; ok && j < ntiles; ++j) {
+      if constexpr (L::SPLIT) ok = widen(cw, j);
+      else ok = widen(0, j) && widen(1, j);
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int x = warp >= 8 ? 1 : 0;
@@ -503,9 +531,52 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     // without (then scores are scaled inside the exponent's FMA)
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    if constexpr (KV8) {  // the queries' power-of-two scale joins the score scale
-      ok = warp_wait(&bars[L::B_Q2], 0, abort_flag, where);
-      sl2 *= __int_as_float((127 + static_cast<int>(misc[4])) << 23);
+    if constexpr (QCONV) {
+      // This tile's bf16 queries become fp16 * 2^-e, e chosen from their
+      // largest magnitude (exact power-of-two scaling, inside fp16's range);
+      // 2^e joins the score scale.  The four warps exchange their maxima
+      // through an mbarrier (bounded waits: no barrier can strand a warp).
+      int e = 0;
+      ok = warp_wait(&bars[L::B_Q], 0, abort_flag, where);
+      uint4 *q4 = reinterpret_cast<uint4 *>(smem + L::OFF_Q + x * L::TILE);
+      const int tid = (warp & 3) * 32 + lane;
+      if (ok) {
+        uint32_t am = 0;  // per-halfword max of |bf16| bit patterns
+        for (int c = tid; c < L::TILE / 16; c += 128) {
+          const uint4 u = q4[c];
+          am = __vmaxu2(am, __vmaxu2(__vmaxu2(u.x & 0x7fff7fffu, u.y & 0x7fff7fffu),
+                                     __vmaxu2(u.z & 0x7fff7fffu, u.w & 0x7fff7fffu)));
+        }
+        am = __reduce_max_sync(0xffffffffu, max(am & 0xffffu, am >> 16));
+        if (lane == 0) misc[8 + x * 4 + (warp & 3)] = am;
+        mbar_arrive(&bars[L::B_QS + x]);
+        ok = warp_wait(&bars[L::B_QS + x], 0, abort_flag, where);
+      }
+      if (ok) {
+        const uint32_t am = max(max(misc[8 + x * 4], misc[9 + x * 4]),
+                                max(misc[10 + x * 4], misc[11 + x * 4]));
+        const int E = static_cast<int>(am >> 7);  // bf16 exponent field of the largest |q|
+        // largest |q| * 2^-e in [2^14, 2^15): inside fp16's range, full precision
+        e = E == 0 ? 0 : min(64, max(-64, E - 141));
+        const unsigned long long mul2 = f2pack(__int_as_float((127 - e) << 23),
+                                               __int_as_float((127 - e) << 23));
+        for (int c = tid; c < L::TILE / 16; c += 128) {
+          const uint4 u = q4[c];
+          uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float f0, f1;
+            f2unpack(fmul2(f2pack(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u)),
+                           mul2),
+                     f0, f1);
+            w[k] = FP16::from_f2(f0, f1);
+          }
+          q4[c] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[L::B_Q2 + x]);
+      }
+      sl2 *= __int_as_float((127 + e) << 23);
     }
     const int n = t.j1 - t.j0;
     for (int k = 0; ok && k < n; ++k) {
@@ -641,13 +712,13 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     // let every copy that was issued land before the CTA's memory goes away
     mbar_wait_bounded(&bars[L::B_Q], 0, where);
     const int nk = static_cast<int>(misc[2]), nv = static_cast<int>(misc[3]);
-    for (int s = 0; s < NSTK; ++s) {
-      const int t = nk - 1 - ((nk - 1 - s) % NSTK + NSTK) % NSTK;  // last K tile of stage s
-      if (t >= 0 && t % NSTK == s) mbar_wait_bounded(&bars[KFT + s], (t / NSTK) & 1, where);
+    for (int s = 0; s < NKT; ++s) {
+      const int t = nk - 1 - ((nk - 1 - s) % NKT + NKT) % NKT;  // last K tile of stage s
+      if (t >= 0 && t % NKT == s) mbar_wait_bounded(&bars[KFT + s], (t / NKT) & 1, where);
     }
-    for (int s = 0; s < NSTV; ++s) {
-      const int t = nv - 1 - ((nv - 1 - s) % NSTV + NSTV) % NSTV;
-      if (t >= 0 && t % NSTV == s) mbar_wait_bounded(&bars[VFT + s], (t / NSTV) & 1, where);
+    for (int s = 0; s < NVT; ++s) {
+      const int t = nv - 1 - ((nv - 1 - s) % NVT + NVT) % NVT;
+      if (t >= 0 && t % NVT == s) mbar_wait_bounded(&bars[VFT + s], (t / NVT) & 1, where);
     }
   }
   __syncthreads();
