@@ -82,7 +82,7 @@ typedef enum pkv_cache_dtype { PKV_CACHE_AUTO = 0, PKV_CACHE_FP8_E4M3 = 1 } pkv_
  * cache block size and the element type.
  *   num_heads % num_kv_heads == 0 (xformers.py XFormersImpl.__init__);
  *     query head h reads KV head h / (num_heads / num_kv_heads).
- *   head_size: 64 or 128.  block_size: 8, 16, 32 or 64.
+ *   head_size: 64 or 128.  block_size: 16 or 32 (others: PKV_ERR_UNSUPPORTED).
  *   scale: > 0, multiplies q.k before the softmax.
  *   alibi_slopes: device fp32[num_heads] or NULL; adds slope_h * (j - i) to
  *     the score of key position j for query position i
@@ -97,9 +97,11 @@ typedef enum pkv_cache_dtype { PKV_CACHE_AUTO = 0, PKV_CACHE_FP8_E4M3 = 1 } pkv_
  *     together with non_causal is PKV_ERR_UNSUPPORTED.
  *   kv_cache_dtype: pkv_cache_dtype.  With PKV_CACHE_FP8_E4M3 the cache holds
  *     one byte per element ([2][num_blocks][block_size * num_kv_heads *
- *     head_size] codes) and k_scale, v_scale (finite, > 0) apply; the write,
- *     decode, copy and swap calls support it; prefill over an fp8 cache
- *     returns PKV_ERR_UNSUPPORTED.
+ *     head_size] codes) and k_scale, v_scale (finite, > 0) apply; every call
+ *     supports it.  Decode computes in fp32 from the exact code values;
+ *     prefill multiplies on fp16 operands (exact for the codes) with each
+ *     128-row tile of bf16 queries rewritten as fp16 times a power of two
+ *     chosen from the tile's largest magnitude, so no query overflows fp16.
  */
 typedef struct pkv_attn_params {
   int32_t num_heads;
