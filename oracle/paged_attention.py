@@ -364,6 +364,56 @@ def paged_attn_decode(query: torch.Tensor, kv_cache: torch.Tensor,
     return out
 
 
+def multi_decode_position(seq_len: int, query_len: int, t: int) -> int:
+    """Position of query token t (0-based) of a decode of query_len tokens.
+
+    A decode with speculative tokens appends query_len = 1 + k tokens; the
+    sequence length seq_len counts them all (as for a single-token decode,
+    xformers.py ``XFormersMetadata`` context_len note), so they are the last
+    query_len positions: seq_len - query_len + t.
+    """
+    return seq_len - query_len + t
+
+
+def paged_attn_decode_multi(query: torch.Tensor, kv_cache: torch.Tensor,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                            query_len: int, p: AttnParams,
+                            seqs: Optional[Sequence[int]] = None) -> torch.Tensor:
+    """A uniform batch of decodes of query_len tokens each (speculative).
+
+    backends.utils ``AttentionCGSupport.UNIFORM_BATCH``: every decode in the
+    batch has the same query length, 1 + num_speculative_tokens
+    (``AttentionMetadataBuilder._init_reorder_batch_threshold`` pulls such
+    decodes to the front for spec-as-decode kernels).  query is
+    [num_seqs * query_len, num_heads * head_size], sequence b's tokens at rows
+    b * query_len + t; token t sits at ``multi_decode_position`` and attends
+    causally (and within the window) to the keys read through block_tables.
+    A sequence with seq_len 0 (padding) gives zero rows.  Returns fp64
+    [num_seqs * query_len, num_heads * head_size]; sequences not in ``seqs``
+    (if given) are left NaN.
+    """
+    B = seq_lens.numel()
+    H, D, qpk = p.num_heads, p.head_size, p.queries_per_kv
+    q_all = query.to(F64).view(B, query_len, H, D)
+    out = torch.full((B * query_len, H * D), float("nan"), dtype=F64)
+    window = _window(p, False)
+    for b in (range(B) if seqs is None else seqs):
+        L = int(seq_lens[b])
+        rows = slice(b * query_len, (b + 1) * query_len)
+        if L == 0:
+            out[rows] = 0.0
+            continue
+        assert L >= query_len, "a decode cannot hold more tokens than its sequence"
+        K, V = gather_kv(kv_cache, block_tables[b], L, p)
+        pos = [multi_decode_position(L, query_len, t) for t in range(query_len)]
+        for h in range(H):
+            g = kv_head_of(h, qpk)
+            o = attend_rows(q_all[b, :, h], pos, K[:, g], V[:, g], p.scale,
+                            _slope(p, h), window)
+            out[rows, h * D:(h + 1) * D] = o
+    return out
+
+
 def decode_split_partials(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
                           i: int, scale: float, slope: Optional[float],
                           window: int, split_tokens: int):

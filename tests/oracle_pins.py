@@ -499,6 +499,46 @@ def pin_fp8_cache_equals_bf16_cache_of_its_values():
     assert int(c8[0].view(6, bs, KVH * D)[2, 0, 0]) == O.e4m3_encode(float(key[0, 0]) / 0.125)
 
 
+def pin_multi_decode_equals_sdpa_last_rows():
+    """A decode of q tokens at length L is the last q rows of the causal SDPA
+    of length L (library routine), for q = 1 .. 4."""
+    g = torch.Generator().manual_seed(31)
+    p = _params(H=8, KVH=2, D=16, bs=4, scale=0.3)
+    lens = [4, 7, 13, 16]
+    Ks, Vs = _rand_seqs(g, lens, p.num_kv_heads, p.head_size)
+    cache, tables = paged_from_contiguous(Ks, Vs, p, g)
+    sl = torch.tensor(lens, dtype=torch.int32)
+    for q in (1, 2, 4):
+        Q = torch.randn(len(lens) * q, p.num_heads * p.head_size, generator=g).to(torch.bfloat16)
+        out = O.paged_attn_decode_multi(Q, cache, tables, sl, q, p)
+        for b, (L, K, V) in enumerate(zip(lens, Ks, Vs)):
+            qf = torch.randn(L, p.num_heads, p.head_size, generator=g).to(torch.bfloat16)
+            qf[L - q:] = Q[b * q:(b + 1) * q].view(q, p.num_heads, p.head_size)
+            ref = _sdpa_causal(qf, K, V, p)[L - q:]
+            _close(out[b * q:(b + 1) * q], ref, what=f"multi decode q={q} L={L}")
+
+
+def pin_multi_decode_cross_paths():
+    """q = 1 is the single-token decode; q tokens are the chunked prefill of
+    the last q rows (window and ALiBi on); padding sequences are zero."""
+    g = torch.Generator().manual_seed(32)
+    p = _params(H=4, KVH=2, D=8, bs=4, slopes=[0.3, 0.2, 0.1, 0.05], window=6)
+    lens = [3, 9, 14]
+    Ks, Vs = _rand_seqs(g, lens, 2, 8)
+    cache, tables = paged_from_contiguous(Ks, Vs, p, g)
+    sl = torch.tensor(lens, dtype=torch.int32)
+    Q1 = torch.randn(3, 32, generator=g).to(torch.bfloat16)
+    _close(O.paged_attn_decode_multi(Q1, cache, tables, sl, 1, p),
+           O.paged_attn_decode(Q1, cache, tables, sl, p), tol=1e-13, what="q=1 vs decode")
+    q = 3
+    Q3 = torch.randn(3 * q, 32, generator=g).to(torch.bfloat16)
+    pre = O.paged_attn_prefill_varlen(Q3, _cu([q] * 3), _cu(lens), cache, tables, p)
+    _close(O.paged_attn_decode_multi(Q3, cache, tables, sl, q, p), pre, tol=1e-13,
+           what="multi decode vs chunked prefill")
+    z = O.paged_attn_decode_multi(Q3, cache, tables, torch.tensor([0, 9, 14]), q, p)
+    assert torch.equal(z[:q], torch.zeros(q, 32, dtype=F64))
+
+
 def pin_empty_decode_row_is_zero():
     p = _params(H=2, KVH=1, D=4, bs=4)
     cache = torch.randn(2, 2, 16).to(torch.bfloat16)

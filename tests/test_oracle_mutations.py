@@ -76,6 +76,9 @@ def _attend_always_causal(q, positions, K, V, scale, slope, window, causal=True)
 
 
 MUTATIONS["noncausal_ignored"] = ("attend_rows", _attend_always_causal)
+# speculative tokens placed one position too early / counted from the front
+MUTATIONS["multi_position_off"] = ("multi_decode_position", lambda L, q, t: L - q + t - 1)
+MUTATIONS["multi_position_front"] = ("multi_decode_position", lambda L, q, t: t)
 
 
 def _encode_truncating(x):
