@@ -6,7 +6,8 @@ needed blocks + 10%, tables randomly permuted).  One step = kv_cache_write of
 the 256 new tokens, then paged_attn_decode (split-KV pass + combine).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode|prefill|mixed|swa]
+                  [--workload decode|prefill|mixed|swa|encoder|decode_fp8|prefill_fp8|
+                              spec_decode]
 
 Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own
 replica of the workload on its own GPU (the path has no exchange step), so
@@ -36,7 +37,7 @@ from paged_kv_cache_246_gb300 import workloads as W  # noqa: E402
 
 METRIC = ("decode tokens/s and HBM GB/s (%peak); prefill TFLOP/s (%bf16 peak), 1×GB300")
 CFG_OF = {"decode": 2, "prefill": 3, "mixed": 4, "swa": 5, "encoder": 6, "decode_fp8": 7,
-          "prefill_fp8": 8}
+          "prefill_fp8": 8, "spec_decode": 9}
 
 
 def peaks():
@@ -127,9 +128,14 @@ class Step:
         if self.has_prefill:
             q, cuq, cuk, bt, mq, mk = w.prefill_slices()
             self.cuq, self.cuk, self.mq, self.mk = cuq.to(dev), cuk.to(dev), mq, mk
+        self.mq_len = w.multi_query_len
         if self.has_decode:
             self.dmax = int(w.seq_lens[P:].max())
-            n = B.paged_attn_decode_workspace_size(w.num_seqs - P, self.dmax, self.p)
+            if self.mq_len:
+                n = B.paged_attn_decode_multi_workspace_size(w.num_seqs, self.mq_len, self.dmax,
+                                                             self.p)
+            else:
+                n = B.paged_attn_decode_workspace_size(w.num_seqs - P, self.dmax, self.p)
             self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
             self.multi_split = n > 0
         self.ev = []
@@ -155,7 +161,10 @@ class Step:
         if mark:
             e1 = torch.cuda.Event(enable_timing=True)
             e1.record()
-        if self.has_decode:
+        if self.has_decode and self.mq_len:
+            B.paged_attn_decode_multi(self.out, self.query, self.cache, self.tables,
+                                      self.seq_lens, self.mq_len, self.dmax, self.p, self.ws)
+        elif self.has_decode:
             B.paged_attn_decode(self.out[self.Tp:], self.query[self.Tp:], self.cache,
                                 self.tables[self.P:], self.seq_lens[self.P:], self.dmax, self.p,
                                 self.ws)
@@ -172,11 +181,13 @@ def algorithmic(w: W.Workload):
     kv_el = 1 if w.kv_cache_dtype == "fp8_e4m3" else 2   # cache bytes per element
     row = w.num_kv_heads * w.head_size
     dec_bytes = 0
+    mq = max(1, w.multi_query_len)   # query tokens per decoding sequence
     for L in w.seq_lens[P:].tolist():
-        keys = min(L, w.sliding_window) if w.sliding_window > 0 else L
+        # keys visible to any of the sequence's query tokens
+        keys = min(L, w.sliding_window + mq - 1) if w.sliding_window > 0 else L
         dec_bytes += keys * row * kv_el * 2       # K and V of every visible token
     nd = w.num_seqs - P
-    dec_bytes += nd * w.num_heads * w.head_size * el * 2   # query in, output out
+    dec_bytes += nd * mq * w.num_heads * w.head_size * el * 2   # query in, output out
     flops = 0
     for q, L in zip(w.query_lens[:P].tolist(), w.seq_lens[:P].tolist()):
         c = L - q
@@ -313,19 +324,24 @@ def oracle_rate(w: W.Workload, budget_s: float):
     done, t_attn = 0, 0.0
     if w.num_seqs > P:
         q, bt, sl, _ = w.decode_slices()
-        order = torch.randperm(q.shape[0], generator=torch.Generator().manual_seed(0)).tolist()
+        nseq = sl.numel()
+        mq = max(1, w.multi_query_len)
+        order = torch.randperm(nseq, generator=torch.Generator().manual_seed(0)).tolist()
         for b in order:
             t1 = time.perf_counter()
-            O.paged_attn_decode(q, ref, bt, sl, op, seqs=[b])
+            if w.multi_query_len:
+                O.paged_attn_decode_multi(q, ref, bt, sl, mq, op, seqs=[b])
+            else:
+                O.paged_attn_decode(q, ref, bt, sl, op, seqs=[b])
             t_attn += time.perf_counter() - t1
             done += 1
             if t_attn > budget_s:
                 break
         per_seq = t_attn / done
-        step_s = t_write + per_seq * q.shape[0]
-        return {"value": q.shape[0] / step_s, "unit": "tokens/s",
+        step_s = t_write + per_seq * nseq
+        return {"value": nseq * mq / step_s, "unit": "tokens/s",
                 "sample": f"kv_cache_write of all {w.key.shape[0]} tokens + decode of {done} of "
-                          f"{q.shape[0]} sequences (random order), scaled to the full step",
+                          f"{nseq} sequences (random order), scaled to the full step",
                 "step_s": step_s}
     q, cuq, cuk, bt, _, _ = w.prefill_slices()
     _, flops = algorithmic(w)
@@ -443,7 +459,7 @@ def run_ours(args, world, rank, local):
 
     # ---- metric ------------------------------------------------------------
     if st.has_decode:
-        units = (w.num_seqs - w.num_prefill_seqs) * world
+        units = (w.num_seqs - w.num_prefill_seqs) * max(1, w.multi_query_len) * world
         value = units / (ms_step * 1e-3)
         unit = "tokens/s"
         e2e_value = units / (e2e_ms * 1e-3)
@@ -453,7 +469,9 @@ def run_ours(args, world, rank, local):
                 "traffic": profiled_traffic("decode.cu",
                                             "decode_split_kernel_llama3_8b_decode.md")
                 if cfg == 2 and args.scale_down == 1 else None,
-                "kernel": "paged_attn_decode (split-KV pass + combine)",
+                "kernel": ("paged_attn_decode_multi (tensor-core split pass + combine)"
+                           if w.multi_query_len else
+                           "paged_attn_decode (split-KV pass + combine)"),
                 "peak_kind": peak_kind, "algorithmic_bytes_per_launch": dec_bytes,
                 "avg_launch_ms": dec_ms}
     else:

@@ -209,6 +209,44 @@ size_t paged_attn_decode_workspace_size(int32_t num_seqs, int32_t max_seq_len,
                                         const pkv_attn_params *params);
 
 /*
+ * paged_attn_decode_multi -- a uniform batch of decodes of query_len tokens
+ * each: speculative decoding's "decodes" of 1 + num_speculative_tokens
+ * tokens (backends.utils AttentionCGSupport.UNIFORM_BATCH; the
+ * reorder_batch_threshold of AttentionMetadataBuilder
+ * ._init_reorder_batch_threshold pulls them to the front of the batch for
+ * spec-as-decode kernels).  Token t of sequence b is the query at position
+ * seq_lens[b] - query_len + t and attends to the keys up to and including
+ * its own position (and within sliding_window), all read through the block
+ * table; the cache write of the query_len new tokens comes first.  With
+ * query_len = 1 this is paged_attn_decode.
+ *
+ *   out, query   [num_seqs * query_len][num_heads * head_size] elements,
+ *                row b * query_len + t = token t of sequence b
+ *   query_len    1 .. 64
+ *   seq_lens     int32[num_seqs]: length including the query_len new
+ *                tokens; 0 gives all-zero rows; 0 < seq_len < query_len,
+ *                or above max_seq_len or max_blocks_per_seq * block_size,
+ *                records PKV_ERR_BOUNDS and gives zero rows
+ *   workspace    >= paged_attn_decode_multi_workspace_size(...) bytes of
+ *                device scratch, 256-byte aligned (NULL when that is 0)
+ *   Other arguments as paged_attn_decode.  Caches of the model dtype only:
+ *   an fp8 cache, or non_causal, returns PKV_ERR_UNSUPPORTED.
+ */
+pkv_status paged_attn_decode_multi(void *out, const void *query, int32_t num_seqs,
+                                   int32_t query_len, const void *kv_cache,
+                                   int64_t num_blocks, const int32_t *block_tables,
+                                   int32_t max_blocks_per_seq,
+                                   const int32_t *seq_lens, int32_t max_seq_len,
+                                   const pkv_attn_params *params, void *workspace,
+                                   size_t workspace_bytes, pkv_stream_t stream);
+
+/* Bytes of workspace paged_attn_decode_multi needs (host only; 0 when no
+ * split is used or the arguments are not supported). */
+size_t paged_attn_decode_multi_workspace_size(int32_t num_seqs, int32_t query_len,
+                                              int32_t max_seq_len,
+                                              const pkv_attn_params *params);
+
+/*
  * paged_attn_prefill_varlen -- packed prompts or prompt chunks attending
  * causally to their cached context plus themselves, all K/V read from the
  * paged cache (the chunk's own K/V are stored by kv_cache_write first).

@@ -51,7 +51,8 @@ __all__ = [
     "lengths_from_cu", "gather_kv", "attend_rows", "paged_attn_decode",
     "paged_attn_prefill_varlen", "decode_split_partials",
     "combine_split_partials", "kv_copy_blocks", "kv_swap_blocks",
-    "e4m3_decode", "e4m3_encode", "fp8_quantize",
+    "e4m3_decode", "e4m3_encode", "fp8_quantize", "multi_decode_position",
+    "paged_attn_decode_multi",
 ]
 
 

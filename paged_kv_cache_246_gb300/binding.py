@@ -24,7 +24,8 @@ _DTYPES = {torch.float16: PKV_FP16, torch.bfloat16: PKV_BF16}
 
 # Every function include/pkv.h declares.
 EXPORTS = ("kv_cache_write", "paged_attn_decode", "paged_attn_decode_workspace_size",
-           "paged_attn_decode_noalloc",
+           "paged_attn_decode_noalloc", "paged_attn_decode_multi",
+           "paged_attn_decode_multi_workspace_size",
            "paged_attn_prefill_varlen", "kv_copy_blocks", "kv_swap_blocks",
            "pkv_status_string", "pkv_device_error", "pkv_abi_version")
 
@@ -63,6 +64,9 @@ def lib() -> ctypes.CDLL:
             "paged_attn_decode": (i32, [vp, vp, i32, vp, i64, vp, i32, vp, i32, P, vp, sz, vp]),
             "paged_attn_decode_workspace_size": (sz, [i32, i32, P]),
             "paged_attn_decode_noalloc": (i32, [vp, vp, i32, vp, i64, vp, i32, vp, i32, P, vp]),
+            "paged_attn_decode_multi": (i32, [vp, vp, i32, i32, vp, i64, vp, i32, vp, i32, P, vp,
+                                              sz, vp]),
+            "paged_attn_decode_multi_workspace_size": (sz, [i32, i32, i32, P]),
             "paged_attn_prefill_varlen": (i32, [vp, vp, i64, i32, vp, vp, i32, i32, vp, i64, vp,
                                                 i32, P, vp]),
             "kv_copy_blocks": (i32, [vp, i32, i64, vp, i64, P, vp]),
@@ -212,6 +216,40 @@ def paged_attn_decode_noalloc(out: torch.Tensor, query: torch.Tensor, kv_cache: 
                                            int(max_seq_len), ctypes.byref(params),
                                            _stream(stream)),
            "paged_attn_decode_noalloc")
+
+
+def paged_attn_decode_multi_workspace_size(num_seqs: int, query_len: int, max_seq_len: int,
+                                           params: AttnParams) -> int:
+    return int(lib().paged_attn_decode_multi_workspace_size(num_seqs, query_len, max_seq_len,
+                                                            ctypes.byref(params)))
+
+
+def paged_attn_decode_multi(out: torch.Tensor, query: torch.Tensor, kv_cache: torch.Tensor,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor, query_len: int,
+                            max_seq_len: int, params: AttnParams,
+                            workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Uniform batch of decodes of query_len tokens per sequence; query/out
+    rows b * query_len + t."""
+    for t, n in ((out, "out"), (query, "query"), (kv_cache, "kv_cache")):
+        _need(t, n)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    nb = _cache_blocks(kv_cache, params)
+    B = seq_lens.numel()
+    hd = params.num_heads * params.head_size
+    rows = B * int(query_len)
+    if query.numel() != rows * hd or out.numel() != rows * hd or block_tables.shape[0] != B:
+        raise ValueError("query/out/block_tables sizes disagree with seq_lens and query_len")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need(workspace, "workspace")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(lib().paged_attn_decode_multi(out.data_ptr(), query.data_ptr(), B, int(query_len),
+                                         kv_cache.data_ptr(), nb, block_tables.data_ptr(),
+                                         int(block_tables.shape[1]), seq_lens.data_ptr(),
+                                         int(max_seq_len), ctypes.byref(params), ws_ptr, ws_bytes,
+                                         _stream(stream)),
+           "paged_attn_decode_multi")
 
 
 def paged_attn_prefill_varlen(out: torch.Tensor, query: torch.Tensor, cu_seqlens_q: torch.Tensor,

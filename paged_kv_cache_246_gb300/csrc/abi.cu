@@ -132,6 +132,8 @@ static pkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKV_OK : 
 
 static bool decode_qpk_supported(int qpk) { return qpk == 1 || qpk == 2 || qpk % 4 == 0; }
 
+constexpr int32_t kMaxMultiQueryLen = 64;  // tokens per sequence of a multi-token decode
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -236,6 +238,55 @@ pkv_status paged_attn_decode_noalloc(void *out, const void *query, int32_t num_s
                            scratch_bytes, stream);
 }
 
+static bool multi_args_supported(const Geometry &g, int32_t query_len) {
+  return !g.fp8 && !g.non_causal && query_len >= 1 && query_len <= kMaxMultiQueryLen;
+}
+
+size_t paged_attn_decode_multi_workspace_size(int32_t num_seqs, int32_t query_len,
+                                              int32_t max_seq_len,
+                                              const pkv_attn_params *params) {
+  Geometry g;
+  if (make_geometry(params, 1, &g) != PKV_OK || num_seqs <= 0 || max_seq_len < 0 ||
+      !multi_args_supported(g, query_len))
+    return 0;
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) dev.sms = 152;
+  return plan_decode_multi(num_seqs, query_len, max_seq_len, g, dev.sms).workspace_bytes;
+}
+
+pkv_status paged_attn_decode_multi(void *out, const void *query, int32_t num_seqs,
+                                   int32_t query_len, const void *kv_cache, int64_t num_blocks,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *seq_lens, int32_t max_seq_len,
+                                   const pkv_attn_params *params, void *workspace,
+                                   size_t workspace_bytes, pkv_stream_t stream) {
+  Geometry g;
+  pkv_status st = make_geometry(params, num_blocks, &g);
+  if (st != PKV_OK) return st;
+  if (query_len < 1 || num_seqs < 0 || num_seqs > 65535 || max_seq_len < 0 ||
+      max_blocks_per_seq <= 0)
+    return PKV_ERR_INVALID;
+  if (!multi_args_supported(g, query_len)) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (static_cast<int64_t>(num_seqs) * query_len > 0x7fffffffLL / g.H) return PKV_ERR_UNSUPPORTED;
+  if (!out || !query || !kv_cache || !block_tables || !seq_lens) return PKV_ERR_INVALID;
+  if (!aligned(out, 16) || !aligned(query, 16) || !aligned(kv_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+    return PKV_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = select_device(s);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  DeviceInfo dev;
+  e = current_device_info(&dev);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  const MultiDecodePlan plan = plan_decode_multi(num_seqs, query_len, max_seq_len, g, dev.sms);
+  if (plan.workspace_bytes > 0 &&
+      (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16)))
+    return PKV_ERR_INVALID;
+  return from_cuda(launch_decode_multi(out, query, num_seqs, query_len, kv_cache, block_tables,
+                                       max_blocks_per_seq, seq_lens, g, plan, workspace, s));
+}
+
 pkv_status paged_attn_prefill_varlen(void *out, const void *query, int64_t num_query_tokens,
                                      int32_t num_seqs,
                                      const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
@@ -331,13 +382,14 @@ pkv_status kv_swap_blocks(const void *src_cache, int64_t src_num_blocks, void *d
 }
 
 pkv_status pkv_device_error(int64_t *detail) {
-  unsigned long long words[3] = {0, 0, 0};
-  cudaError_t (*readers[3])(unsigned long long *) = {read_device_error_kv_ops,
-                                                     read_device_error_decode,
-                                                     read_device_error_prefill};
-  for (int k = 0; k < 3; ++k)
+  constexpr int kUnits = 4;
+  unsigned long long words[kUnits] = {0, 0, 0, 0};
+  cudaError_t (*readers[kUnits])(unsigned long long *) = {
+      read_device_error_kv_ops, read_device_error_decode, read_device_error_decode_multi,
+      read_device_error_prefill};
+  for (int k = 0; k < kUnits; ++k)
     if (readers[k](&words[k]) != cudaSuccess) return PKV_ERR_CUDA;
-  for (int k = 0; k < 3; ++k) {
+  for (int k = 0; k < kUnits; ++k) {
     if (words[k]) {
       if (detail) {
         int64_t v = static_cast<int64_t>(words[k] & ((1ull << 56) - 1));

@@ -1,0 +1,543 @@
+// Multi-token (speculative) decode over the paged cache on the tensor core.
+//
+// What is computed (backends.utils AttentionCGSupport.UNIFORM_BATCH: every
+// decode of the batch has the same query length q = 1 + num_speculative_tokens;
+// AttentionMetadataBuilder._init_reorder_batch_threshold pulls such decodes to
+// the front for spec-as-decode kernels): token t of sequence b sits at
+// position i = L_b - q + t (L_b counts the q new tokens, as the single-token
+// decode's seq_len counts its one) and attends to keys lo(i) <= j <= i read
+// through the block table:
+//     s_j = scale * q.k_j + slope_h * (j - i),   out = softmax(s) . V.
+//
+// Design.  Rows are (token t, query head h of the KV group) pairs,
+// r = t * QPK + h, in groups of 16: one m16 tile of mma.sync m16n8k16 (the
+// group's rows share every K/V byte; tcgen05's smallest tile, 64 rows, would
+// leave most of it empty at these row counts, and the step is bound by HBM,
+// not by tensor throughput).  CTA = (split of the key range, KV head x row
+// group, sequence), 4 warps.  Each warp walks its own 16-token units of the
+// split (unit k of the warp = split unit warp + 4k) through a two-stage ring
+// of TMA boxes (16 tokens x 64 dims, 128-byte swizzle; K and V).  Per unit:
+//   S[16 rows x 16 keys] = Q K^T   Q fragments held in registers for the
+//                                  whole CTA, K fragments by ldmatrix;
+//   scores scaled into the log2 domain (+ ALiBi), masked per row (its own
+//   causal position and window start), online softmax per row with a lazy
+//   reference max (moved, and O rescaled, only when a score passes it by 2^8);
+//   O += P V                       P packed to bf16/fp16 pairs in registers as
+//                                  the A operand, V fragments by
+//                                  ldmatrix.trans.
+// The four warps merge their (m, l, O) through shared memory; a sequence cut
+// into several splits writes (o, m, l) partials that decode_mt_combine_kernel
+// merges.  Every wait is bounded (a timeout records PKV_ERR_TIMEOUT, drains
+// the warp's copies in flight and leaves the output unwritten for that CTA).
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace mt {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kUnit = 16;   // keys per unit (one TMA box height)
+constexpr int kRows = 16;   // rows per CTA: one m16 tile
+constexpr int kStages = 2;  // TMA ring depth per warp
+constexpr float kLazy = 8.f;
+
+struct Args {
+  void *out;
+  const uint16_t *query;
+  const int32_t *block_tables;
+  const int32_t *seq_lens;
+  const float *alibi;
+  float *part_o;   // [B * q * H][max_splits][D]
+  float *part_ml;  // [B * q * H][max_splits][2]
+  int64_t num_blocks;
+  int num_seqs, max_blocks_per_seq;
+  int H, QPK, q, rows, row_groups;
+  int BS, window, split_units, max_splits;
+  float scale_log2;
+};
+
+struct Span {
+  int L;           // length (0: padding, or a bad length that was reported)
+  int first_unit;  // unit of the first visible key of token 0
+  int nunits;      // units up to position L - 1
+  int nsplit;
+};
+
+__device__ __forceinline__ Span span_of(const Args &a, int b, bool report) {
+  Span s{};
+  int L = __ldg(a.seq_lens + b);
+  const int cap = a.max_blocks_per_seq * a.BS;
+  if (L < 0 || L > cap || (L > 0 && L < a.q)) {  // the decode must fit its sequence
+    if (report) record_error(PKV_ERR_BOUNDS, b);
+    L = 0;
+  }
+  s.L = L;
+  if (L == 0) return s;
+  const int i0 = L - a.q;  // token 0: its window starts first
+  const int lo = a.window > 0 ? max(0, i0 - a.window + 1) : 0;
+  s.first_unit = lo / kUnit;
+  s.nunits = (L - 1) / kUnit - s.first_unit + 1;
+  s.nsplit = (s.nunits + a.split_units - 1) / a.split_units;
+  if (s.nsplit > a.max_splits) {  // seq_len above the host's max_seq_len
+    if (report) record_error(PKV_ERR_BOUNDS, b);
+    s.nsplit = a.max_splits;
+  }
+  return s;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// D[16x8] += A[16x16] B[16x8], fp32 accumulate; A row-major, B column-major.
+template <class T>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1);
+template <>
+__device__ __forceinline__ void mma16816<BF16>(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<FP16>(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int D>
+struct Lay {
+  static constexpr int BOX = kUnit * 128;        // 16 rows x 64 dims x 2 B
+  static constexpr int TILE = (D / 64) * BOX;    // K (or V) of one unit
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int TILES = kWarps * kStages * STAGE;
+  static constexpr int MERGE = kWarps * kRows * (D + 2) * 4;  // reuses the tiles
+  static_assert(MERGE <= TILES, "merge buffers fit in the tile area");
+};
+
+// Byte offset, inside a unit's K or V tile, of the 16-byte chunk `chunk`
+// (8 dims) of key row `tok`: 64-dim box, row, 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(int tok, int chunk) {
+  return static_cast<uint32_t>((chunk >> 3) * (kUnit * 128) + tok * 128 +
+                               (((chunk & 7) ^ (tok & 7)) << 4));
+}
+
+template <class T, int D>
+__global__ void __launch_bounds__(kThreads, 3)
+decode_mt_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
+  using L = Lay<D>;
+  constexpr int KS = D / 16;  // k-steps of q.k
+  constexpr int NT = D / 8;   // n-tiles of p.V
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y / a.row_groups, rg = blockIdx.y % a.row_groups;
+  const int b = blockIdx.z;
+  const int H = a.H, q = a.q, QPK = a.QPK;
+  const Span sp = span_of(a, b, split == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+
+  // this lane's two rows of the m16 tile: g and g + 8
+  const int g = lane >> 2, tq = lane & 3;
+  int R[2], orow[2], pos[2], lo[2];
+  bool valid[2];
+  float slope[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    R[x] = rg * kRows + g + 8 * x;
+    valid[x] = R[x] < a.rows;
+    const int t = valid[x] ? R[x] / QPK : 0, h = valid[x] ? R[x] % QPK : 0;
+    const int head = kvh * QPK + h;
+    orow[x] = (b * q + t) * H + head;  // output row (token, head)
+    pos[x] = sp.L - q + t;
+    lo[x] = a.window > 0 ? max(0, pos[x] - a.window + 1) : 0;
+    slope[x] = (a.alibi && valid[x]) ? __ldg(a.alibi + head) * kLog2e : 0.f;
+  }
+
+  if (sp.L == 0) {  // padding (or a reported bad length): zero rows
+    if (split == 0 && warp == 0) {
+      uint16_t *o16 = static_cast<uint16_t *>(a.out);
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+        if (valid[x])
+          for (int d = tq; d < D; d += 4) o16[static_cast<int64_t>(orow[x]) * D + d] = 0;
+    }
+    return;
+  }
+  const int u_begin = sp.first_unit + split * a.split_units;
+  const int u_end = min(u_begin + a.split_units, sp.first_unit + sp.nunits);
+  if (split >= sp.nsplit || u_begin >= u_end) return;
+  const int nu = u_end - u_begin;
+
+  uint8_t *tiles = smem;
+  int32_t *coord = reinterpret_cast<int32_t *>(smem + L::TILES);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(
+      smem + L::TILES + ((a.split_units * 4 + 15) / 16) * 16);
+
+  if (threadIdx.x == 0) prefetch_tensormap(&tmap);
+  // cache row coordinate of each unit of the split, range-checked once
+  const int32_t *trow = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+  for (int k = threadIdx.x; k < nu; k += kThreads) {
+    const int p0 = (u_begin + k) * kUnit;
+    const int lb = p0 / a.BS;
+    int pb = __ldg(trow + lb);
+    if (pb < 0 || pb >= a.num_blocks) {
+      record_error(PKV_ERR_BOUNDS, static_cast<int64_t>(b) * a.max_blocks_per_seq + lb);
+      pb = 0;
+    }
+    coord[k] = pb * a.BS + p0 % a.BS;
+  }
+  uint64_t *wbar = bars + warp * kStages;
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(&wbar[st], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int my_count = nu > warp ? (nu - warp + kWarps - 1) / kWarps : 0;
+  uint8_t *wt = tiles + warp * kStages * L::STAGE;
+  auto issue = [&](int k) {
+    const int st = k % kStages;
+    const int c = coord[warp + k * kWarps];
+    mbar_arrive_expect_tx(&wbar[st], 2u * L::TILE);
+    uint8_t *kt = wt + st * L::STAGE;
+#pragma unroll
+    for (int r = 0; r < D / 64; ++r) {
+      tma_load_4d(kt + r * L::BOX, &tmap, &wbar[st], 64 * r, kvh, c, 0);
+      tma_load_4d(kt + L::TILE + r * L::BOX, &tmap, &wbar[st], 64 * r, kvh, c, 1);
+    }
+  };
+  int issued = 0;
+  if (lane == 0)
+    for (; issued < min(kStages, my_count); ++issued) issue(issued);
+
+  // ---- Q fragments (A operand, row-major 16 x 16 per k-step) ---------------
+  uint32_t qa[KS][4];
+  {
+    const uint32_t *q0 = reinterpret_cast<const uint32_t *>(a.query) +
+                         (static_cast<int64_t>(orow[0]) * D) / 2;
+    const uint32_t *q1 = reinterpret_cast<const uint32_t *>(a.query) +
+                         (static_cast<int64_t>(orow[1]) * D) / 2;
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+      qa[s][0] = valid[0] ? __ldg(q0 + 8 * s + tq) : 0u;
+      qa[s][1] = valid[1] ? __ldg(q1 + 8 * s + tq) : 0u;
+      qa[s][2] = valid[0] ? __ldg(q0 + 8 * s + 4 + tq) : 0u;
+      qa[s][3] = valid[1] ? __ldg(q1 + 8 * s + 4 + tq) : 0u;
+    }
+  }
+
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float o[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
+  // ldmatrix row addresses: lane -> (matrix mi, row rr)
+  const int mi = lane >> 3, rr = lane & 7;
+  const int k_tok = (mi >> 1) * 8 + rr, k_half = mi & 1;  // K: tokens x dim halves
+  const int v_tok = (mi & 1) * 8 + rr, v_half = mi >> 1;  // V^T: token halves x dims
+  bool ok = true;
+  int consumed = 0;
+  const float sl2 = a.scale_log2;
+
+  for (int k = 0; k < my_count; ++k) {
+    const int st = k % kStages;
+    const bool got = mbar_wait_bounded(&wbar[st], (k / kStages) & 1, b);
+    if (!__all_sync(0xffffffffu, got)) {
+      ok = false;
+      break;
+    }
+    consumed = k + 1;
+    const uint32_t kt = smem_u32(wt + st * L::STAGE);
+    const uint32_t vt = kt + L::TILE;
+    const int j0 = (u_begin + warp + k * kWarps) * kUnit;  // position of the unit's key 0
+
+    // ---- S = Q K^T: two n-tiles of 8 keys ---------------------------------
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+      uint32_t kb[4];
+      ldsm_x4(kt + swz(k_tok, 2 * s + k_half), kb);
+      mma16816<T>(sc[0], qa[s], kb[0], kb[1]);
+      mma16816<T>(sc[1], qa[s], kb[2], kb[3]);
+    }
+    // ---- scores in the log2 domain, per-row masks --------------------------
+    // sc[n][e] : row g (e < 2) or g + 8 (e >= 2), key j0 + 8n + 2tq + (e & 1)
+    float x[2][4];  // [row][n * 2 + (e & 1)]
+    bool grow = false;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = e >> 1;
+        const int j = j0 + 8 * n + 2 * tq + (e & 1);
+        float v = fmaf(sc[n][e], sl2, slope[r] * static_cast<float>(j - pos[r]));
+        if (!valid[r] || j < lo[r] || j > pos[r]) v = -INFINITY;
+        x[r][n * 2 + (e & 1)] = v;
+        grow |= v > m[r] + kLazy;
+      }
+    if (__any_sync(0xffffffffu, grow)) {
+      // move the references to the true row maxima (4 lanes hold a row)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float mx = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m[r], mx);
+        if (mn > m[r]) {
+          const float alpha = m[r] == -INFINITY ? 0.f : fast_exp2(m[r] - mn);
+          m[r] = mn;
+          l[r] *= alpha;
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            o[n][2 * r] *= alpha;
+            o[n][2 * r + 1] *= alpha;
+          }
+        }
+      }
+    }
+    // ---- P (A operand of P V): rows g / g + 8, keys 2tq.. and 8 + 2tq.. -----
+    uint32_t pa[4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float mr = m[r] == -INFINITY ? 0.f : m[r];
+      float p[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) p[c] = fast_exp2(x[r][c] - mr);
+      l[r] += (p[0] + p[1]) + (p[2] + p[3]);
+      pa[r] = T::from_f2(p[0], p[1]);      // keys 2tq, 2tq + 1
+      pa[2 + r] = T::from_f2(p[2], p[3]);  // keys 8 + 2tq, 9 + 2tq
+    }
+    // ---- O += P V: n-tiles of 8 dims, two per ldmatrix ---------------------
+#pragma unroll
+    for (int n2 = 0; n2 < NT / 2; ++n2) {
+      uint32_t vb[4];
+      ldsm_x4_t(vt + swz(v_tok, 2 * n2 + v_half), vb);
+      mma16816<T>(o[2 * n2], pa, vb[0], vb[1]);
+      mma16816<T>(o[2 * n2 + 1], pa, vb[2], vb[3]);
+    }
+    __syncwarp();  // every lane has read the stage: refill it
+    if (lane == 0 && issued < my_count) {
+      issue(issued);
+      ++issued;
+    }
+    __syncwarp();
+  }
+  issued = __shfl_sync(0xffffffffu, issued, 0);
+  if (!ok) {  // drain this warp's copies still in flight, bounded
+    for (int k = consumed; k < issued; ++k) mbar_wait_bounded(&wbar[k % kStages], (k / kStages) & 1, b);
+  }
+
+  // ---- merge the 4 warps' (m, l, O) ----------------------------------------
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+  }
+  __syncthreads();  // all TMA traffic has landed; the tile area is reusable
+  float *sM = reinterpret_cast<float *>(smem);  // [warp][row]
+  float *sL = sM + kWarps * kRows;               // [warp][row]
+  float *sO = sL + kWarps * kRows;               // [warp][row][D]
+  if (tq == 0) {
+    sM[warp * kRows + g] = ok ? m[0] : -INFINITY;
+    sM[warp * kRows + g + 8] = ok ? m[1] : -INFINITY;
+    sL[warp * kRows + g] = ok ? l[0] : 0.f;
+    sL[warp * kRows + g + 8] = ok ? l[1] : 0.f;
+  }
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    float *r0 = sO + (warp * kRows + g) * D + 8 * n + 2 * tq;
+    float *r1 = r0 + 8 * D;
+    r0[0] = o[n][0];
+    r0[1] = o[n][1];
+    r1[0] = o[n][2];
+    r1[1] = o[n][3];
+  }
+  __syncthreads();
+  const bool single = sp.nsplit == 1;
+  for (int idx = threadIdx.x; idx < kRows * D; idx += kThreads) {
+    const int r = idx / D, d = idx % D;
+    const int Rr = rg * kRows + r;
+    if (Rr >= a.rows) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sM[w * kRows + r]);
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float e = fast_exp2(sM[w * kRows + r] - M);
+        num = fmaf(e, sO[(w * kRows + r) * D + d], num);
+        den = fmaf(e, sL[w * kRows + r], den);
+      }
+    }
+    const float val = den > 0.f ? num / den : 0.f;
+    const int t = Rr / QPK, h = Rr % QPK;
+    const int64_t hh = static_cast<int64_t>(b * q + t) * H + kvh * QPK + h;
+    if (single) {
+      uint16_t *o16 = static_cast<uint16_t *>(a.out);
+      o16[hh * D + d] = static_cast<uint16_t>(T::from_f2(val, 0.f) & 0xffffu);
+    } else {
+      const int64_t slot = hh * a.max_splits + split;
+      a.part_o[slot * D + d] = val;
+      if (d == 0) {
+        a.part_ml[slot * 2] = M;
+        a.part_ml[slot * 2 + 1] = den;
+      }
+    }
+  }
+}
+
+// One CTA per (decode token row, query head) of a sequence with several splits.
+template <class T, int D>
+__global__ void __launch_bounds__(D) decode_mt_combine_kernel(const Args a) {
+  const int row = blockIdx.x, h = blockIdx.y;  // row = b * q + t
+  const int b = row / a.q;
+  const Span sp = span_of(a, b, false);
+  if (sp.L == 0 || sp.nsplit <= 1) return;  // written by the split kernel
+  const int64_t hh = static_cast<int64_t>(row) * a.H + h;
+  const float *ml = a.part_ml + hh * a.max_splits * 2;
+  float M = -INFINITY;
+  for (int s = 0; s < sp.nsplit; ++s) M = fmaxf(M, ml[2 * s]);
+  const int d = threadIdx.x;
+  const float *po = a.part_o + hh * a.max_splits * D + d;
+  float num = 0.f, den = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < sp.nsplit; ++s) {
+      const float w = fast_exp2(ml[2 * s] - M) * ml[2 * s + 1];
+      num = fmaf(w, po[static_cast<int64_t>(s) * D], num);
+      den += w;
+    }
+  }
+  const float val = den > 0.f ? num / den : 0.f;
+  uint16_t *o16 = static_cast<uint16_t *>(a.out);
+  o16[hh * D + d] = static_cast<uint16_t>(T::from_f2(val, 0.f) & 0xffffu);
+}
+
+static size_t smem_bytes(int D, int split_units) {
+  const size_t tiles = static_cast<size_t>(kWarps) * kStages * 2 * (D / 64) * kUnit * 128;
+  const size_t table = ((split_units * 4 + 15) / 16) * 16;
+  return 1024 + tiles + table + kWarps * kStages * 8;  // + alignment slack
+}
+
+template <class T, int D>
+static cudaError_t launch_typed(const Args &a, const CUtensorMap &tmap, int KVH, int num_seqs,
+                                cudaStream_t stream) {
+  const size_t smem = smem_bytes(D, a.split_units);
+  auto kern = decode_mt_kernel<T, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.max_splits, KVH * a.row_groups, num_seqs);
+  kern<<<grid, kThreads, smem, stream>>>(a, tmap);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.max_splits <= 1) return e;
+  decode_mt_combine_kernel<T, D><<<dim3(num_seqs * a.q, a.H), D, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mt
+
+MultiDecodePlan plan_decode_multi(int num_seqs, int query_len, int max_seq_len,
+                                  const Geometry &g, int sms) {
+  MultiDecodePlan p{};
+  const int U = mt::kUnit;
+  // keys the batch's widest row set can see
+  int eff = std::max(max_seq_len, 1);
+  if (g.window > 0 && g.window + query_len - 1 < eff) eff = g.window + query_len - 1;
+  const int units = (eff + U - 1) / U + 1;  // a window start can straddle a unit
+  p.row_groups = (query_len * g.QPK + mt::kRows - 1) / mt::kRows;
+  const int64_t items = static_cast<int64_t>(num_seqs) * g.KVH * p.row_groups;
+  int split_units = 32;  // 512 keys
+  while (split_units > 8 && items * ((units + split_units - 1) / split_units) < 8LL * sms)
+    split_units /= 2;
+  if (units <= 2 * split_units) split_units = units;  // short: one split
+  p.split_units = split_units;
+  p.max_splits = (units + split_units - 1) / split_units;
+  if (p.max_splits > 1) {
+    const size_t rows = static_cast<size_t>(num_seqs) * query_len * g.H * p.max_splits;
+    const size_t o_bytes = ((rows * g.D * 4 + 255) / 256) * 256;
+    const size_t ml_bytes = ((rows * 2 * 4 + 255) / 256) * 256;
+    p.workspace_bytes = o_bytes + ml_bytes;
+  }
+  return p;
+}
+
+cudaError_t launch_decode_multi(void *out, const void *query, int num_seqs, int query_len,
+                                const void *kv_cache, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *seq_lens,
+                                const Geometry &g, const MultiDecodePlan &plan, void *workspace,
+                                cudaStream_t stream) {
+  CUtensorMap tmap;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.D), static_cast<cuuint64_t>(g.KVH),
+                              static_cast<cuuint64_t>(g.num_blocks * g.BS), 2};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.D) * 2,
+                                 static_cast<cuuint64_t>(g.row_elems) * 2,
+                                 static_cast<cuuint64_t>(g.num_blocks * g.block_elems) * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(mt::kUnit), 1};
+  const bool bf = g.dtype == PKV_BF16;
+  if (encode_tensor_map(&tmap,
+                        bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        4, const_cast<void *>(kv_cache), dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  mt::Args a{};
+  a.out = out;
+  a.query = static_cast<const uint16_t *>(query);
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.alibi = g.alibi;
+  if (plan.max_splits > 1) {
+    const size_t rows = static_cast<size_t>(num_seqs) * query_len * g.H * plan.max_splits;
+    const size_t o_bytes = ((rows * g.D * 4 + 255) / 256) * 256;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + o_bytes);
+  }
+  a.num_blocks = g.num_blocks;
+  a.num_seqs = num_seqs;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.H = g.H;
+  a.QPK = g.QPK;
+  a.q = query_len;
+  a.rows = query_len * g.QPK;
+  a.row_groups = plan.row_groups;
+  a.BS = g.BS;
+  a.window = g.window;
+  a.split_units = plan.split_units;
+  a.max_splits = plan.max_splits;
+  a.scale_log2 = g.scale * kLog2e;
+  if (g.D == 128)
+    return bf ? mt::launch_typed<BF16, 128>(a, tmap, g.KVH, num_seqs, stream)
+              : mt::launch_typed<FP16, 128>(a, tmap, g.KVH, num_seqs, stream);
+  if (g.D == 64)
+    return bf ? mt::launch_typed<BF16, 64>(a, tmap, g.KVH, num_seqs, stream)
+              : mt::launch_typed<FP16, 64>(a, tmap, g.KVH, num_seqs, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t read_device_error_decode_multi(unsigned long long *out) {
+  return read_and_clear_unit_error(out);
+}
+
+}  // namespace pkv

@@ -30,6 +30,8 @@ The five named workloads follow the attention-backend pages' metadata
 8. ``varlen_prefill_fp8``: the shape of 3 over an fp8 (E4M3) cache with the
    same scales as 7 (the prompts' keys and values are quantised by the
    cache write).
+9. ``llama3_8b_spec_decode``: the shape of 2 with 128 sequences each
+   decoding 4 tokens (1 + 3 speculative, a uniform batch).
 """
 from __future__ import annotations
 
@@ -72,6 +74,8 @@ class Workload:
     kv_cache_dtype: str = "auto"             # or "fp8_e4m3" (uint8 cache)
     k_scale: float = 1.0
     v_scale: float = 1.0
+    multi_query_len: int = 0                 # > 0: a uniform batch of decodes
+                                             # of this many tokens each
 
     # -- views used by the calls --------------------------------------------
     @property
@@ -145,7 +149,7 @@ def build(*, name: str, g: torch.Generator, dtype: torch.dtype,
           alibi: bool = False, sliding_window: int = 0,
           n_copy: int = 0, n_swap: int = 0, fill_cache: bool = True,
           causal: bool = True, kv_cache_dtype: str = "auto", k_scale: float = 1.0,
-          v_scale: float = 1.0) -> Workload:
+          v_scale: float = 1.0, multi_query_len: int = 0) -> Workload:
     """Lay out a batch in a paged pool and draw its tensors.
 
     Block placement: the N = sum ceil(seq_len / block_size) blocks the batch
@@ -158,6 +162,8 @@ def build(*, name: str, g: torch.Generator, dtype: torch.dtype,
     seq_lens = torch.as_tensor(seq_lens, dtype=torch.int64)
     query_lens = torch.as_tensor(query_lens, dtype=torch.int64)
     B = seq_lens.numel()
+    if multi_query_len:  # every sequence decodes multi_query_len tokens
+        assert num_prefill_seqs == 0 and bool((query_lens == multi_query_len).all())
     assert bool((query_lens <= seq_lens).all()) and bool((query_lens >= 0).all())
     bs = block_size
     nblk = [(int(L) + bs - 1) // bs for L in seq_lens]
@@ -236,7 +242,8 @@ def build(*, name: str, g: torch.Generator, dtype: torch.dtype,
         num_prefill_seqs=num_prefill_seqs, block_tables=tables,
         kv_cache=kv_cache, query=query, key=key, value=value,
         slot_mapping=slots, copy_pairs=copy_pairs, swap_pairs=swap_pairs,
-        causal=causal, kv_cache_dtype=kv_cache_dtype, k_scale=k_scale, v_scale=v_scale)
+        causal=causal, kv_cache_dtype=kv_cache_dtype, k_scale=k_scale, v_scale=v_scale,
+        multi_query_len=multi_query_len)
 
 
 # ---------------------------------------------------------------------------
@@ -311,6 +318,16 @@ def _varlen_prefill_fp8(g, scale_down=1):
                  k_scale=0.02, v_scale=0.02)
 
 
+def _llama3_8b_spec_decode(g, scale_down=1):
+    B = max(1, 128 // scale_down)
+    q = 4  # one token + 3 speculative tokens per sequence
+    L = _uniform_int(g, B, 512, 4096)
+    return build(name="llama3_8b_spec_decode", g=g, dtype=torch.bfloat16,
+                 num_heads=32, num_kv_heads=8, head_size=128, block_size=16,
+                 seq_lens=L, query_lens=torch.full((B,), q, dtype=torch.int64),
+                 num_prefill_seqs=0, multi_query_len=q)
+
+
 def _llama3_8b_decode_fp8(g, scale_down=1):
     B = max(1, 256 // scale_down)
     L = _uniform_int(g, B, 512, 4096)
@@ -330,11 +347,12 @@ CONFIGS = {
     6: _encoder_varlen_prefill,
     7: _llama3_8b_decode_fp8,
     8: _varlen_prefill_fp8,
+    9: _llama3_8b_spec_decode,
 }
 
 
 def make_config(index: int, scale_down: int = 1) -> Workload:
-    """Workload ``index`` (1..8) drawn from generator seed 1000 + index.
+    """Workload ``index`` (1..9) drawn from generator seed 1000 + index.
 
     ``scale_down`` > 1 divides the batch counts (not the lengths), for tests
     that want the shape of a workload at a fraction of its size.

@@ -53,6 +53,18 @@ class GpuRun:
         B.paged_attn_decode(out, q, self.cache, bt, sl, mx, self.p, ws)
         return out
 
+    def decode_multi(self, max_seq_len=None):
+        """Every sequence decodes w.multi_query_len tokens (rows b * q + t)."""
+        w = self.w
+        q = w.multi_query_len
+        sl = w.seq_lens.to(DEV)
+        mx = int(w.seq_lens.max()) if max_seq_len is None else max_seq_len
+        out = torch.full_like(self.query, float("nan"))
+        n = B.paged_attn_decode_multi_workspace_size(w.num_seqs, q, mx, self.p)
+        ws = torch.empty(max(n, 16), dtype=torch.uint8, device=DEV)
+        B.paged_attn_decode_multi(out, self.query, self.cache, self.tables, sl, q, mx, self.p, ws)
+        return out
+
     def prefill(self):
         q, cuq, cuk, bt, mq, mk = self.w.prefill_slices()
         Tp = q.shape[0]

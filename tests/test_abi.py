@@ -106,6 +106,25 @@ def test_decode_and_prefill_validation(lib):
                                          ctypes.byref(p8), nul) == B.PKV_ERR_INVALID
 
 
+def test_multi_decode_validation(lib):
+    nul = ctypes.c_void_p(0)
+    p = _p()
+    call = lambda pp, B=2, q=4: lib.paged_attn_decode_multi(nul, nul, B, q, nul, 4, nul, 1, nul,
+                                                          8, ctypes.byref(pp), nul, 0, nul)
+    assert call(p, B=0) == B.PKV_OK                     # empty: nothing enqueued
+    assert call(p, q=0) == B.PKV_ERR_INVALID
+    assert call(p, q=65) == B.PKV_ERR_UNSUPPORTED
+    assert call(p) == B.PKV_ERR_INVALID                 # null pointers
+    assert call(_p(non_causal=1)) == B.PKV_ERR_UNSUPPORTED
+    fp8 = _p(kv_cache_dtype=B.PKV_CACHE_FP8_E4M3, k_scale=0.1, v_scale=0.1)
+    assert call(fp8) == B.PKV_ERR_UNSUPPORTED
+    assert call(_p(num_heads=24, num_kv_heads=8)) == B.PKV_ERR_INVALID   # any group size
+    assert B.paged_attn_decode_multi_workspace_size(4, 4, 64, p) == 0   # one split
+    n = B.paged_attn_decode_multi_workspace_size(128, 4, 4096, p)
+    assert n > 0 and n % 256 == 0
+    assert B.paged_attn_decode_multi_workspace_size(128, 0, 4096, p) == 0
+
+
 def test_workspace_size_is_host_only(lib):
     p = _p()
     assert B.paged_attn_decode_workspace_size(0, 100, p) == 0

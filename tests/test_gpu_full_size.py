@@ -106,6 +106,20 @@ def test_varlen_prefill_fp8_full():
     assert_close(out[rows], ref[rows], "varlen_prefill_fp8")
 
 
+def test_llama3_8b_spec_decode_full():
+    w = W.make_config(9)
+    r = GpuRun(w)
+    ref_cache = _write_and_check(w, r)
+    out = r.decode_multi()
+    assert_no_device_error("spec decode")
+    seqs = _sample_seqs(w.seq_lens)
+    ref = O.paged_attn_decode_multi(w.query, ref_cache, w.block_tables, w.seq_lens,
+                                    w.multi_query_len, oracle_params(w), seqs=seqs)
+    q = w.multi_query_len
+    rows = [b * q + t for b in seqs for t in range(q)]
+    assert_close(out[rows], ref[rows], "llama3_8b_spec_decode")
+
+
 def test_mixed_chunked_alibi_full():
     w = W.make_config(4)
     r = GpuRun(w)

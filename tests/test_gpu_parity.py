@@ -19,14 +19,14 @@ if torch.cuda.is_available():
 
 
 def small(seed, *, dtype=torch.bfloat16, H=8, KVH=2, D=128, bs=16, seq_lens, query_lens=None,
-          P=0, alibi=False, window=0, num_blocks=None, causal=True):
+          P=0, alibi=False, window=0, num_blocks=None, causal=True, multi=0):
     g = torch.Generator().manual_seed(seed)
     if query_lens is None:
-        query_lens = [1] * len(seq_lens)
+        query_lens = [multi or 1] * len(seq_lens)
     return W.build(name=f"case{seed}", g=g, dtype=dtype, num_heads=H, num_kv_heads=KVH,
                    head_size=D, block_size=bs, seq_lens=seq_lens, query_lens=query_lens,
                    num_prefill_seqs=P, alibi=alibi, sliding_window=window, num_blocks=num_blocks,
-                   causal=causal)
+                   causal=causal, multi_query_len=multi)
 
 
 def rand_lens(seed, n, lo, hi):
@@ -132,6 +132,79 @@ def test_decode_split_invariance():
     assert_no_device_error("split invariance")
     err = (a.double() - b.double()).abs().max().item()
     assert err <= 2e-2
+
+
+# ---------------------------------------------------------------------------
+# f3: multi-token (speculative) decode
+# ---------------------------------------------------------------------------
+
+def mlens(seed, n, q, hi):
+    return [max(q, x) for x in rand_lens(seed, n, 1, hi)]
+
+
+MULTI_CASES = {
+    "q2_qpk4": lambda: small(121, H=32, KVH=8, multi=2, seq_lens=mlens(1, 9, 2, 600)),
+    "q4_qpk4_multi_split": lambda: small(122, H=32, KVH=8, multi=4, seq_lens=mlens(2, 6, 4, 3000)),
+    "q1_is_decode": lambda: small(123, H=32, KVH=8, multi=1, seq_lens=mlens(3, 7, 1, 700)),
+    "q3_qpk1": lambda: small(124, H=4, KVH=4, multi=3, seq_lens=mlens(4, 7, 3, 400)),
+    "q5_qpk4_two_row_groups": lambda: small(125, H=8, KVH=2, multi=5, seq_lens=mlens(5, 5, 5, 900)),
+    "q4_qpk8_d64": lambda: small(126, H=16, KVH=2, D=64, multi=4, seq_lens=mlens(6, 5, 4, 700)),
+    "q3_qpk6_odd_group": lambda: small(127, H=12, KVH=2, multi=3, seq_lens=mlens(7, 4, 3, 500)),
+    "fp16_bs32": lambda: small(128, dtype=torch.float16, bs=32, multi=4,
+                               seq_lens=mlens(8, 6, 4, 900)),
+    "window_alibi": lambda: small(129, window=100, alibi=True, multi=4,
+                                  seq_lens=mlens(9, 8, 4, 900)),
+    "window_bs32_q6": lambda: small(130, bs=32, window=37, multi=6, seq_lens=mlens(10, 6, 6, 800)),
+    "exact_lengths": lambda: small(131, multi=4, seq_lens=[4, 5, 16, 17, 31, 33]),
+    "long_single": lambda: small(132, H=32, KVH=8, multi=4, seq_lens=[5000]),
+    "q16_qpk4": lambda: small(133, H=32, KVH=8, multi=16, seq_lens=mlens(11, 3, 16, 600)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(MULTI_CASES))
+def test_decode_multi_parity(case):
+    w = MULTI_CASES[case]()
+    r = GpuRun(w)
+    r.write()
+    out = r.decode_multi()
+    assert_no_device_error(case)
+    ref_cache = oracle_cache_after_write(w)
+    ref = O.paged_attn_decode_multi(w.query, ref_cache, w.block_tables, w.seq_lens,
+                                    w.multi_query_len, oracle_params(w))
+    assert_close(out, ref, case)
+
+
+def test_decode_multi_q1_matches_decode_and_split_invariance():
+    w = small(134, H=32, KVH=8, multi=1, seq_lens=mlens(12, 10, 1, 2000))
+    r = GpuRun(w)
+    r.write()
+    a = r.decode_multi()
+    b = r.decode()
+    c = r.decode_multi(max_seq_len=8 * int(w.seq_lens.max()))  # other split plan
+    assert_no_device_error("multi q=1")
+    assert (a.double() - b.double()).abs().max().item() <= 2e-2
+    assert (a.double() - c.double()).abs().max().item() <= 2e-2
+
+
+def test_decode_multi_padding_and_short_lengths():
+    w = small(135, multi=4, seq_lens=[40, 9, 70])
+    r = GpuRun(w)
+    r.write()
+    sl = w.seq_lens.clone()
+    sl[1] = 0                      # padding sequence: zero rows
+    out = torch.full_like(r.query, float("nan"))
+    B.paged_attn_decode_multi(out, r.query, r.cache, r.tables, sl.to(DEV), 4, 70, r.p)
+    assert_no_device_error("multi padding")
+    assert torch.equal(out[4:8].cpu(), torch.zeros_like(out[4:8].cpu()))
+    ref = O.paged_attn_decode_multi(w.query, oracle_cache_after_write(w), w.block_tables, sl, 4,
+                                    oracle_params(w))
+    assert_close(out, ref, "multi padding")
+    sl[1] = 3                      # shorter than its 4 query tokens: reported, zero rows
+    B.paged_attn_decode_multi(out, r.query, r.cache, r.tables, sl.to(DEV), 4, 70, r.p)
+    torch.cuda.synchronize()
+    st, detail = B.device_error()
+    assert st == B.PKV_ERR_BOUNDS and detail == 1
+    assert torch.equal(out[4:8].cpu(), torch.zeros_like(out[4:8].cpu()))
 
 
 # ---------------------------------------------------------------------------
