@@ -229,8 +229,9 @@ size_t paged_attn_decode_workspace_size(int32_t num_seqs, int32_t max_seq_len,
  *                records PKV_ERR_BOUNDS and gives zero rows
  *   workspace    >= paged_attn_decode_multi_workspace_size(...) bytes of
  *                device scratch, 256-byte aligned (NULL when that is 0)
- *   Other arguments as paged_attn_decode.  Caches of the model dtype only:
- *   an fp8 cache, or non_causal, returns PKV_ERR_UNSUPPORTED.
+ *   Other arguments as paged_attn_decode (the fp8 cache included: products
+ *   on fp16 operands, queries scaled by a power of two as in the prefill
+ *   call); non_causal returns PKV_ERR_UNSUPPORTED.
  */
 pkv_status paged_attn_decode_multi(void *out, const void *query, int32_t num_seqs,
                                    int32_t query_len, const void *kv_cache,

@@ -130,8 +130,6 @@ static pkv_status make_geometry(const pkv_attn_params *p, int64_t num_blocks, Ge
 
 static pkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
-static bool decode_qpk_supported(int qpk) { return qpk == 1 || qpk == 2 || qpk % 4 == 0; }
-
 constexpr int32_t kMaxMultiQueryLen = 64;  // tokens per sequence of a multi-token decode
 
 }  // namespace pkv
@@ -175,12 +173,10 @@ pkv_status kv_cache_write(const void *key, const void *value, int64_t num_tokens
 size_t paged_attn_decode_workspace_size(int32_t num_seqs, int32_t max_seq_len,
                                         const pkv_attn_params *params) {
   Geometry g;
-  if (make_geometry(params, 1, &g) != PKV_OK || num_seqs <= 0 || max_seq_len < 0 ||
-      !decode_qpk_supported(g.QPK))
-    return 0;
+  if (make_geometry(params, 1, &g) != PKV_OK || num_seqs <= 0 || max_seq_len < 0) return 0;
   DeviceInfo dev;
   if (current_device_info(&dev) != cudaSuccess) dev.sms = 152;
-  return plan_decode(num_seqs, max_seq_len, g, dev.sms).workspace_bytes;
+  return plan_decode(num_seqs, 1, max_seq_len, g, dev.sms).workspace_bytes;
 }
 
 pkv_status paged_attn_decode(void *out, const void *query, int32_t num_seqs, const void *kv_cache,
@@ -191,7 +187,6 @@ pkv_status paged_attn_decode(void *out, const void *query, int32_t num_seqs, con
   Geometry g;
   pkv_status st = make_geometry(params, num_blocks, &g);
   if (st != PKV_OK) return st;
-  if (!decode_qpk_supported(g.QPK)) return PKV_ERR_UNSUPPORTED;
   if (num_seqs < 0 || num_seqs > 65535 || max_seq_len < 0 || max_blocks_per_seq <= 0)
     return PKV_ERR_INVALID;
   if (num_seqs == 0) return PKV_OK;
@@ -205,12 +200,12 @@ pkv_status paged_attn_decode(void *out, const void *query, int32_t num_seqs, con
   DeviceInfo dev;
   e = current_device_info(&dev);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
-  const DecodePlan plan = plan_decode(num_seqs, max_seq_len, g, dev.sms);
+  const DecodePlan plan = plan_decode(num_seqs, 1, max_seq_len, g, dev.sms);
   if (plan.workspace_bytes > 0 &&
       (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16)))
     return PKV_ERR_INVALID;
-  return from_cuda(launch_decode(out, query, num_seqs, kv_cache, block_tables, max_blocks_per_seq,
-                                 seq_lens, max_seq_len, g, plan, workspace, s));
+  return from_cuda(launch_decode(out, query, num_seqs, 1, kv_cache, block_tables,
+                                 max_blocks_per_seq, seq_lens, g, plan, workspace, s));
 }
 
 pkv_status paged_attn_decode_noalloc(void *out, const void *query, int32_t num_seqs,
@@ -221,7 +216,6 @@ pkv_status paged_attn_decode_noalloc(void *out, const void *query, int32_t num_s
   Geometry g;
   pkv_status st = make_geometry(params, num_blocks, &g);
   if (st != PKV_OK) return st;
-  if (!decode_qpk_supported(g.QPK)) return PKV_ERR_UNSUPPORTED;
   if (num_seqs < 0 || num_seqs > 65535 || max_seq_len < 0 || max_blocks_per_seq <= 0)
     return PKV_ERR_INVALID;
   if (num_seqs == 0) return PKV_OK;
@@ -239,7 +233,7 @@ pkv_status paged_attn_decode_noalloc(void *out, const void *query, int32_t num_s
 }
 
 static bool multi_args_supported(const Geometry &g, int32_t query_len) {
-  return !g.fp8 && !g.non_causal && query_len >= 1 && query_len <= kMaxMultiQueryLen;
+  return !g.non_causal && query_len >= 1 && query_len <= kMaxMultiQueryLen;
 }
 
 size_t paged_attn_decode_multi_workspace_size(int32_t num_seqs, int32_t query_len,
@@ -251,7 +245,7 @@ size_t paged_attn_decode_multi_workspace_size(int32_t num_seqs, int32_t query_le
     return 0;
   DeviceInfo dev;
   if (current_device_info(&dev) != cudaSuccess) dev.sms = 152;
-  return plan_decode_multi(num_seqs, query_len, max_seq_len, g, dev.sms).workspace_bytes;
+  return plan_decode(num_seqs, query_len, max_seq_len, g, dev.sms).workspace_bytes;
 }
 
 pkv_status paged_attn_decode_multi(void *out, const void *query, int32_t num_seqs,
@@ -279,12 +273,12 @@ pkv_status paged_attn_decode_multi(void *out, const void *query, int32_t num_seq
   DeviceInfo dev;
   e = current_device_info(&dev);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
-  const MultiDecodePlan plan = plan_decode_multi(num_seqs, query_len, max_seq_len, g, dev.sms);
+  const DecodePlan plan = plan_decode(num_seqs, query_len, max_seq_len, g, dev.sms);
   if (plan.workspace_bytes > 0 &&
       (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16)))
     return PKV_ERR_INVALID;
-  return from_cuda(launch_decode_multi(out, query, num_seqs, query_len, kv_cache, block_tables,
-                                       max_blocks_per_seq, seq_lens, g, plan, workspace, s));
+  return from_cuda(launch_decode(out, query, num_seqs, query_len, kv_cache, block_tables,
+                                 max_blocks_per_seq, seq_lens, g, plan, workspace, s));
 }
 
 pkv_status paged_attn_prefill_varlen(void *out, const void *query, int64_t num_query_tokens,
@@ -382,11 +376,10 @@ pkv_status kv_swap_blocks(const void *src_cache, int64_t src_num_blocks, void *d
 }
 
 pkv_status pkv_device_error(int64_t *detail) {
-  constexpr int kUnits = 4;
-  unsigned long long words[kUnits] = {0, 0, 0, 0};
+  constexpr int kUnits = 3;
+  unsigned long long words[kUnits] = {0, 0, 0};
   cudaError_t (*readers[kUnits])(unsigned long long *) = {
-      read_device_error_kv_ops, read_device_error_decode, read_device_error_decode_multi,
-      read_device_error_prefill};
+      read_device_error_kv_ops, read_device_error_decode, read_device_error_prefill};
   for (int k = 0; k < kUnits; ++k)
     if (readers[k](&words[k]) != cudaSuccess) return PKV_ERR_CUDA;
   for (int k = 0; k < kUnits; ++k) {

@@ -161,6 +161,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Four E4M3 codes (low byte first) -> two fp16 pairs (low half first),
+// exactly: every E4M3 value is an fp16 value.
+__device__ __forceinline__ uint2 e4m3x4_to_h4(uint32_t u) {
+  uint2 r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(r.x), "=r"(r.y)
+      : "r"(u));
+  return r;
+}
+
 // Packed fp32 pairs (Blackwell f32x2 FMA/ADD/MUL) and the 3-input max: the
 // attention inner loops are instruction-bound, and the packed forms halve
 // their per-element arithmetic.

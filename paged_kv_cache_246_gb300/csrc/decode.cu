@@ -1,88 +1,108 @@
-// Split-KV paged decode (a query of one token per sequence) and the merge of
-// the split partials.
+// Decode over the paged cache on the tensor core: one query token per
+// sequence (paged_attn_decode), or a uniform batch of q tokens per sequence
+// (paged_attn_decode_multi, speculative decoding).
 //
 // What is computed (xformers.py XFormersImpl.forward -> forward_decode;
-// cpu_attn TorchSDPABackendImpl.forward -> forward_decode): for sequence b
-// of length L (the new token already written), query position i = L - 1,
-// query head h reading KV head h / qpk, keys lo <= j <= i with
-// lo = max(0, i - W + 1) under a window W (else 0):
+// cpu_attn TorchSDPABackendImpl.forward -> forward_decode; for q > 1
+// backends.utils AttentionCGSupport.UNIFORM_BATCH: every decode of the batch
+// has the same query length q = 1 + num_speculative_tokens, and
+// AttentionMetadataBuilder._init_reorder_batch_threshold pulls such decodes
+// to the front for spec-as-decode kernels): token t of sequence b sits at
+// position i = L_b - q + t (L_b counts the q new tokens, as a single-token
+// decode's seq_len counts its one) and attends to keys lo(i) <= j <= i read
+// through the block table:
 //     s_j = scale * q.k_j + slope_h * (j - i),   out = softmax(s) . V.
 //
-// Design (GB300): the kernel is HBM-bound (each cached K/V byte is read once
-// and used for qpk query heads), so the work is organised around the loads.
-//  * CTA = (split, KV head [, head group], sequence); 4 warps.  A split is a
-//    run of `split_blocks` logical blocks; warp w takes blocks w, w+4, ...
-//  * Each warp owns a ring of TMA stages in shared memory: one 4-D tiled TMA
-//    copy brings one block's keys of this KV head (block_size rows x
-//    head_size) and a second its values, both completing on the stage's
-//    mbarrier.  Lane 0 refills a stage as soon as the warp is done with it, so
-//    up to (4 warps x stages x 2 tiles) loads are in flight per CTA.
-//  * q.k: lane (dg = lane % 8, ts = lane / 8) holds 8-element chunks dg
-//    (and dg + 8) of the query heads in fp32 registers and dots them with the
-//    same chunks of token ts, ts + 4, ...; three xor-shuffles finish each dot.
-//  * Online softmax per warp in the log2 domain (q pre-scaled by
-//    scale * log2 e), probabilities staged in shared memory, then p.V with each
-//    lane owning head_size / 32 output dims of every query head.
-//  * Warps merge through shared memory; a single split writes the output,
-//    several splits write (o, m, l) partials that decode_combine_kernel
-//    merges (flash-decoding).
-#include <cuda_fp8.h>
-
+// Design.  Rows are (token t, query head h of the KV group) pairs,
+// r = t * QPK + h, in groups of 16: one m16 tile of mma.sync m16n8k16, so the
+// group's rows share every K/V byte.  (tcgen05's smallest tile, 64 rows,
+// would leave most of it empty at these row counts; the step is bound by
+// HBM, and the tensor core serves to keep the per-key instruction count low
+// enough for the 8-bit cache's doubled key rate.)  CTA = (split of the key
+// range, KV head x row group, sequence), 4 warps.  Each warp walks its own
+// 16-token units of the split (unit k of the warp = split unit warp + 4k)
+// through a two-stage ring of TMA boxes (16 tokens x 64 dims, 128-byte
+// swizzle; K and V).  Per unit:
+//   S[16 rows x 16 keys] = Q K^T   Q fragments held in registers for the
+//                                  whole CTA, K fragments by ldmatrix;
+//   scores scaled into the log2 domain (+ ALiBi), masked per row (its own
+//   causal position and window start), online softmax per row with a lazy
+//   reference max (moved, and O rescaled, only when a score passes it by 2^8);
+//   O += P V                       P packed to bf16/fp16 pairs in registers as
+//                                  the A operand, V fragments by
+//                                  ldmatrix.trans.
+// The four warps merge their (m, l, O) through shared memory; a sequence cut
+// into several splits writes (o, m, l) partials that decode_combine_kernel
+// merges (flash-decoding).  Every wait is bounded (a timeout records
+// PKV_ERR_TIMEOUT, drains the warp's copies in flight and leaves the output
+// unwritten for that CTA).
+//
+// Over an fp8 (E4M3) cache (KV8) the MMAs run on fp16 operands: the boxes
+// carry the 8-bit codes (16 tokens x D bytes, no swizzle); a lane's K
+// fragments come straight from its codes with cvt.rn.f16x2.e4m3x2, taking
+// the head dimension in a fixed permuted order (lane tq of a k-step covers
+// dims tq * D/4 + 4s .. + 3, one 32-bit word of codes) that the queries'
+// fragments follow too (a dot product does not depend on the order of its
+// terms); each unit's V codes are widened by the warp into a swizzled fp16
+// tile read by the same ldmatrix.trans as a 16-bit cache.  Queries are
+// fp16 x 2^-e, e chosen from the row group's largest magnitude (exact
+// power-of-two scaling); 2^e and k_scale join the softmax scale, v_scale
+// multiplies the output.
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace pkv {
+namespace dec {
 
-constexpr int kDecWarps = 4;
-constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kSub = 16;  // tokens per compute sub-tile
-constexpr float kLazy = 8.f;  // reference-max slack (log2 units) before a rescale
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kUnit = 16;   // keys per unit (one TMA box height)
+constexpr int kRows = 16;   // rows per CTA: one m16 tile
+constexpr int kStages = 2;  // TMA ring depth per warp
+constexpr float kLazy = 8.f;
 
-struct DecodeArgs {
+struct Args {
   void *out;
   const uint16_t *query;
   const int32_t *block_tables;
   const int32_t *seq_lens;
   const float *alibi;
-  float *part_o;   // [B][H][max_splits][D]
-  float *part_ml;  // [B][H][max_splits][2]
+  float *part_o;   // [B * q * H][max_splits][D]
+  float *part_ml;  // [B * q * H][max_splits][2]
   int64_t num_blocks;
   int num_seqs, max_blocks_per_seq;
-  int H, QPK, head_groups;  // head_groups = QPK / QT
-  int BS, window, split_blocks, max_splits, stages;
-  float scale_log2;  // scale * log2(e) (* k_scale for an fp8 cache)
+  int H, QPK, q, rows, row_groups;
+  int BS, window, split_units, max_splits;
+  float scale_log2;  // scale * log2(e) (* k_scale over an fp8 cache)
   float v_scale;     // 1, or the fp8 cache's value scale
 };
 
-struct SeqSpan {
-  int L;          // clamped length
-  int lo;         // first visible key position
-  int first_blk;  // logical block of lo
-  int nblk;       // logical blocks lo .. L-1 touch
-  int nsplit;     // splits this sequence uses (<= max_splits)
+struct Span {
+  int L;           // length (0: padding, or a bad length that was reported)
+  int first_unit;  // unit of the first visible key of token 0
+  int nunits;      // units up to position L - 1
+  int nsplit;
 };
 
-__device__ __forceinline__ SeqSpan seq_span(const DecodeArgs &a, int b, bool report) {
-  SeqSpan s;
+__device__ __forceinline__ Span span_of(const Args &a, int b, bool report) {
+  Span s{};
   int L = __ldg(a.seq_lens + b);
   const int cap = a.max_blocks_per_seq * a.BS;
-  if (L < 0 || L > cap) {
+  if (L < 0 || L > cap || (L > 0 && L < a.q)) {  // the decode must fit its sequence
     if (report) record_error(PKV_ERR_BOUNDS, b);
-    L = L < 0 ? 0 : cap;
+    L = 0;
   }
   s.L = L;
-  if (L == 0) {
-    s.lo = s.first_blk = s.nblk = s.nsplit = 0;
-    return s;
-  }
-  const int i = L - 1;
-  s.lo = a.window > 0 ? max(0, i - a.window + 1) : 0;
-  s.first_blk = s.lo / a.BS;
-  s.nblk = i / a.BS - s.first_blk + 1;
-  s.nsplit = (s.nblk + a.split_blocks - 1) / a.split_blocks;
+  if (L == 0) return s;
+  const int i0 = L - a.q;  // token 0: its window starts first
+  const int lo = a.window > 0 ? max(0, i0 - a.window + 1) : 0;
+  s.first_unit = lo / kUnit;
+  s.nunits = (L - 1) / kUnit - s.first_unit + 1;
+  s.nsplit = (s.nunits + a.split_units - 1) / a.split_units;
   if (s.nsplit > a.max_splits) {  // seq_len above the host's max_seq_len
     if (report) record_error(PKV_ERR_BOUNDS, b);
     s.nsplit = a.max_splits;
@@ -90,347 +110,347 @@ __device__ __forceinline__ SeqSpan seq_span(const DecodeArgs &a, int b, bool rep
   return s;
 }
 
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// D[16x8] += A[16x16] B[16x8], fp32 accumulate; A row-major, B column-major.
 template <class T>
-__device__ __forceinline__ void load_chunk_f32(const uint4 &u, float (&f)[8]) {
-  float2 t;
-  t = T::to_f2(u.x); f[0] = t.x; f[1] = t.y;
-  t = T::to_f2(u.y); f[2] = t.x; f[3] = t.y;
-  t = T::to_f2(u.z); f[4] = t.x; f[5] = t.y;
-  t = T::to_f2(u.w); f[6] = t.x; f[7] = t.y;
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1);
+template <>
+__device__ __forceinline__ void mma16816<BF16>(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<FP16>(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Dots each lane finishes after the recursive halving of 4 * QT partials
-// over 8 lanes, and the head of its f-th one (token is (dg >> 1) * 4 + ts).
-template <int QT> struct NfOf { static constexpr int v = QT >= 2 ? QT / 2 : 1; };
-template <int QT>
-__device__ __forceinline__ int head_of(int dg, int f) {
-  if constexpr (QT == 4) return 2 * (dg & 1) + f;
-  else if constexpr (QT == 2) return dg & 1;
-  else return 0;
+template <int D, bool KV8 = false>
+struct Lay {
+  static constexpr int BOX = kUnit * 128;  // 16 rows x 64 dims x 2 B
+  static constexpr int V16 = (D / 64) * BOX;  // one unit of K or V as 16-bit values
+  static constexpr int TILE = KV8 ? kUnit * D : V16;  // one unit as stored in the cache
+  static constexpr int STAGE = 2 * TILE;
+  // per-warp rings, then (fp8) each warp's widened V tile
+  static constexpr int TILES = kWarps * kStages * STAGE + (KV8 ? kWarps * V16 : 0);
+  static constexpr int MERGE = kWarps * kRows * (D + 2) * 4;  // reuses the tiles
+  static_assert(MERGE <= TILES, "merge buffers fit in the tile area");
+};
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// One halving level over lanes xor MASK: N values -> N / 2 (or a plain sum
-// when one value is left).
-template <int N, int MASK>
-__device__ __forceinline__ void halve(float *v, int lane) {
-  if constexpr (N >= 2) {
-    const bool up = (lane & MASK) != 0;
-#pragma unroll
-    for (int k = 0; k < N / 2; ++k) {
-      const float send = up ? v[k] : v[k + N / 2];
-      const float keep = up ? v[k + N / 2] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, MASK);
-    }
-  } else {
-    v[0] += __shfl_xor_sync(0xffffffffu, v[0], MASK);
-  }
+// Byte offset, inside a unit's K or V tile, of the 16-byte chunk `chunk`
+// (8 dims) of key row `tok`: 64-dim box, row, 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(int tok, int chunk) {
+  return static_cast<uint32_t>((chunk >> 3) * (kUnit * 128) + tok * 128 +
+                               (((chunk & 7) ^ (tok & 7)) << 4));
 }
 
-template <int NV>
-__device__ __forceinline__ void reduce_over_dg(float *v, int lane) {
-  halve<NV, 4>(v, lane);
-  halve<(NV >= 2 ? NV / 2 : 1), 2>(v, lane);
-  halve<(NV >= 4 ? NV / 4 : 1), 1>(v, lane);
-}
-
-// Eight / four / two E4M3 cache codes (low byte first) widened to fp32.
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
-  return __half22float2(*reinterpret_cast<const __half2 *>(&h));
-}
-__device__ __forceinline__ void load_chunk8_f32(const uint2 &u, float (&f)[8]) {
-  float2 t;
-  t = e4m3x2_to_f2(u.x); f[0] = t.x; f[1] = t.y;
-  t = e4m3x2_to_f2(u.x >> 16); f[2] = t.x; f[3] = t.y;
-  t = e4m3x2_to_f2(u.y); f[4] = t.x; f[5] = t.y;
-  t = e4m3x2_to_f2(u.y >> 16); f[6] = t.x; f[7] = t.y;
-}
-
-// T: element type of queries / outputs; D: head size; QT: query heads per
-// CTA (<= 4); KV8: the cache holds E4M3 codes (k_scale is folded into the
-// query scale, v_scale applied to the merged output).
-template <class T, int D, int QT, bool KV8>
-__global__ void __launch_bounds__(kDecThreads, KV8 ? 4 : 3)
-decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
-  constexpr int CPL = D / 64;  // 8-element chunks per lane per token (q.k)
-  constexpr int DPL = D / 32;  // output dims per lane (p.V)
-  constexpr int ROWC = D / 8;  // 16-byte chunks per K/V row
-  extern __shared__ __align__(128) uint8_t smem[];
+template <class T, int D, bool KV8>
+__global__ void __launch_bounds__(kThreads, 3)
+decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
+  using L = Lay<D, KV8>;
+  using MT = std::conditional_t<KV8, FP16, T>;  // MMA operand type (and P)
+  constexpr int KS = D / 16;  // k-steps of q.k
+  constexpr int NT = D / 8;   // n-tiles of p.V
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x;
-  const int kvh = blockIdx.y / a.head_groups;
-  const int hgrp = blockIdx.y % a.head_groups;
+  const int kvh = blockIdx.y / a.row_groups, rg = blockIdx.y % a.row_groups;
   const int b = blockIdx.z;
-  const int head0 = kvh * a.QPK + hgrp * QT;  // first query head of this CTA
-  const int BS = a.BS;
-  const int nst = a.stages;
-  const int tile_elems = BS * D;
-  constexpr int EB = KV8 ? 1 : 2;  // cache bytes per element
-  const uint32_t tile_bytes = static_cast<uint32_t>(tile_elems) * EB;
+  const int H = a.H, q = a.q, QPK = a.QPK;
+  const Span sp = span_of(a, b, split == 0 && blockIdx.y == 0 && threadIdx.x == 0);
 
-  const SeqSpan sp = seq_span(a, b, split == 0 && blockIdx.y == 0 && threadIdx.x == 0);
-  const int H = a.H;
-  if (sp.L == 0) {  // no keys: the output row is zero
-    if (split == 0) {
-      uint16_t *o = static_cast<uint16_t *>(a.out) + static_cast<int64_t>(b) * H * D + head0 * D;
-      for (int k = threadIdx.x; k < QT * D; k += kDecThreads) o[k] = 0;
+  // this lane's two rows of the m16 tile: g and g + 8
+  const int g = lane >> 2, tq = lane & 3;
+  int R[2], orow[2], pos[2], lo[2];
+  bool valid[2];
+  float slope[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    R[x] = rg * kRows + g + 8 * x;
+    valid[x] = R[x] < a.rows;
+    const int t = valid[x] ? R[x] / QPK : 0, h = valid[x] ? R[x] % QPK : 0;
+    const int head = kvh * QPK + h;
+    orow[x] = (b * q + t) * H + head;  // output row (token, head)
+    pos[x] = sp.L - q + t;
+    lo[x] = a.window > 0 ? max(0, pos[x] - a.window + 1) : 0;
+    slope[x] = (a.alibi && valid[x]) ? __ldg(a.alibi + head) * kLog2e : 0.f;
+  }
+
+  if (sp.L == 0) {  // padding (or a reported bad length): zero rows
+    if (split == 0 && warp == 0) {
+      uint16_t *o16 = static_cast<uint16_t *>(a.out);
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+        if (valid[x])
+          for (int d = tq; d < D; d += 4) o16[static_cast<int64_t>(orow[x]) * D + d] = 0;
     }
     return;
   }
-  const int blk_begin = sp.first_blk + split * a.split_blocks;
-  const int blk_end = min(blk_begin + a.split_blocks, sp.first_blk + sp.nblk);
-  if (split >= sp.nsplit || blk_begin >= blk_end) return;
-  const int nb_split = blk_end - blk_begin;
+  const int u_begin = sp.first_unit + split * a.split_units;
+  const int u_end = min(u_begin + a.split_units, sp.first_unit + sp.nunits);
+  if (split >= sp.nsplit || u_begin >= u_end) return;
+  const int nu = u_end - u_begin;
 
-  // ---- shared memory carve-up -------------------------------------------
-  uint8_t *tiles = smem;  // [warp][stage][K,V][tile]
-  float *sP = reinterpret_cast<float *>(smem + static_cast<size_t>(kDecWarps) * nst * 2 * tile_bytes);
-  int32_t *sTable = reinterpret_cast<int32_t *>(sP + kDecWarps * kSub * QT);
+  uint8_t *tiles = smem;
+  int32_t *coord = reinterpret_cast<int32_t *>(smem + L::TILES);
   uint64_t *bars = reinterpret_cast<uint64_t *>(
-      reinterpret_cast<uint8_t *>(sTable) + ((a.split_blocks * 4 + 15) / 16) * 16);
+      smem + L::TILES + ((a.split_units * 4 + 15) / 16) * 16);
 
   if (threadIdx.x == 0) prefetch_tensormap(&tmap);
-  // Physical blocks of this split, range-checked once.
+  // cache row coordinate of each unit of the split, range-checked once
   const int32_t *trow = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
-  for (int k = threadIdx.x; k < nb_split; k += kDecThreads) {
-    int32_t pb = __ldg(trow + blk_begin + k);
+  for (int k = threadIdx.x; k < nu; k += kThreads) {
+    const int p0 = (u_begin + k) * kUnit;
+    const int lb = p0 / a.BS;
+    int pb = __ldg(trow + lb);
     if (pb < 0 || pb >= a.num_blocks) {
-      record_error(PKV_ERR_BOUNDS, static_cast<int64_t>(b) * a.max_blocks_per_seq + blk_begin + k);
+      record_error(PKV_ERR_BOUNDS, static_cast<int64_t>(b) * a.max_blocks_per_seq + lb);
       pb = 0;
     }
-    sTable[k] = pb;
+    coord[k] = pb * a.BS + p0 % a.BS;
   }
-  uint64_t *wbar = bars + warp * nst;
+  uint64_t *wbar = bars + warp * kStages;
   if (lane == 0) {
-    for (int st = 0; st < nst; ++st) mbar_init(&wbar[st], 1);
+    for (int st = 0; st < kStages; ++st) mbar_init(&wbar[st], 1);
     fence_mbar_init();
   }
   __syncthreads();
 
-  // ---- this warp's blocks: k-th is split block warp + 4k -------------------
-  const int my_count = nb_split > warp ? (nb_split - warp + kDecWarps - 1) / kDecWarps : 0;
-  uint8_t *wtiles = tiles + static_cast<size_t>(warp) * nst * 2 * tile_bytes;
+  const int my_count = nu > warp ? (nu - warp + kWarps - 1) / kWarps : 0;
+  uint8_t *wt = tiles + warp * kStages * L::STAGE;
   auto issue = [&](int k) {
-    const int st = k % nst;
-    const int pb = sTable[warp + k * kDecWarps];
-    mbar_arrive_expect_tx(&wbar[st], 2u * tile_bytes);
-    uint8_t *kt = wtiles + static_cast<size_t>(st) * 2 * tile_bytes;
-    tma_load_4d(kt, &tmap, &wbar[st], 0, kvh, pb * BS, 0);
-    tma_load_4d(kt + tile_bytes, &tmap, &wbar[st], 0, kvh, pb * BS, 1);
+    const int st = k % kStages;
+    const int c = coord[warp + k * kWarps];
+    mbar_arrive_expect_tx(&wbar[st], 2u * L::TILE);
+    uint8_t *kt = wt + st * L::STAGE;
+    if constexpr (KV8) {  // one box of 16 rows x D codes each
+      tma_load_4d(kt, &tmap, &wbar[st], 0, kvh, c, 0);
+      tma_load_4d(kt + L::TILE, &tmap, &wbar[st], 0, kvh, c, 1);
+    } else {
+#pragma unroll
+      for (int r = 0; r < D / 64; ++r) {
+        tma_load_4d(kt + r * L::BOX, &tmap, &wbar[st], 64 * r, kvh, c, 0);
+        tma_load_4d(kt + L::TILE + r * L::BOX, &tmap, &wbar[st], 64 * r, kvh, c, 1);
+      }
+    }
   };
   int issued = 0;
-  if (lane == 0) {
-    for (; issued < min(nst, my_count); ++issued) issue(issued);
+  if (lane == 0)
+    for (; issued < min(kStages, my_count); ++issued) issue(issued);
+
+  // ---- Q fragments (A operand, row-major 16 x 16 per k-step) ---------------
+  uint32_t qa[KS][4];
+  float sl2 = a.scale_log2;
+  if constexpr (KV8) {
+    // permuted dims: k-step s, positions 2tq, 2tq+1 -> dims tq * D/4 + 4s + 0, 1
+    // and positions 8 + 2tq, 9 + 2tq -> + 2, 3: four consecutive elements
+    uint2 raw[2][KS];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const uint2 *qp = reinterpret_cast<const uint2 *>(a.query) +
+                        (static_cast<int64_t>(orow[x]) * D + tq * (D / 4)) / 4;
+#pragma unroll
+      for (int s = 0; s < KS; ++s) raw[x][s] = valid[x] ? __ldg(qp + s) : make_uint2(0u, 0u);
+    }
+    if constexpr (std::is_same<T, BF16>::value) {
+      uint32_t am = 0;  // per-halfword max of |bf16| bit patterns
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int s = 0; s < KS; ++s)
+          am = __vmaxu2(am, __vmaxu2(raw[x][s].x & 0x7fff7fffu, raw[x][s].y & 0x7fff7fffu));
+      // every warp holds the whole row group, so a warp's max is the group's
+      am = __reduce_max_sync(0xffffffffu, max(am & 0xffffu, am >> 16));
+      const int E = static_cast<int>(am >> 7);
+      // largest |q| * 2^-e in [2^14, 2^15): inside fp16's range, full precision
+      const int e = E == 0 ? 0 : min(64, max(-64, E - 141));
+      const float mul = __int_as_float((127 - e) << 23);
+      sl2 *= __int_as_float((127 + e) << 23);
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+          const float2 f0 = BF16::to_f2(raw[x][s].x), f1 = BF16::to_f2(raw[x][s].y);
+          qa[s][x] = FP16::from_f2(f0.x * mul, f0.y * mul);
+          qa[s][2 + x] = FP16::from_f2(f1.x * mul, f1.y * mul);
+        }
+    } else {
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+          qa[s][x] = raw[x][s].x;
+          qa[s][2 + x] = raw[x][s].y;
+        }
+    }
+  } else {
+    const uint32_t *q0 = reinterpret_cast<const uint32_t *>(a.query) +
+                         (static_cast<int64_t>(orow[0]) * D) / 2;
+    const uint32_t *q1 = reinterpret_cast<const uint32_t *>(a.query) +
+                         (static_cast<int64_t>(orow[1]) * D) / 2;
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+      qa[s][0] = valid[0] ? __ldg(q0 + 8 * s + tq) : 0u;
+      qa[s][1] = valid[1] ? __ldg(q1 + 8 * s + tq) : 0u;
+      qa[s][2] = valid[0] ? __ldg(q0 + 8 * s + 4 + tq) : 0u;
+      qa[s][3] = valid[1] ? __ldg(q1 + 8 * s + 4 + tq) : 0u;
+    }
   }
 
-  // ---- query registers (pre-scaled into the log2 domain) ------------------
-  const int dg = lane & 7, ts = lane >> 3;
-  unsigned long long q2[QT][CPL * 4];  // packed dim pairs
-  {
-    const uint4 *qrow = reinterpret_cast<const uint4 *>(a.query + (static_cast<int64_t>(b) * H + head0) * D);
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float o[NT][4];
 #pragma unroll
-    for (int h = 0; h < QT; ++h)
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        float f[8];
-        load_chunk_f32<T>(__ldg(qrow + h * ROWC + c * 8 + dg), f);
-#pragma unroll
-        for (int e = 0; e < 8; e += 2)
-          q2[h][c * 4 + e / 2] = f2pack(f[e] * a.scale_log2, f[e + 1] * a.scale_log2);
-      }
-  }
-  float slope[QT];
-#pragma unroll
-  for (int h = 0; h < QT; ++h) slope[h] = a.alibi ? __ldg(a.alibi + head0 + h) * kLog2e : 0.f;
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
-  constexpr int NF = NfOf<QT>::v;  // dots (heads) each lane finishes per sub-tile
-  float slope_own[NF];  // ALiBi slopes of this lane's heads head_of(dg, f)
-#pragma unroll
-  for (int f = 0; f < NF; ++f) {
-    if constexpr (QT == 4) slope_own[f] = (dg & 1) ? slope[2 + f] : slope[f];
-    else if constexpr (QT == 2) slope_own[f] = (dg & 1) ? slope[1] : slope[0];
-    else slope_own[f] = slope[0];
-  }
-  float m[NF], l[NF];
-  unsigned long long o2[QT][DPL / 2];  // packed output dim pairs
-#pragma unroll
-  for (int f = 0; f < NF; ++f) {
-    m[f] = -INFINITY;
-    l[f] = 0.f;
-  }
-#pragma unroll
-  for (int h = 0; h < QT; ++h)
-#pragma unroll
-    for (int e = 0; e < DPL / 2; ++e) o2[h][e] = 0ull;  // (+0, +0)
-  float *wP = sP + warp * kSub * QT;
-  const int qpos = sp.L - 1;
+  // ldmatrix row addresses: lane -> (matrix mi, row rr)
+  const int mi = lane >> 3, rr = lane & 7;
+  const int k_tok = (mi >> 1) * 8 + rr, k_half = mi & 1;  // K: tokens x dim halves
+  const int v_tok = (mi & 1) * 8 + rr, v_half = mi >> 1;  // V^T: token halves x dims
   bool ok = true;
   int consumed = 0;
+  uint8_t *v16 = tiles + kWarps * kStages * L::STAGE + warp * L::V16;  // fp8: widened V
 
   for (int k = 0; k < my_count; ++k) {
-    const int st = k % nst;
-    // every lane observes the phase (acquire); the verdict is warp-uniform
-    const bool got = mbar_wait_bounded(&wbar[st], (k / nst) & 1, b);
+    const int st = k % kStages;
+    const bool got = mbar_wait_bounded(&wbar[st], (k / kStages) & 1, b);
     if (!__all_sync(0xffffffffu, got)) {
       ok = false;
       break;
     }
     consumed = k + 1;
-    const uint8_t *kt = wtiles + static_cast<size_t>(st) * 2 * tile_bytes;
-    const uint8_t *vt = kt + tile_bytes;
-    const int blk = blk_begin + warp + k * kDecWarps;  // logical block
-    for (int sub = 0; sub < BS; sub += kSub) {
-      const int j0 = blk * BS + sub;  // position of the sub-tile's token 0
-      const int t_lo = max(sp.lo - j0, 0);
-      const int t_hi = min(sp.L - j0, kSub);
-      if (t_lo >= t_hi) continue;  // warp-uniform
-      // ---- q.k for 16 tokens: lane (dg, ts) accumulates partial dots of
-      // tokens it*4 + ts over its dims, index it * QT + h ---------------------
-      constexpr int NV = (kSub / 4) * QT;  // partial dots per lane
-      float v[NV];
-      const uint4 *k4 = reinterpret_cast<const uint4 *>(kt + sub * D * EB);
-      const uint2 *k2 = reinterpret_cast<const uint2 *>(kt + sub * D * EB);
+    const uint32_t kt = smem_u32(wt + st * L::STAGE);
+    uint32_t vt = kt + L::TILE;
+    const int j0 = (u_begin + warp + k * kWarps) * kUnit;  // position of the unit's key 0
+
+    // ---- S = Q K^T: two n-tiles of 8 keys ---------------------------------
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if constexpr (KV8) {
+      // keys g and g + 8: this lane's D/4 codes of each, widened per k-step
+      const uint8_t *kc = wt + st * L::STAGE;
+      uint4 kk[2][D / 64];
 #pragma unroll
-      for (int it = 0; it < kSub / 4; ++it) {
-        const int tok = it * 4 + ts;
-        unsigned long long acc[QT];  // even / odd dim partial sums
+      for (int n = 0; n < 2; ++n)
 #pragma unroll
-        for (int h = 0; h < QT; ++h) acc[h] = 0ull;
+        for (int c = 0; c < D / 64; ++c)
+          kk[n][c] = *reinterpret_cast<const uint4 *>(kc + (g + 8 * n) * D + tq * (D / 4) + 16 * c);
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          float f[8];
-          if constexpr (KV8)
-            load_chunk8_f32(k2[tok * ROWC + c * 8 + dg], f);
-          else
-            load_chunk_f32<T>(k4[tok * ROWC + c * 8 + dg], f);
+      for (int s = 0; s < KS; ++s)
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const unsigned long long kk = f2pack(f[e], f[e + 1]);
+        for (int n = 0; n < 2; ++n) {
+          const uint2 kb = e4m3x4_to_h4(word_of(kk[n][s / 4], s % 4));
+          mma16816<MT>(sc[n], qa[s], kb.x, kb.y);
+        }
+      // this unit's V codes -> the warp's swizzled fp16 tile: lane (token
+      // vt_, half vh) widens D/2 codes, 16 at a time, reads rotated by token
+      const uint8_t *vc = kc + L::TILE;
+      const int vt_ = lane >> 1, vh = lane & 1;
+      constexpr int NI = D / 32;  // 16-code pieces per lane
 #pragma unroll
-            for (int h = 0; h < QT; ++h) acc[h] = ffma2(q2[h][c * 4 + e / 2], kk, acc[h]);
+      for (int i = 0; i < NI; ++i) {
+        const int ip = (i + vt_) % NI;
+        const int d0 = vh * (D / 2) + 16 * ip;
+        const uint4 u = *reinterpret_cast<const uint4 *>(vc + vt_ * D + d0);
+        const uint2 h0 = e4m3x4_to_h4(u.x), h1 = e4m3x4_to_h4(u.y);
+        const uint2 h2 = e4m3x4_to_h4(u.z), h3 = e4m3x4_to_h4(u.w);
+        *reinterpret_cast<uint4 *>(v16 + swz(vt_, d0 / 8)) = make_uint4(h0.x, h0.y, h1.x, h1.y);
+        *reinterpret_cast<uint4 *>(v16 + swz(vt_, d0 / 8 + 1)) =
+            make_uint4(h2.x, h2.y, h3.x, h3.y);
+      }
+      vt = smem_u32(v16);
+    } else {
+#pragma unroll
+      for (int s = 0; s < KS; ++s) {
+        uint32_t kb[4];
+        ldsm_x4(kt + swz(k_tok, 2 * s + k_half), kb);
+        mma16816<T>(sc[0], qa[s], kb[0], kb[1]);
+        mma16816<T>(sc[1], qa[s], kb[2], kb[3]);
+      }
+    }
+    // ---- scores in the log2 domain, per-row masks --------------------------
+    // sc[n][e] : row g (e < 2) or g + 8 (e >= 2), key j0 + 8n + 2tq + (e & 1)
+    float x[2][4];  // [row][n * 2 + (e & 1)]
+    bool grow = false;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = e >> 1;
+        const int j = j0 + 8 * n + 2 * tq + (e & 1);
+        float v = fmaf(sc[n][e], sl2, slope[r] * static_cast<float>(j - pos[r]));
+        if (!valid[r] || j < lo[r] || j > pos[r]) v = -INFINITY;
+        x[r][n * 2 + (e & 1)] = v;
+        grow |= v > m[r] + kLazy;
+      }
+    if (__any_sync(0xffffffffu, grow)) {
+      // move the references to the true row maxima (4 lanes hold a row)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float mx = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m[r], mx);
+        if (mn > m[r]) {
+          const float alpha = m[r] == -INFINITY ? 0.f : fast_exp2(m[r] - mn);
+          m[r] = mn;
+          l[r] *= alpha;
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            o[n][2 * r] *= alpha;
+            o[n][2 * r + 1] *= alpha;
           }
         }
-#pragma unroll
-        for (int h = 0; h < QT; ++h) {
-          float x, y;
-          f2unpack(acc[h], x, y);
-          v[it * QT + h] = x + y;
-        }
       }
-      // Recursive halving over the 8 dg lanes (xor 4, 2, 1): each level a lane
-      // keeps half of its values and adds the partner's copy of that half, so
-      // the 8 lanes finish the NV dots between them (NF each) instead of every
-      // lane finishing all of them.
-      reduce_over_dg<NV>(v, lane);
-      // lane now holds NF dots of token tk = (dg >> 1) * 4 + ts, heads head_of(dg, f)
-      const int tk = (dg >> 1) * 4 + ts;
-      const int j = j0 + tk;
-      const bool valid = tk >= t_lo && tk < t_hi;
-      float sc[NF];
-#pragma unroll
-      for (int f = 0; f < NF; ++f)
-        sc[f] = valid ? v[f] + slope_own[f] * static_cast<float>(j - qpos) : -INFINITY;
-      // ---- online softmax with a lazy reference max: while no score exceeds
-      // the head's reference m by more than kLazy (log2 units) the weights
-      // 2^(s - m) stay <= 2^kLazy and nothing is rescaled; otherwise the
-      // reference moves to the true running max (the 16 lanes of a head) --
-      bool grow = false;
-#pragma unroll
-      for (int f = 0; f < NF; ++f) grow |= sc[f] > m[f] + kLazy;
-      if (!__any_sync(0xffffffffu, grow)) {
-#pragma unroll
-        for (int f = 0; f < NF; ++f) {
-          const float p = fast_exp2(sc[f] - m[f]);
-          l[f] += p;
-          if (QT > 1 || (dg & 1) == 0) wP[tk * QT + head_of<QT>(dg, f)] = p;
-        }
-        __syncwarp();
-      } else {
-        float alpha_own[NF];
-#pragma unroll
-        for (int f = 0; f < NF; ++f) {
-          float bm = sc[f];
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-          const float mn = fmaxf(m[f], bm);
-          alpha_own[f] = fast_exp2(m[f] - mn);
-          m[f] = mn;
-          const float p = fast_exp2(sc[f] - mn);
-          l[f] = l[f] * alpha_own[f] + p;  // per-lane partial, summed at the end
-          if (QT > 1 || (dg & 1) == 0) wP[tk * QT + head_of<QT>(dg, f)] = p;
-        }
-        // every lane needs every head's rescale factor for its p.V accumulators
-        float alpha[QT];
-        if constexpr (QT == 4) {
-          const float x0 = __shfl_xor_sync(0xffffffffu, alpha_own[0], 1);
-          const float x1 = __shfl_xor_sync(0xffffffffu, alpha_own[1], 1);
-          const bool hi = dg & 1;
-          alpha[0] = hi ? x0 : alpha_own[0];
-          alpha[1] = hi ? x1 : alpha_own[1];
-          alpha[2] = hi ? alpha_own[0] : x0;
-          alpha[3] = hi ? alpha_own[1] : x1;
-        } else if constexpr (QT == 2) {
-          const float x0 = __shfl_xor_sync(0xffffffffu, alpha_own[0], 1);
-          const bool hi = dg & 1;
-          alpha[0] = hi ? x0 : alpha_own[0];
-          alpha[1] = hi ? alpha_own[0] : x0;
-        } else {
-          alpha[0] = alpha_own[0];
-        }
-#pragma unroll
-        for (int h = 0; h < QT; ++h) {
-          const unsigned long long a2 = f2pack(alpha[h], alpha[h]);
-#pragma unroll
-          for (int e = 0; e < DPL / 2; ++e) o2[h][e] = fmul2(o2[h][e], a2);
-        }
-        __syncwarp();
-      }
-      // ---- p.V over the valid tokens ---------------------------------------
-      const uint8_t *vrow = vt + (sub * D + lane * DPL) * EB;
-      for (int tok = t_lo; tok < t_hi; ++tok) {
-        float vf[DPL];
-        if constexpr (KV8 && DPL == 4) {
-          const uint32_t u = *reinterpret_cast<const uint32_t *>(vrow + tok * D);
-          float2 t0 = e4m3x2_to_f2(u), t1 = e4m3x2_to_f2(u >> 16);
-          vf[0] = t0.x; vf[1] = t0.y; vf[2] = t1.x; vf[3] = t1.y;
-        } else if constexpr (KV8) {
-          const uint32_t u = *reinterpret_cast<const uint16_t *>(vrow + tok * D);
-          float2 t0 = e4m3x2_to_f2(u);
-          vf[0] = t0.x; vf[1] = t0.y;
-        } else if constexpr (DPL == 4) {
-          const uint2 u = *reinterpret_cast<const uint2 *>(vrow + tok * D * 2);
-          float2 t0 = T::to_f2(u.x), t1 = T::to_f2(u.y);
-          vf[0] = t0.x; vf[1] = t0.y; vf[2] = t1.x; vf[3] = t1.y;
-        } else {
-          const uint32_t u = *reinterpret_cast<const uint32_t *>(vrow + tok * D * 2);
-          float2 t0 = T::to_f2(u);
-          vf[0] = t0.x; vf[1] = t0.y;
-        }
-        float pp[QT];
-        if constexpr (QT == 4) {
-          const float4 p4 = *reinterpret_cast<const float4 *>(wP + tok * 4);
-          pp[0] = p4.x; pp[1] = p4.y; pp[2] = p4.z; pp[3] = p4.w;
-        } else {
-#pragma unroll
-          for (int h = 0; h < QT; ++h) pp[h] = wP[tok * QT + h];
-        }
-        unsigned long long vv[DPL / 2];
-#pragma unroll
-        for (int e = 0; e < DPL / 2; ++e) vv[e] = f2pack(vf[2 * e], vf[2 * e + 1]);
-#pragma unroll
-        for (int h = 0; h < QT; ++h) {
-          const unsigned long long p2 = f2pack(pp[h], pp[h]);
-#pragma unroll
-          for (int e = 0; e < DPL / 2; ++e) o2[h][e] = ffma2(p2, vv[e], o2[h][e]);
-        }
-      }
-      __syncwarp();
     }
-    // stage st is free again: refill it
+    // ---- P (A operand of P V): rows g / g + 8, keys 2tq.. and 8 + 2tq.. -----
+    uint32_t pa[4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float mr = m[r] == -INFINITY ? 0.f : m[r];
+      float p[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) p[c] = fast_exp2(x[r][c] - mr);
+      l[r] += (p[0] + p[1]) + (p[2] + p[3]);
+      pa[r] = MT::from_f2(p[0], p[1]);      // keys 2tq, 2tq + 1
+      pa[2 + r] = MT::from_f2(p[2], p[3]);  // keys 8 + 2tq, 9 + 2tq
+    }
+    if constexpr (KV8) __syncwarp();  // the widened V tile is complete
+    // ---- O += P V: n-tiles of 8 dims, two per ldmatrix ---------------------
+#pragma unroll
+    for (int n2 = 0; n2 < NT / 2; ++n2) {
+      uint32_t vb[4];
+      ldsm_x4_t(vt + swz(v_tok, 2 * n2 + v_half), vb);
+      mma16816<MT>(o[2 * n2], pa, vb[0], vb[1]);
+      mma16816<MT>(o[2 * n2 + 1], pa, vb[2], vb[3]);
+    }
+    __syncwarp();  // every lane has read the stage: refill it
     if (lane == 0 && issued < my_count) {
       issue(issued);
       ++issued;
@@ -439,56 +459,58 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
   }
   issued = __shfl_sync(0xffffffffu, issued, 0);
   if (!ok) {  // drain this warp's copies still in flight, bounded
-    for (int k = consumed; k < issued; ++k) mbar_wait_bounded(&wbar[k % nst], (k / nst) & 1, b);
+    for (int k = consumed; k < issued; ++k) mbar_wait_bounded(&wbar[k % kStages], (k / kStages) & 1, b);
   }
 
-  // ---- merge the 4 warps' softmax states ----------------------------------
-  __syncthreads();  // every warp's TMA traffic has landed; tiles are reusable
-  float *sM = reinterpret_cast<float *>(smem);          // [warp][QT]
-  float *sL = sM + kDecWarps * QT;                       // [warp][QT]
-  float *sO = sL + kDecWarps * QT;                       // [warp][QT][D]
+  // ---- merge the 4 warps' (m, l, O) ----------------------------------------
 #pragma unroll
-  for (int h = 0; h < QT; ++h)
+  for (int r = 0; r < 2; ++r) {
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+  }
+  __syncthreads();  // all TMA traffic has landed; the tile area is reusable
+  float *sM = reinterpret_cast<float *>(smem);  // [warp][row]
+  float *sL = sM + kWarps * kRows;               // [warp][row]
+  float *sO = sL + kWarps * kRows;               // [warp][row][D]
+  if (tq == 0) {
+    sM[warp * kRows + g] = ok ? m[0] : -INFINITY;
+    sM[warp * kRows + g + 8] = ok ? m[1] : -INFINITY;
+    sL[warp * kRows + g] = ok ? l[0] : 0.f;
+    sL[warp * kRows + g + 8] = ok ? l[1] : 0.f;
+  }
 #pragma unroll
-    for (int e = 0; e < DPL / 2; ++e) {
-      float x, y;
-      f2unpack(o2[h][e], x, y);
-      sO[(warp * QT + h) * D + lane * DPL + 2 * e] = x;
-      sO[(warp * QT + h) * D + lane * DPL + 2 * e + 1] = y;
-    }
-#pragma unroll
-  for (int f = 0; f < NF; ++f) {
-    float lt = l[f];
-    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
-    lt += __shfl_xor_sync(0xffffffffu, lt, 4);
-    lt += __shfl_xor_sync(0xffffffffu, lt, 8);
-    lt += __shfl_xor_sync(0xffffffffu, lt, 16);
-    if (lane < 2 && (QT > 1 || lane == 0)) {
-      const int hf = head_of<QT>(lane, f);
-      sM[warp * QT + hf] = m[f];
-      sL[warp * QT + hf] = lt;
-    }
+  for (int n = 0; n < NT; ++n) {
+    float *r0 = sO + (warp * kRows + g) * D + 8 * n + 2 * tq;
+    float *r1 = r0 + 8 * D;
+    r0[0] = o[n][0];
+    r0[1] = o[n][1];
+    r1[0] = o[n][2];
+    r1[1] = o[n][3];
   }
   __syncthreads();
   const bool single = sp.nsplit == 1;
-  for (int idx = threadIdx.x; idx < QT * D; idx += kDecThreads) {
-    const int h = idx / D, d = idx % D;
+  for (int idx = threadIdx.x; idx < kRows * D; idx += kThreads) {
+    const int r = idx / D, d = idx % D;
+    const int Rr = rg * kRows + r;
+    if (Rr >= a.rows) continue;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sM[w * QT + h]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sM[w * kRows + r]);
     float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) {
-      const float e = fast_exp2(sM[w * QT + h] - M);
-      num = fmaf(e, sO[(w * QT + h) * D + d], num);
-      den = fmaf(e, sL[w * QT + h], den);
+      for (int w = 0; w < kWarps; ++w) {
+        const float e = fast_exp2(sM[w * kRows + r] - M);
+        num = fmaf(e, sO[(w * kRows + r) * D + d], num);
+        den = fmaf(e, sL[w * kRows + r], den);
+      }
     }
-    const float val = num / den * a.v_scale;
-    const int64_t hh = static_cast<int64_t>(b) * H + head0 + h;
+    const float val = den > 0.f ? num / den * a.v_scale : 0.f;
+    const int t = Rr / QPK, h = Rr % QPK;
+    const int64_t hh = static_cast<int64_t>(b * q + t) * H + kvh * QPK + h;
     if (single) {
       uint16_t *o16 = static_cast<uint16_t *>(a.out);
-      const uint32_t packed = T::from_f2(val, 0.f);
-      o16[hh * D + d] = static_cast<uint16_t>(packed & 0xffffu);
+      o16[hh * D + d] = static_cast<uint16_t>(T::from_f2(val, 0.f) & 0xffffu);
     } else {
       const int64_t slot = hh * a.max_splits + split;
       a.part_o[slot * D + d] = val;
@@ -500,98 +522,85 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
   }
 }
 
-// One CTA per (query head, sequence) with more than one split.
+// One CTA per (decode token row, query head) of a sequence with several splits.
 template <class T, int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
-  const int h = blockIdx.x, b = blockIdx.y;
-  const SeqSpan sp = seq_span(a, b, false);
-  if (sp.nsplit <= 1) return;  // the split kernel wrote the output itself
-  const int64_t hh = static_cast<int64_t>(b) * a.H + h;
+__global__ void __launch_bounds__(D) decode_combine_kernel(const Args a) {
+  const int row = blockIdx.x, h = blockIdx.y;  // row = b * q + t
+  const int b = row / a.q;
+  const Span sp = span_of(a, b, false);
+  if (sp.L == 0 || sp.nsplit <= 1) return;  // written by the split kernel
+  const int64_t hh = static_cast<int64_t>(row) * a.H + h;
   const float *ml = a.part_ml + hh * a.max_splits * 2;
   float M = -INFINITY;
   for (int s = 0; s < sp.nsplit; ++s) M = fmaxf(M, ml[2 * s]);
   const int d = threadIdx.x;
   const float *po = a.part_o + hh * a.max_splits * D + d;
   float num = 0.f, den = 0.f;
-  for (int s = 0; s < sp.nsplit; ++s) {
-    const float w = fast_exp2(ml[2 * s] - M) * ml[2 * s + 1];
-    num = fmaf(w, po[static_cast<int64_t>(s) * D], num);
-    den += w;
+  if (M != -INFINITY) {
+    for (int s = 0; s < sp.nsplit; ++s) {
+      const float w = fast_exp2(ml[2 * s] - M) * ml[2 * s + 1];
+      num = fmaf(w, po[static_cast<int64_t>(s) * D], num);
+      den += w;
+    }
   }
-  const float val = num / den;
+  const float val = den > 0.f ? num / den : 0.f;
   uint16_t *o16 = static_cast<uint16_t *>(a.out);
   o16[hh * D + d] = static_cast<uint16_t>(T::from_f2(val, 0.f) & 0xffffu);
 }
 
-// ---------------------------------------------------------------------------
-// Host side
-// ---------------------------------------------------------------------------
-static int stages_for(int BS) { return BS <= 16 ? 2 : 1; }
-
-static size_t split_smem_bytes(int BS, int D, int QT, int split_blocks, int eb) {
-  const size_t tiles = static_cast<size_t>(kDecWarps) * stages_for(BS) * 2 * BS * D * eb;
-  const size_t p = static_cast<size_t>(kDecWarps) * kSub * QT * 4;
-  const size_t table = ((split_blocks * 4 + 15) / 16) * 16;
-  const size_t bars = static_cast<size_t>(kDecWarps) * stages_for(BS) * 8;
-  return tiles + p + table + bars;
+template <class T, int D, bool KV8>
+static cudaError_t launch_typed(const Args &a, const CUtensorMap &tmap, int KVH, int num_seqs,
+                                cudaStream_t stream) {
+  const size_t table = ((a.split_units * 4 + 15) / 16) * 16;
+  const size_t smem = 1024 + Lay<D, KV8>::TILES + table + kWarps * kStages * 8;  // + alignment
+  auto kern = decode_kernel<T, D, KV8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.max_splits, KVH * a.row_groups, num_seqs);
+  kern<<<grid, kThreads, smem, stream>>>(a, tmap);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.max_splits <= 1) return e;
+  decode_combine_kernel<T, D><<<dim3(num_seqs * a.q, a.H), D, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
-DecodePlan plan_decode(int num_seqs, int max_seq_len, const Geometry &g, int sms) {
+}  // namespace dec
+
+DecodePlan plan_decode(int num_seqs, int query_len, int max_seq_len,
+                                  const Geometry &g, int sms) {
   DecodePlan p{};
-  const int BS = g.BS;
-  int eff = max_seq_len;
-  int eff_blocks;
-  if (g.window > 0 && g.window < max_seq_len) {
-    eff = g.window;
-    eff_blocks = (eff + BS - 1) / BS + 1;  // a window start can straddle a block
-  } else {
-    eff_blocks = (eff + BS - 1) / BS;
-  }
-  eff_blocks = std::max(eff_blocks, 1);
-  const int QT = g.QPK >= 4 ? 4 : g.QPK;
-  const int64_t items = static_cast<int64_t>(num_seqs) * g.KVH * (g.QPK / QT);
-  // Splits of ~1024 tokens bound the longest CTA (load balance over uneven
-  // lengths) while keeping the fp32 partials small; shrink them while the
-  // grid would leave SMs idle.  (Measured, 256 sequences of 512..4096 tokens:
-  // 0.889 / 0.918 / 0.900 of HBM with 512 / 1024 / 2048-token splits.)
-  int split_blocks = std::max(1024 / BS, 4);
-  while (split_blocks > 8 &&
-         items * ((eff_blocks + split_blocks - 1) / split_blocks) < 8LL * sms)
-    split_blocks /= 2;
-  if (eff_blocks <= 2 * split_blocks) split_blocks = eff_blocks;  // short: one split
-  p.split_blocks = split_blocks;
-  p.max_splits = (eff_blocks + split_blocks - 1) / split_blocks;
-  p.workspace_bytes = 0;
+  const int U = dec::kUnit;
+  // keys the batch's widest row set can see
+  int eff = std::max(max_seq_len, 1);
+  if (g.window > 0 && g.window + query_len - 1 < eff) eff = g.window + query_len - 1;
+  const int units = (eff + U - 1) / U + 1;  // a window start can straddle a unit
+  p.row_groups = (query_len * g.QPK + dec::kRows - 1) / dec::kRows;
+  const int64_t items = static_cast<int64_t>(num_seqs) * g.KVH * p.row_groups;
+  // Splits of up to 128 units (2048 keys): every split writes fp32 partials of
+  // all its q * QPK rows, so short splits cost real HBM traffic; shrink them
+  // only while the grid would leave SMs idle.  (Measured on 128 sequences x 4
+  // tokens, 512..4096 keys: 0.71 / 0.82 / 0.85 of HBM with 32 / 64 / 128.)
+  int split_units = 128;
+  while (split_units > 8 && items * ((units + split_units - 1) / split_units) < 8LL * sms)
+    split_units /= 2;
+  if (units <= 2 * split_units) split_units = units;  // short: one split
+  p.split_units = split_units;
+  p.max_splits = (units + split_units - 1) / split_units;
   if (p.max_splits > 1) {
-    const size_t n = static_cast<size_t>(num_seqs) * g.H * p.max_splits;
-    p.workspace_bytes = n * g.D * 4 + n * 2 * 4;
-    p.workspace_bytes = (p.workspace_bytes + 255) / 256 * 256;
+    const size_t rows = static_cast<size_t>(num_seqs) * query_len * g.H * p.max_splits;
+    const size_t o_bytes = ((rows * g.D * 4 + 255) / 256) * 256;
+    const size_t ml_bytes = ((rows * 2 * 4 + 255) / 256) * 256;
+    p.workspace_bytes = o_bytes + ml_bytes;
   }
   return p;
 }
 
-template <class T, int D, int QT, bool KV8>
-static cudaError_t launch_typed(const DecodeArgs &a, const CUtensorMap &tmap, int KVH, int num_seqs,
+cudaError_t launch_decode(void *out, const void *query, int num_seqs, int query_len,
+                                const void *kv_cache, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *seq_lens,
+                                const Geometry &g, const DecodePlan &plan, void *workspace,
                                 cudaStream_t stream) {
-  const size_t smem = split_smem_bytes(a.BS, D, QT, a.split_blocks, KV8 ? 1 : 2);
-  auto kern = decode_split_kernel<T, D, QT, KV8>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  dim3 grid(a.max_splits, KVH * a.head_groups, num_seqs);
-  kern<<<grid, kDecThreads, smem, stream>>>(a, tmap);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || a.max_splits <= 1) return e;
-  decode_combine_kernel<T, D><<<dim3(a.H, num_seqs), D, 0, stream>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_decode(void *out, const void *query, int num_seqs, const void *kv_cache,
-                          const int32_t *block_tables, int max_blocks_per_seq,
-                          const int32_t *seq_lens, int max_seq_len, const Geometry &g,
-                          const DecodePlan &plan, void *workspace, cudaStream_t stream) {
-  (void)max_seq_len;
-  // Tensor map over the whole cache: (D, KVH, NB * BS tokens, 2 halves).
   CUtensorMap tmap;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.D), static_cast<cuuint64_t>(g.KVH),
                               static_cast<cuuint64_t>(g.num_blocks * g.BS), 2};
@@ -599,54 +608,57 @@ cudaError_t launch_decode(void *out, const void *query, int num_seqs, const void
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.D) * eb,
                                  static_cast<cuuint64_t>(g.row_elems) * eb,
                                  static_cast<cuuint64_t>(g.num_blocks * g.block_elems) * eb};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(g.D), 1, static_cast<cuuint32_t>(g.BS), 1};
+  // 16-bit cache: 64-dim boxes, 128-byte swizzle (ldmatrix reads them);
+  // fp8 cache: one plain box of D codes per row
+  const cuuint32_t box[4] = {g.fp8 ? static_cast<cuuint32_t>(g.D) : 64u, 1,
+                             static_cast<cuuint32_t>(dec::kUnit), 1};
+  const bool bf = g.dtype == PKV_BF16;
   const CUtensorMapDataType dt =
       g.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-            : (g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+            : (bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   if (encode_tensor_map(&tmap, dt, 4, const_cast<void *>(kv_cache), dims, strides, box,
-                        CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+                        g.fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B) !=
+      CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-
-  DecodeArgs a{};
+  dec::Args a{};
   a.out = out;
   a.query = static_cast<const uint16_t *>(query);
   a.block_tables = block_tables;
   a.seq_lens = seq_lens;
   a.alibi = g.alibi;
-  const size_t n = static_cast<size_t>(num_seqs) * g.H * plan.max_splits;
-  a.part_o = static_cast<float *>(workspace);
-  a.part_ml = plan.max_splits > 1 ? a.part_o + n * g.D : nullptr;
+  if (plan.max_splits > 1) {
+    const size_t rows = static_cast<size_t>(num_seqs) * query_len * g.H * plan.max_splits;
+    const size_t o_bytes = ((rows * g.D * 4 + 255) / 256) * 256;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + o_bytes);
+  }
   a.num_blocks = g.num_blocks;
   a.num_seqs = num_seqs;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.H = g.H;
   a.QPK = g.QPK;
-  const int QT = g.QPK >= 4 ? 4 : g.QPK;
-  a.head_groups = g.QPK / QT;
+  a.q = query_len;
+  a.rows = query_len * g.QPK;
+  a.row_groups = plan.row_groups;
   a.BS = g.BS;
   a.window = g.window;
-  a.split_blocks = plan.split_blocks;
+  a.split_units = plan.split_units;
   a.max_splits = plan.max_splits;
-  a.stages = stages_for(g.BS);
   a.scale_log2 = g.scale * kLog2e * g.k_scale;
   a.v_scale = g.v_scale;
-
-  const bool bf = g.dtype == PKV_BF16;
-#define PKV_DEC(TT, DD, QQ)                                                    \
-  if (g.D == DD && QT == QQ)                                                   \
-    return g.fp8 ? launch_typed<TT, DD, QQ, true>(a, tmap, g.KVH, num_seqs, stream) \
-                 : launch_typed<TT, DD, QQ, false>(a, tmap, g.KVH, num_seqs, stream);
+#define PKV_MT(TT, DD)                                                             \
+  if (g.D == DD)                                                                   \
+    return g.fp8 ? dec::launch_typed<TT, DD, true>(a, tmap, g.KVH, num_seqs, stream) \
+                 : dec::launch_typed<TT, DD, false>(a, tmap, g.KVH, num_seqs, stream);
   if (bf) {
-    PKV_DEC(BF16, 128, 4) PKV_DEC(BF16, 128, 2) PKV_DEC(BF16, 128, 1)
-    PKV_DEC(BF16, 64, 4) PKV_DEC(BF16, 64, 2) PKV_DEC(BF16, 64, 1)
+    PKV_MT(BF16, 128) PKV_MT(BF16, 64)
   } else {
-    PKV_DEC(FP16, 128, 4) PKV_DEC(FP16, 128, 2) PKV_DEC(FP16, 128, 1)
-    PKV_DEC(FP16, 64, 4) PKV_DEC(FP16, 64, 2) PKV_DEC(FP16, 64, 1)
+    PKV_MT(FP16, 128) PKV_MT(FP16, 64)
   }
-#undef PKV_DEC
+#undef PKV_MT
   return cudaErrorInvalidValue;
 }
+
 
 // ---------------------------------------------------------------------------
 // Static decode scratch for callers that cannot allocate device memory.

@@ -51,37 +51,22 @@ cudaError_t launch_kv_swap(const void *src, int64_t src_blocks, void *dst, int64
                            cudaStream_t stream);
 cudaError_t read_device_error_kv_ops(unsigned long long *out);
 
-// decode.cu
+// decode.cu (single- and multi-token decode)
 struct DecodePlan {
-  int split_blocks;  // logical blocks per split
-  int max_splits;    // grid extent over splits (1 = no split, no workspace)
-  size_t workspace_bytes;
-};
-DecodePlan plan_decode(int num_seqs, int max_seq_len, const Geometry &g, int sms);
-cudaError_t launch_decode(void *out, const void *query, int num_seqs, const void *kv_cache,
-                          const int32_t *block_tables, int max_blocks_per_seq,
-                          const int32_t *seq_lens, int max_seq_len, const Geometry &g,
-                          const DecodePlan &plan, void *workspace, cudaStream_t stream);
-cudaError_t read_device_error_decode(unsigned long long *out);
-// Device address and size of the static decode scratch of the current device
-// (looked up on the first call per device).
-cudaError_t static_decode_scratch(void **ptr, size_t *bytes);
-
-// decode_mt.cu (multi-token decode)
-struct MultiDecodePlan {
   int row_groups;   // 16-row groups of (token, head) rows per KV head
   int split_units;  // 16-key units per split
   int max_splits;   // grid extent over splits (1 = no split, no workspace)
   size_t workspace_bytes;
 };
-MultiDecodePlan plan_decode_multi(int num_seqs, int query_len, int max_seq_len,
-                                  const Geometry &g, int sms);
-cudaError_t launch_decode_multi(void *out, const void *query, int num_seqs, int query_len,
-                                const void *kv_cache, const int32_t *block_tables,
-                                int max_blocks_per_seq, const int32_t *seq_lens,
-                                const Geometry &g, const MultiDecodePlan &plan, void *workspace,
-                                cudaStream_t stream);
-cudaError_t read_device_error_decode_multi(unsigned long long *out);
+DecodePlan plan_decode(int num_seqs, int query_len, int max_seq_len, const Geometry &g, int sms);
+cudaError_t launch_decode(void *out, const void *query, int num_seqs, int query_len,
+                          const void *kv_cache, const int32_t *block_tables,
+                          int max_blocks_per_seq, const int32_t *seq_lens, const Geometry &g,
+                          const DecodePlan &plan, void *workspace, cudaStream_t stream);
+cudaError_t read_device_error_decode(unsigned long long *out);
+// Device address and size of the static decode scratch of the current device
+// (looked up on the first call per device).
+cudaError_t static_decode_scratch(void **ptr, size_t *bytes);
 
 // prefill.cu
 cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, int num_seqs,

@@ -158,16 +158,6 @@ struct AB<FP16> {
   static constexpr int v = 0;
 };
 
-// Four E4M3 codes (low byte first) -> two fp16 pairs (low half first),
-// exactly: every E4M3 value is an fp16 value.
-__device__ __forceinline__ uint2 e4m3x4_to_h4(uint32_t u) {
-  uint2 r;
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-      : "=r"(r.x), "=r"(r.y)
-      : "r"(u));
-  return r;
-}
 
 // One query tile of the CTA: head, first row within the sequence, rows,
 // and the half-open range of the CTA's key tiles it needs.

@@ -90,9 +90,9 @@ def test_decode_and_prefill_validation(lib):
                                  nul) == B.PKV_ERR_INVALID
     assert lib.paged_attn_decode(nul, nul, 70000, nul, 4, nul, 1, nul, 8, ctypes.byref(p), nul,
                                  0, nul) == B.PKV_ERR_INVALID
-    p3 = _p(num_heads=24, num_kv_heads=8)  # 3 queries per KV head: not built for decode
+    p3 = _p(num_heads=24, num_kv_heads=8)  # any group size: here the null pointers fail
     assert lib.paged_attn_decode(nul, nul, 2, nul, 4, nul, 1, nul, 8, ctypes.byref(p3), nul, 0,
-                                 nul) == B.PKV_ERR_UNSUPPORTED
+                                 nul) == B.PKV_ERR_INVALID
     assert lib.paged_attn_prefill_varlen(nul, nul, 10, 3, nul, nul, 0, 5, nul, 4, nul, 1,
                                          ctypes.byref(p), nul) == B.PKV_OK
     assert lib.paged_attn_prefill_varlen(nul, nul, 10, 3, nul, nul, 5, 5, nul, 4, nul, 1,
@@ -117,7 +117,7 @@ def test_multi_decode_validation(lib):
     assert call(p) == B.PKV_ERR_INVALID                 # null pointers
     assert call(_p(non_causal=1)) == B.PKV_ERR_UNSUPPORTED
     fp8 = _p(kv_cache_dtype=B.PKV_CACHE_FP8_E4M3, k_scale=0.1, v_scale=0.1)
-    assert call(fp8) == B.PKV_ERR_UNSUPPORTED
+    assert call(fp8) == B.PKV_ERR_INVALID               # supported: null pointers
     assert call(_p(num_heads=24, num_kv_heads=8)) == B.PKV_ERR_INVALID   # any group size
     assert B.paged_attn_decode_multi_workspace_size(4, 4, 64, p) == 0   # one split
     n = B.paged_attn_decode_multi_workspace_size(128, 4, 4096, p)

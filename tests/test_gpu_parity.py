@@ -88,6 +88,10 @@ DECODE_CASES = {
     "one_token_seqs": lambda: small(30, seq_lens=[1, 1, 2, 17]),
     "long_single": lambda: small(31, H=32, KVH=8, seq_lens=[5000]),
     "window_ge_len": lambda: small(32, window=4096, seq_lens=rand_lens(10, 4, 1, 300)),
+    "qpk3": lambda: small(35, H=24, KVH=8, seq_lens=rand_lens(12, 6, 1, 700)),
+    "qpk6_fp16_d64": lambda: small(36, dtype=torch.float16, H=12, KVH=2, D=64,
+                                   seq_lens=rand_lens(13, 6, 1, 500)),
+    "qpk32_two_row_groups": lambda: small(37, H=32, KVH=1, seq_lens=rand_lens(14, 4, 1, 900)),
 }
 
 
@@ -164,6 +168,33 @@ MULTI_CASES = {
 @pytest.mark.parametrize("case", sorted(MULTI_CASES))
 def test_decode_multi_parity(case):
     w = MULTI_CASES[case]()
+    r = GpuRun(w)
+    r.write()
+    out = r.decode_multi()
+    assert_no_device_error(case)
+    ref_cache = oracle_cache_after_write(w)
+    ref = O.paged_attn_decode_multi(w.query, ref_cache, w.block_tables, w.seq_lens,
+                                    w.multi_query_len, oracle_params(w))
+    assert_close(out, ref, case)
+
+
+FP8_MULTI_CASES = {
+    "q4_qpk4": lambda: fp8(small(141, H=32, KVH=8, multi=4, seq_lens=mlens(21, 8, 4, 2500))),
+    "q1_qpk4": lambda: fp8(small(142, H=32, KVH=8, multi=1, seq_lens=mlens(22, 8, 1, 900))),
+    "q3_qpk8_d64_fp16": lambda: fp8(small(143, dtype=torch.float16, H=16, KVH=2, D=64, multi=3,
+                                          seq_lens=mlens(23, 5, 3, 700))),
+    "window_alibi_bs32": lambda: fp8(small(144, bs=32, window=90, alibi=True, multi=4,
+                                           seq_lens=mlens(24, 6, 4, 900))),
+    "huge_queries": lambda: scaled_q(fp8(small(145, multi=2, seq_lens=mlens(25, 4, 2, 300))),
+                                     3e4),
+    "tiny_queries": lambda: scaled_q(fp8(small(146, multi=2, seq_lens=mlens(26, 4, 2, 300))),
+                                     1e-6),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FP8_MULTI_CASES))
+def test_decode_multi_fp8_parity(case):
+    w = FP8_MULTI_CASES[case]()
     r = GpuRun(w)
     r.write()
     out = r.decode_multi()
