@@ -36,6 +36,12 @@ if HERE not in sys.path:
 from paged_kv_cache_246_gb300 import workloads as W  # noqa: E402
 
 METRIC = ("decode tokens/s and HBM GB/s (%peak); prefill TFLOP/s (%bf16 peak), 1×GB300")
+# committed ncu summary (kernel source, file) per workload: DRAM traffic per launch
+PROFILE_OF = {2: ("decode.cu", "decode_kernel_llama3_8b_decode.md"),
+              3: ("prefill.cu", "prefill_tc_kernel_varlen_prefill.md"),
+              7: ("decode.cu", "decode_kernel_llama3_8b_decode_fp8.md"),
+              8: ("prefill.cu", "prefill_tc_kernel_varlen_prefill_fp8.md"),
+              9: ("decode.cu", "decode_kernel_llama3_8b_spec_decode.md")}
 CFG_OF = {"decode": 2, "prefill": 3, "mixed": 4, "swa": 5, "encoder": 6, "decode_fp8": 7,
           "prefill_fp8": 8, "spec_decode": 9}
 
@@ -466,9 +472,8 @@ def run_ours(args, world, rank, local):
         achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm,
-                "traffic": profiled_traffic("decode.cu",
-                                            "decode_split_kernel_llama3_8b_decode.md")
-                if cfg == 2 and args.scale_down == 1 else None,
+                "traffic": profiled_traffic(*PROFILE_OF[cfg])
+                if cfg in PROFILE_OF and args.scale_down == 1 else None,
                 "kernel": ("paged_attn_decode_multi (tensor-core split pass + combine)"
                            if w.multi_query_len else
                            "paged_attn_decode (split-KV pass + combine)"),
@@ -481,9 +486,8 @@ def run_ours(args, world, rank, local):
         achieved = flops / (pre_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_burst, "unit": "TFLOP/s",
                 "frac": achieved / bf16_burst,
-                "traffic": profiled_traffic("prefill.cu",
-                                            "prefill_tc_kernel_varlen_prefill.md")
-                if cfg == 3 and args.scale_down == 1 else None,
+                "traffic": profiled_traffic(*PROFILE_OF[cfg])
+                if cfg in PROFILE_OF and args.scale_down == 1 else None,
                 "kernel": "paged_attn_prefill_varlen", "peak_kind": peak_kind,
                 "algorithmic_flops_per_launch": flops, "avg_launch_ms": pre_ms,
                 "frac_of_sustained": achieved / bf16_sust}
