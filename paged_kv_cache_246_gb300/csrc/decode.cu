@@ -146,6 +146,33 @@ __device__ __forceinline__ void mma16816<FP16>(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same product when only rows 0..7 of A are used (rows 8..15 zero): the
+// lane's A registers of rows g + 8 are zero and the D elements of those rows
+// are discarded, so a caller keeps half the fragments.
+template <class T>
+__device__ __forceinline__ void mma16816_top(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
+                                             uint32_t b1);
+template <>
+__device__ __forceinline__ void mma16816_top<BF16>(float (&d)[2], uint32_t a0, uint32_t a2,
+                                                   uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "{\n\t.reg .f32 z0, z1;\n\t"
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, z0, z1}, "
+      "{%2, %4, %3, %4}, {%5, %6}, {%0, %1, %7, %7};\n\t}"
+      : "+f"(d[0]), "+f"(d[1])
+      : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+}
+template <>
+__device__ __forceinline__ void mma16816_top<FP16>(float (&d)[2], uint32_t a0, uint32_t a2,
+                                                   uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "{\n\t.reg .f32 z0, z1;\n\t"
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, z0, z1}, "
+      "{%2, %4, %3, %4}, {%5, %6}, {%0, %1, %7, %7};\n\t}"
+      : "+f"(d[0]), "+f"(d[1])
+      : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 template <int D, bool KV8 = false>
 struct Lay {
   static constexpr int BOX = kUnit * 128;  // 16 rows x 64 dims x 2 B
@@ -169,11 +196,16 @@ __device__ __forceinline__ uint32_t swz(int tok, int chunk) {
                                (((chunk & 7) ^ (tok & 7)) << 4));
 }
 
-template <class T, int D, bool KV8>
+// HALF: the CTA's rows are 8 or fewer (a single-token decode of up to 8
+// heads per KV head): rows 8..15 of the m16 tile are not kept at all.  (3
+// CTAs per SM in every variant: capping the fp8 half-tile variant at 128
+// registers for a 4th spills, and measured 28% slower.)
+template <class T, int D, bool KV8, bool HALF>
 __global__ void __launch_bounds__(kThreads, 3)
 decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   using L = Lay<D, KV8>;
   using MT = std::conditional_t<KV8, FP16, T>;  // MMA operand type (and P)
+  constexpr int NR = HALF ? 1 : 2;              // row halves a lane keeps (g, g + 8)
   constexpr int KS = D / 16;  // k-steps of q.k
   constexpr int NT = D / 8;   // n-tiles of p.V
   extern __shared__ uint8_t smem_raw[];
@@ -195,7 +227,7 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
 #pragma unroll
   for (int x = 0; x < 2; ++x) {
     R[x] = rg * kRows + g + 8 * x;
-    valid[x] = R[x] < a.rows;
+    valid[x] = R[x] < a.rows && x < NR;
     const int t = valid[x] ? R[x] / QPK : 0, h = valid[x] ? R[x] % QPK : 0;
     const int head = kvh * QPK + h;
     orow[x] = (b * q + t) * H + head;  // output row (token, head)
@@ -326,9 +358,16 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   }
 
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-  float o[NT][4];
+  float o[NT][2 * NR];
 #pragma unroll
-  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int c = 0; c < 2 * NR; ++c) o[n][c] = 0.f;
+  // keys every row of the CTA sees: no masking needed on a unit inside them
+  const int pos_min = sp.L - q;  // token 0
+  const int lo_max = a.window > 0 ? max(0, sp.L - a.window) : 0;  // last token's window start
+  const bool has_alibi = a.alibi != nullptr;
+  const float tq2 = static_cast<float>(2 * tq);
 
   // ldmatrix row addresses: lane -> (matrix mi, row rr)
   const int mi = lane >> 3, rr = lane & 7;
@@ -352,6 +391,17 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
 
     // ---- S = Q K^T: two n-tiles of 8 keys ---------------------------------
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // product of one k-step into n-tile n (the top half only, with HALF)
+    auto mma_s = [&](int n, const uint32_t (&qs)[4], uint32_t b0, uint32_t b1) {
+      if constexpr (HALF) {
+        float d2[2] = {sc[n][0], sc[n][1]};
+        mma16816_top<MT>(d2, qs[0], qs[2], b0, b1);
+        sc[n][0] = d2[0];
+        sc[n][1] = d2[1];
+      } else {
+        mma16816<MT>(sc[n], qs, b0, b1);
+      }
+    };
     if constexpr (KV8) {
       // keys g and g + 8: this lane's D/4 codes of each, widened per k-step
       const uint8_t *kc = wt + st * L::STAGE;
@@ -366,7 +416,7 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
           const uint2 kb = e4m3x4_to_h4(word_of(kk[n][s / 4], s % 4));
-          mma16816<MT>(sc[n], qa[s], kb.x, kb.y);
+          mma_s(n, qa[s], kb.x, kb.y);
         }
       // this unit's V codes -> the warp's swizzled fp16 tile: lane (token
       // vt_, half vh) widens D/2 codes, 16 at a time, reads rotated by token
@@ -390,29 +440,38 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
       for (int s = 0; s < KS; ++s) {
         uint32_t kb[4];
         ldsm_x4(kt + swz(k_tok, 2 * s + k_half), kb);
-        mma16816<T>(sc[0], qa[s], kb[0], kb[1]);
-        mma16816<T>(sc[1], qa[s], kb[2], kb[3]);
+        mma_s(0, qa[s], kb[0], kb[1]);
+        mma_s(1, qa[s], kb[2], kb[3]);
       }
     }
     // ---- scores in the log2 domain, per-row masks --------------------------
     // sc[n][e] : row g (e < 2) or g + 8 (e >= 2), key j0 + 8n + 2tq + (e & 1)
+    // A unit inside [lo_max, pos_min] needs no mask (rows past a.rows hold
+    // zero queries; their results are never stored).
+    const bool interior = j0 >= lo_max && j0 + kUnit - 1 <= pos_min;
     float x[2][4];  // [row][n * 2 + (e & 1)]
     bool grow = false;
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+    for (int r = 0; r < NR; ++r) {
+      const float rel = static_cast<float>(j0 - pos[r]) + tq2;  // key j0 + 2tq minus i
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = e >> 1;
-        const int j = j0 + 8 * n + 2 * tq + (e & 1);
-        float v = fmaf(sc[n][e], sl2, slope[r] * static_cast<float>(j - pos[r]));
-        if (!valid[r] || j < lo[r] || j > pos[r]) v = -INFINITY;
-        x[r][n * 2 + (e & 1)] = v;
-        grow |= v > m[r] + kLazy;
-      }
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float v = sc[n][2 * r + c] * sl2;
+          if (has_alibi) v = fmaf(slope[r], rel + static_cast<float>(8 * n + c), v);
+          if (!interior) {
+            const int j = j0 + 8 * n + 2 * tq + c;
+            if (!valid[r] || j < lo[r] || j > pos[r]) v = -INFINITY;
+          }
+          x[r][n * 2 + c] = v;
+          grow |= v > m[r] + kLazy;
+        }
+    }
     if (__any_sync(0xffffffffu, grow)) {
       // move the references to the true row maxima (4 lanes hold a row)
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
+      for (int r = 0; r < NR; ++r) {
         float mx = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -430,9 +489,9 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
       }
     }
     // ---- P (A operand of P V): rows g / g + 8, keys 2tq.. and 8 + 2tq.. -----
-    uint32_t pa[4];
+    uint32_t pa[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
+    for (int r = 0; r < NR; ++r) {
       const float mr = m[r] == -INFINITY ? 0.f : m[r];
       float p[4];
 #pragma unroll
@@ -447,8 +506,13 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
     for (int n2 = 0; n2 < NT / 2; ++n2) {
       uint32_t vb[4];
       ldsm_x4_t(vt + swz(v_tok, 2 * n2 + v_half), vb);
-      mma16816<MT>(o[2 * n2], pa, vb[0], vb[1]);
-      mma16816<MT>(o[2 * n2 + 1], pa, vb[2], vb[3]);
+      if constexpr (HALF) {
+        mma16816_top<MT>(o[2 * n2], pa[0], pa[2], vb[0], vb[1]);
+        mma16816_top<MT>(o[2 * n2 + 1], pa[0], pa[2], vb[2], vb[3]);
+      } else {
+        mma16816<MT>(o[2 * n2], pa, vb[0], vb[1]);
+        mma16816<MT>(o[2 * n2 + 1], pa, vb[2], vb[3]);
+      }
     }
     __syncwarp();  // every lane has read the stage: refill it
     if (lane == 0 && issued < my_count) {
@@ -464,7 +528,7 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
 
   // ---- merge the 4 warps' (m, l, O) ----------------------------------------
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
+  for (int r = 0; r < NR; ++r) {
     l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
     l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
   }
@@ -481,11 +545,12 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
     float *r0 = sO + (warp * kRows + g) * D + 8 * n + 2 * tq;
-    float *r1 = r0 + 8 * D;
     r0[0] = o[n][0];
     r0[1] = o[n][1];
-    r1[0] = o[n][2];
-    r1[1] = o[n][3];
+    if constexpr (!HALF) {
+      r0[8 * D] = o[n][2];
+      r0[8 * D + 1] = o[n][3];
+    }
   }
   __syncthreads();
   const bool single = sp.nsplit == 1;
@@ -553,7 +618,7 @@ static cudaError_t launch_typed(const Args &a, const CUtensorMap &tmap, int KVH,
                                 cudaStream_t stream) {
   const size_t table = ((a.split_units * 4 + 15) / 16) * 16;
   const size_t smem = 1024 + Lay<D, KV8>::TILES + table + kWarps * kStages * 8;  // + alignment
-  auto kern = decode_kernel<T, D, KV8>;
+  auto kern = a.rows <= kRows / 2 ? decode_kernel<T, D, KV8, true> : decode_kernel<T, D, KV8, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

@@ -98,13 +98,12 @@ struct Lay {
   static constexpr int NREG = D / 64;
   static constexpr int TILE = REG * NREG;
   static constexpr int TILE8 = BN * D;  // one key tile of 8-bit codes
-  // 16-bit K / V stages.  Over an fp8 cache fewer, plus N8K / N8V staging
-  // areas for the K / V tiles' codes, each refilled as soon as its codes have
-  // been widened; SPLIT: warp 2 widens every K tile and warp 3 every V tile
-  // (else both widen half the rows of each).
+  // 16-bit K / V stages.  Over an fp8 cache fewer (one K stage: a key tile
+  // is widened a full step before its QK products are issued), plus N8K /
+  // N8V staging areas for the K / V tiles' codes, each refilled as soon as
+  // its codes have been widened.
   static constexpr int NK = KV8 ? 1 : NSTK, NV = KV8 ? 2 : NSTV;
   static constexpr int N8K = 2, N8V = 2;
-  static constexpr bool SPLIT = false;
   static constexpr int OFF_Q = 0;  // two Q tiles
   static constexpr int OFF_K = 2 * TILE;
   static constexpr int OFF_V = OFF_K + NK * TILE;
@@ -246,7 +245,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       if (KV8 && (i == L::B_Q2 || i == L::B_Q2 + 1 || i == L::B_QS || i == L::B_QS + 1))
         count = 128;
       if (KV8 && ((i >= L::B_KF && i < L::B_VF + NV) || (i >= L::B_E8K && i < L::B_E8V + L::N8V)))
-        count = L::SPLIT ? 32 : 64;
+        count = 64;
       mbar_init(&bars[i], count);
     }
     misc[1] = 0;  // abort flag
@@ -444,16 +443,16 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     // ------------------------------------------------------------ fp8 widening
     const int cw = warp - 2;
     bool ok = true;
-    // Per key tile the K then the V codes are widened: with SPLIT by warp 2
-    // (K) and warp 3 (V) alone, else by both, each taking half the rows.
+    // Per key tile the K then the V codes are widened by warps 2 and 3, each
+    // taking half the rows.
     // Lane (row r0, column group cc) widens 16 codes (one 16-byte load) into
     // two 16-byte chunks of the swizzled fp16 tile; lanes of the upper column
     // half store their two chunks in the opposite order, so that the 8 lanes
     // of one row never hit the same bank group in one store.
     constexpr int LPR = D / 16, RPI = 32 / LPR;  // lanes per row, rows per pass
-    constexpr int ROWS = L::SPLIT ? BM : BM / 2;  // rows each converter warp widens
+    constexpr int ROWS = BM / 2;  // rows each converter warp widens
     const int cc = lane % LPR, r0 = lane / LPR;
-    const int row_base = L::SPLIT ? 0 : cw * (BM / 2);
+    const int row_base = cw * ROWS;
     const int swap = (cc >= LPR / 2) ? 1 : 0;
     auto widen = [&](int kv, int j) -> bool {
       const int ns = kv ? NV : NK, n8 = kv ? L::N8V : L::N8K;
@@ -500,10 +499,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       mbar_arrive(&bars[(kv ? L::B_E8V : L::B_E8K) + s8]);  // staging area free again
       return true;
     };
-    for (int j = 0; ok && j < ntiles; ++j) {
-      if constexpr (L::SPLIT) ok = widen(cw, j);
-      else ok = widen(0, j) && widen(1, j);
-    }
+    for (int j = 0; ok && j < ntiles; ++j) ok = widen(0, j) && widen(1, j);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int x = warp >= 8 ? 1 : 0;
