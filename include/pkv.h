@@ -18,9 +18,19 @@
  * - Ordering: work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  *   default stream) and the call returns without synchronising.  No call
  *   reads device memory on the host.
+ * - CUDA graphs: a call only launches kernels on `stream`, its arguments
+ *   passed by value or living in device memory, so it can be captured in a
+ *   CUDA graph and replayed on new contents of the same buffers (the
+ *   backends.utils AttentionCGSupport levels).  Make one call per
+ *   configuration on the device before capturing (the first call sets
+ *   kernel attributes and resolves a driver entry point), and capture with
+ *   the stream's device current.  kv_swap_blocks
+ *   takes its pair list by value: a captured swap replays the pairs of the
+ *   capture.
  * - Element type: fp16 or bf16 (pkv_attn_params.dtype) for queries, keys,
- *   values, outputs and the cache; arithmetic is fp32; outputs are rounded to
- *   nearest even.
+ *   values and outputs; the cache holds the same type, or 8-bit E4M3 codes
+ *   (pkv_attn_params.kv_cache_dtype); arithmetic is fp32; outputs are
+ *   rounded to nearest even.
  * - KV cache: kv_cache is [2][num_blocks][block_size * num_kv_heads *
  *   head_size] elements, contiguous (the shape of xformers.py
  *   XFormersImpl.forward and cpu_attn TorchSDPABackendImpl.forward).  Half 0

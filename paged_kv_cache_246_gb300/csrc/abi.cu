@@ -39,14 +39,21 @@ cudaError_t current_device_info(DeviceInfo *out) {
   return cudaSuccess;
 }
 
-// The library runs on the device that owns the caller's stream.
+// The library runs on the device that owns the caller's stream.  A stream
+// that is being captured into a CUDA graph is left alone: asking it for its
+// device invalidates the capture, and a capture runs with the stream's device
+// current.
 static cudaError_t select_device(cudaStream_t stream) {
   const uintptr_t s = reinterpret_cast<uintptr_t>(stream);
   if (s == 0 || s == reinterpret_cast<uintptr_t>(cudaStreamLegacy) ||
       s == reinterpret_cast<uintptr_t>(cudaStreamPerThread))
     return cudaSuccess;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs != cudaStreamCaptureStatusNone) return cudaSuccess;
   int dev = -1, cur = -1;
-  cudaError_t e = cudaStreamGetDevice(stream, &dev);
+  e = cudaStreamGetDevice(stream, &dev);
   if (e != cudaSuccess) return e;
   e = cudaGetDevice(&cur);
   if (e != cudaSuccess) return e;
