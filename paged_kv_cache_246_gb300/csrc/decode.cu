@@ -62,7 +62,13 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kUnit = 16;   // keys per unit (one TMA box height)
 constexpr int kRows = 16;   // rows per CTA: one m16 tile
-constexpr int kStages = 2;  // TMA ring depth per warp
+// TMA ring depth per warp.  (A 3-deep ring for the fp8 cache, which moves
+// half the bytes per unit, measured the same as 2: the fp8 decode is bound by
+// the per-unit instruction latency of its warps, not by bytes in flight.)
+template <bool KV8>
+struct Ring {
+  static constexpr int stages = 2;
+};
 constexpr float kLazy = 8.f;
 
 struct Args {
@@ -180,7 +186,8 @@ struct Lay {
   static constexpr int TILE = KV8 ? kUnit * D : V16;  // one unit as stored in the cache
   static constexpr int STAGE = 2 * TILE;
   // per-warp rings, then (fp8) each warp's widened V tile
-  static constexpr int TILES = kWarps * kStages * STAGE + (KV8 ? kWarps * V16 : 0);
+  static constexpr int NST = Ring<KV8>::stages;
+  static constexpr int TILES = kWarps * NST * STAGE + (KV8 ? kWarps * V16 : 0);
   static constexpr int MERGE = kWarps * kRows * (D + 2) * 4;  // reuses the tiles
   static_assert(MERGE <= TILES, "merge buffers fit in the tile area");
 };
@@ -269,17 +276,17 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
     }
     coord[k] = pb * a.BS + p0 % a.BS;
   }
-  uint64_t *wbar = bars + warp * kStages;
+  uint64_t *wbar = bars + warp * L::NST;
   if (lane == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(&wbar[st], 1);
+    for (int st = 0; st < L::NST; ++st) mbar_init(&wbar[st], 1);
     fence_mbar_init();
   }
   __syncthreads();
 
   const int my_count = nu > warp ? (nu - warp + kWarps - 1) / kWarps : 0;
-  uint8_t *wt = tiles + warp * kStages * L::STAGE;
+  uint8_t *wt = tiles + warp * L::NST * L::STAGE;
   auto issue = [&](int k) {
-    const int st = k % kStages;
+    const int st = k % L::NST;
     const int c = coord[warp + k * kWarps];
     mbar_arrive_expect_tx(&wbar[st], 2u * L::TILE);
     uint8_t *kt = wt + st * L::STAGE;
@@ -296,7 +303,7 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   };
   int issued = 0;
   if (lane == 0)
-    for (; issued < min(kStages, my_count); ++issued) issue(issued);
+    for (; issued < min(L::NST, my_count); ++issued) issue(issued);
 
   // ---- Q fragments (A operand, row-major 16 x 16 per k-step) ---------------
   uint32_t qa[KS][4];
@@ -375,11 +382,11 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   const int v_tok = (mi & 1) * 8 + rr, v_half = mi >> 1;  // V^T: token halves x dims
   bool ok = true;
   int consumed = 0;
-  uint8_t *v16 = tiles + kWarps * kStages * L::STAGE + warp * L::V16;  // fp8: widened V
+  uint8_t *v16 = tiles + kWarps * L::NST * L::STAGE + warp * L::V16;  // fp8: widened V
 
   for (int k = 0; k < my_count; ++k) {
-    const int st = k % kStages;
-    const bool got = mbar_wait_bounded(&wbar[st], (k / kStages) & 1, b);
+    const int st = k % L::NST;
+    const bool got = mbar_wait_bounded(&wbar[st], (k / L::NST) & 1, b);
     if (!__all_sync(0xffffffffu, got)) {
       ok = false;
       break;
@@ -390,16 +397,20 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
     const int j0 = (u_begin + warp + k * kWarps) * kUnit;  // position of the unit's key 0
 
     // ---- S = Q K^T: two n-tiles of 8 keys ---------------------------------
+    // Even and odd k-steps accumulate apart (summed below): four independent
+    // MMA chains of KS / 2 instead of two of KS, for the latency.
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    // product of one k-step into n-tile n (the top half only, with HALF)
-    auto mma_s = [&](int n, const uint32_t (&qs)[4], uint32_t b0, uint32_t b1) {
+    float sc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // product of k-step s into n-tile n (the top half only, with HALF)
+    auto mma_s = [&](int n, int s, const uint32_t (&qs)[4], uint32_t b0, uint32_t b1) {
+      float(&acc)[4] = (s & 1) ? sc2[n] : sc[n];
       if constexpr (HALF) {
-        float d2[2] = {sc[n][0], sc[n][1]};
+        float d2[2] = {acc[0], acc[1]};
         mma16816_top<MT>(d2, qs[0], qs[2], b0, b1);
-        sc[n][0] = d2[0];
-        sc[n][1] = d2[1];
+        acc[0] = d2[0];
+        acc[1] = d2[1];
       } else {
-        mma16816<MT>(sc[n], qs, b0, b1);
+        mma16816<MT>(acc, qs, b0, b1);
       }
     };
     if constexpr (KV8) {
@@ -416,14 +427,14 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
           const uint2 kb = e4m3x4_to_h4(word_of(kk[n][s / 4], s % 4));
-          mma_s(n, qa[s], kb.x, kb.y);
+          mma_s(n, s, qa[s], kb.x, kb.y);
         }
       // this unit's V codes -> the warp's swizzled fp16 tile: lane (token
       // vt_, half vh) widens D/2 codes, 16 at a time, reads rotated by token
       const uint8_t *vc = kc + L::TILE;
       const int vt_ = lane >> 1, vh = lane & 1;
       constexpr int NI = D / 32;  // 16-code pieces per lane
-#pragma unroll
+#pragma unroll 2  // (fully unrolled, the half-tile fp8 variant spills)
       for (int i = 0; i < NI; ++i) {
         const int ip = (i + vt_) % NI;
         const int d0 = vh * (D / 2) + 16 * ip;
@@ -440,12 +451,16 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
       for (int s = 0; s < KS; ++s) {
         uint32_t kb[4];
         ldsm_x4(kt + swz(k_tok, 2 * s + k_half), kb);
-        mma_s(0, qa[s], kb[0], kb[1]);
-        mma_s(1, qa[s], kb[2], kb[3]);
+        mma_s(0, s, qa[s], kb[0], kb[1]);
+        mma_s(1, s, qa[s], kb[2], kb[3]);
       }
     }
     // ---- scores in the log2 domain, per-row masks --------------------------
     // sc[n][e] : row g (e < 2) or g + 8 (e >= 2), key j0 + 8n + 2tq + (e & 1)
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int c = 0; c < 2 * NR; ++c) sc[n][c] += sc2[n][c];
     // A unit inside [lo_max, pos_min] needs no mask (rows past a.rows hold
     // zero queries; their results are never stored).
     const bool interior = j0 >= lo_max && j0 + kUnit - 1 <= pos_min;
@@ -523,7 +538,7 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   }
   issued = __shfl_sync(0xffffffffu, issued, 0);
   if (!ok) {  // drain this warp's copies still in flight, bounded
-    for (int k = consumed; k < issued; ++k) mbar_wait_bounded(&wbar[k % kStages], (k / kStages) & 1, b);
+    for (int k = consumed; k < issued; ++k) mbar_wait_bounded(&wbar[k % L::NST], (k / L::NST) & 1, b);
   }
 
   // ---- merge the 4 warps' (m, l, O) ----------------------------------------
@@ -617,7 +632,7 @@ template <class T, int D, bool KV8>
 static cudaError_t launch_typed(const Args &a, const CUtensorMap &tmap, int KVH, int num_seqs,
                                 cudaStream_t stream) {
   const size_t table = ((a.split_units * 4 + 15) / 16) * 16;
-  const size_t smem = 1024 + Lay<D, KV8>::TILES + table + kWarps * kStages * 8;  // + alignment
+  const size_t smem = 1024 + Lay<D, KV8>::TILES + table + kWarps * Lay<D, KV8>::NST * 8;
   auto kern = a.rows <= kRows / 2 ? decode_kernel<T, D, KV8, true> : decode_kernel<T, D, KV8, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
