@@ -52,7 +52,8 @@ __all__ = [
     "paged_attn_prefill_varlen", "decode_split_partials",
     "combine_split_partials", "kv_copy_blocks", "kv_swap_blocks",
     "e4m3_decode", "e4m3_encode", "fp8_quantize", "multi_decode_position",
-    "paged_attn_decode_multi",
+    "paged_attn_decode_multi", "dcp_local_seq_len", "dcp_global_position",
+    "paged_attn_decode_dcp_partials", "combine_dcp_partials",
 ]
 
 
@@ -450,6 +451,91 @@ def combine_split_partials(parts) -> torch.Tensor:
     w = [math.exp(ms - m) * ls for _, ms, ls in parts]
     num = sum(wk * o for wk, (o, _, _) in zip(w, parts))
     return num / sum(w)
+
+
+# ---------------------------------------------------------------------------
+# f4: decode context parallelism
+# ---------------------------------------------------------------------------
+
+def dcp_local_seq_len(seq_len: int, world: int, rank: int) -> int:
+    """Tokens of a sequence of seq_len that rank ``rank`` of a decode
+    context parallel group of ``world`` ranks holds (backends.utils
+    CommonAttentionMetadata dcp_local_seq_lens).
+
+    The pages give only these local lengths; the reading taken here places
+    token j on rank j % world at local position j // world, which keeps the
+    ranks' lengths within one of each other.
+    """
+    return max(0, (seq_len - rank + world - 1) // world)
+
+
+def dcp_global_position(local_index: int, world: int, rank: int) -> int:
+    """Position in the sequence of the rank's local token local_index."""
+    return local_index * world + rank
+
+
+def paged_attn_decode_dcp_partials(query: torch.Tensor, local_cache: torch.Tensor,
+                                   local_tables: torch.Tensor, seq_lens: torch.Tensor,
+                                   query_len: int, world: int, rank: int,
+                                   p: AttnParams):
+    """One rank's share of a decode under decode context parallelism.
+
+    The query tokens (query_len per sequence, rows b * query_len + t, at
+    positions seq_len - query_len + t) attend to the keys this rank holds,
+    read through its own cache and block table (its local tokens in local
+    order); the result is the (o, m, l) of a3 over those keys: o the
+    softmax-normalised output, m the score maximum, l the sum of
+    exp(score - m).  A row with no visible key on this rank gets o = 0,
+    m = -inf, l = 0.  Returns fp64 o [rows, heads * head_size], m and l
+    [rows, heads].
+    """
+    B = seq_lens.numel()
+    H, D, qpk = p.num_heads, p.head_size, p.queries_per_kv
+    q_all = query.to(F64).view(B, query_len, H, D)
+    o = torch.zeros(B * query_len, H * D, dtype=F64)
+    m = torch.full((B * query_len, H), -math.inf, dtype=F64)
+    l = torch.zeros(B * query_len, H, dtype=F64)
+    window = _window(p, False)
+    for b in range(B):
+        L = int(seq_lens[b])
+        Lr = dcp_local_seq_len(L, world, rank)
+        if L == 0 or Lr == 0:
+            continue
+        K, V = gather_kv(local_cache, local_tables[b], Lr, p)
+        pos = torch.tensor([dcp_global_position(k, world, rank) for k in range(Lr)], dtype=F64)
+        for t in range(query_len):
+            i = multi_decode_position(L, query_len, t)
+            keep = (pos <= i) & (pos >= window_lo(i, window))
+            if not bool(keep.any()):
+                continue
+            r = b * query_len + t
+            for h in range(H):
+                g = kv_head_of(h, qpk)
+                s = p.scale * (K[keep, g] @ q_all[b, t, h])
+                sl = _slope(p, h)
+                if sl is not None:
+                    s = s + alibi_bias(sl, pos[keep], i)
+                mm = s.max()
+                e = torch.exp(s - mm)
+                o[r, h * D:(h + 1) * D] = (e / e.sum()) @ V[keep, g]
+                m[r, h] = float(mm)
+                l[r, h] = float(e.sum())
+    return o, m, l
+
+
+def combine_dcp_partials(parts, num_heads: int, head_size: int) -> torch.Tensor:
+    """Merge every rank's (o, m, l) with a3 (combine_split_partials), row by
+    row and head by head; ranks with no visible key (l = 0) drop out."""
+    o0 = parts[0][0]
+    out = torch.zeros_like(o0)
+    D = head_size
+    for r in range(o0.shape[0]):
+        for h in range(num_heads):
+            sel = [(o[r, h * D:(h + 1) * D], float(m[r, h]), float(l[r, h]))
+                   for o, m, l in parts if float(l[r, h]) > 0.0]
+            if sel:
+                out[r, h * D:(h + 1) * D] = combine_split_partials(sel)
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -44,7 +44,7 @@ import torch
 SEED_BASE = 1000
 
 __all__ = ["Workload", "build", "CONFIGS", "make_config", "alibi_slopes",
-           "cu_from_lengths", "fill_normal"]
+           "cu_from_lengths", "fill_normal", "shard_for_dcp"]
 
 
 @dataclass
@@ -105,6 +105,38 @@ class Workload:
         sl = self.seq_lens[P:]
         return (self.query[Tp:], self.block_tables[P:], sl,
                 int(sl.max()) if sl.numel() else 0)
+
+
+def shard_for_dcp(kv_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                  block_size: int, world: int):
+    """Lay a batch's cached tokens out over ``world`` decode context parallel
+    ranks: token j of a sequence goes to rank j % world at local position
+    j // world (layout only, no attention arithmetic).  Returns per rank
+    (local_cache, local_tables), each cache [2, NB_r, row * block_size] with
+    the rank's tokens in local order behind a fresh block table."""
+    bs = block_size
+    row = kv_cache.shape[2] // bs
+    B = seq_lens.numel()
+    out = []
+    for r in range(world):
+        lens = [max(0, (int(L) - r + world - 1) // world) for L in seq_lens.tolist()]
+        nblk = [(Lr + bs - 1) // bs for Lr in lens]
+        NB = max(1, sum(nblk))
+        cache = torch.zeros(2, NB, bs * row, dtype=kv_cache.dtype)
+        tables = torch.zeros(B, max(1, max(nblk) if nblk else 1), dtype=torch.int32)
+        k = 0
+        for b in range(B):
+            for lb in range(nblk[b]):
+                tables[b, lb] = k
+                k += 1
+            for jl in range(lens[b]):
+                j = jl * world + r
+                src_blk, src_off = int(block_tables[b, j // bs]), j % bs
+                dst_blk, dst_off = int(tables[b, jl // bs]), jl % bs
+                cache[:, dst_blk, dst_off * row:(dst_off + 1) * row] = \
+                    kv_cache[:, src_blk, src_off * row:(src_off + 1) * row]
+        out.append((cache, tables))
+    return out
 
 
 def cu_from_lengths(lengths: torch.Tensor) -> torch.Tensor:

@@ -539,6 +539,45 @@ def pin_multi_decode_cross_paths():
     assert torch.equal(z[:q], torch.zeros(q, 32, dtype=F64))
 
 
+def pin_dcp_local_lengths_count_the_rank_tokens():
+    """dcp_local_seq_len is the count of positions j < L with j % R == r,
+    and the local positions enumerate exactly those (brute force)."""
+    for R in (1, 2, 3, 4):
+        for L in range(0, 23):
+            total = 0
+            for r in range(R):
+                n = O.dcp_local_seq_len(L, R, r)
+                assert n == sum(1 for j in range(L) if j % R == r), (L, R, r)
+                assert [O.dcp_global_position(k, R, r) for k in range(n)] == \
+                    [j for j in range(L) if j % R == r]
+                total += n
+            assert total == L
+
+
+def pin_dcp_partials_combine_to_the_decode():
+    """Every rank's (o, m, l) over its own keys, merged by a3, gives the
+    decode over the whole sequence: single and multi-token, with window and
+    ALiBi, 2 and 3 ranks; one rank alone is the plain decode."""
+    from paged_kv_cache_246_gb300.workloads import shard_for_dcp
+    g = torch.Generator().manual_seed(41)
+    for R, q, window, slopes in ((1, 1, 0, None), (2, 1, 0, None), (3, 2, 6, [0.3, 0.1]),
+                                 (2, 3, 0, [0.25, 0.05])):
+        p = _params(H=2, KVH=1, D=8, bs=4, scale=0.4, slopes=slopes, window=window)
+        lens = [q, 5, 13, 16]
+        Ks, Vs = _rand_seqs(g, lens, 1, 8)
+        cache, tables = paged_from_contiguous(Ks, Vs, p, g)
+        sl = torch.tensor(lens, dtype=torch.int32)
+        Q = torch.randn(len(lens) * q, 16, generator=g).to(torch.bfloat16)
+        ref = O.paged_attn_decode_multi(Q, cache, tables, sl, q, p)
+        parts = []
+        for r, (lc, lt) in enumerate(shard_for_dcp(cache, tables, sl, 4, R)):
+            parts.append(O.paged_attn_decode_dcp_partials(Q, lc, lt, sl, q, R, r, p))
+        got = O.combine_dcp_partials(parts, 2, 8)
+        _close(got, ref, tol=1e-12, what=f"dcp R={R} q={q}")
+        if R == 1:
+            _close(parts[0][0], ref, tol=1e-12, what="one rank")
+
+
 def pin_empty_decode_row_is_zero():
     p = _params(H=2, KVH=1, D=4, bs=4)
     cache = torch.randn(2, 2, 16).to(torch.bfloat16)

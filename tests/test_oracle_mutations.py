@@ -79,6 +79,9 @@ MUTATIONS["noncausal_ignored"] = ("attend_rows", _attend_always_causal)
 # speculative tokens placed one position too early / counted from the front
 MUTATIONS["multi_position_off"] = ("multi_decode_position", lambda L, q, t: L - q + t - 1)
 MUTATIONS["multi_position_front"] = ("multi_decode_position", lambda L, q, t: t)
+# decode context parallelism: ranks' tokens placed contiguously, or miscounted
+MUTATIONS["dcp_position_block"] = ("dcp_global_position", lambda k, R, r: r * 5 + k)
+MUTATIONS["dcp_local_len_floor"] = ("dcp_local_seq_len", lambda L, R, r: (L - r) // R if L > r else 0)
 
 
 def _encode_truncating(x):
