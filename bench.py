@@ -43,7 +43,7 @@ PROFILE_OF = {2: ("decode.cu", "decode_kernel_llama3_8b_decode.md"),
               8: ("prefill.cu", "prefill_tc_kernel_varlen_prefill_fp8.md"),
               9: ("decode.cu", "decode_kernel_llama3_8b_spec_decode.md")}
 CFG_OF = {"decode": 2, "prefill": 3, "mixed": 4, "swa": 5, "encoder": 6, "decode_fp8": 7,
-          "prefill_fp8": 8, "spec_decode": 9}
+          "prefill_fp8": 8, "spec_decode": 9, "dcp2_share": 2}
 
 
 def peaks():
@@ -529,6 +529,100 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_dcp_share(args, world, rank, local):
+    """One rank's step of a decode spread over a 2-rank decode context
+    parallel group, on this GPU: the cache write of the new tokens the rank
+    holds, its share over its half of every sequence's tokens, and the merge
+    of the two shares.  The peer's share is computed once beforehand and
+    stands in for the all-gather, which one GPU cannot time."""
+    from paged_kv_cache_246_gb300 import binding as B
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    R, me = 2, 0
+    w = W.make_config(2, scale_down=args.scale_down)
+    st = Step(w, dev, B)
+    B.kv_cache_write(st.key, st.value, st.cache, st.slots, st.p)   # the whole cache, once
+    torch.cuda.synchronize()
+    shards = W.shard_for_dcp(st.cache.cpu(), w.block_tables, w.seq_lens, w.block_size, R)
+    caches = [c.to(dev) for c, _ in shards]
+    tables = [t.to(dev) for _, t in shards]
+    # the new token of sequence b (position L_b - 1) and its slot on its rank
+    mine = [b for b, L in enumerate(w.seq_lens.tolist()) if (L - 1) % R == me]
+    bs = w.block_size
+    slots = torch.tensor([int(shards[me][1][b, ((L - 1) // R) // bs]) * bs + ((L - 1) // R) % bs
+                          for b, L in ((b, int(w.seq_lens[b])) for b in mine)], dtype=torch.int64)
+    key_me, val_me = st.key[mine].contiguous(), st.value[mine].contiguous()
+    slots_me = slots.to(dev)
+    Bn, H, D = w.num_seqs, w.num_heads, w.head_size
+    mx = int(w.seq_lens.max())
+    ws_bytes = B.paged_attn_decode_dcp_workspace_size(Bn, 1, mx, R, st.p)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    launches = 1 + (2 if ws_bytes > 0 else 1) + 1   # write, share (+ split combine), merge
+    parts_o = torch.empty((R, Bn * H, D), dtype=torch.float32, device=dev)
+    parts_ml = torch.empty((R, Bn * H, 2), dtype=torch.float32, device=dev)
+    for k in range(R):   # the peer's share, as the all-gather would deliver it
+        B.paged_attn_decode_dcp_partial(parts_o[k], parts_ml[k], st.query, caches[k], tables[k],
+                                        st.seq_lens, 1, mx, R, k, st.p, ws)
+    out = torch.empty_like(st.query)
+    hbm, _, _, peak_kind = peaks()
+    row = w.num_kv_heads * w.head_size
+    kv_bytes = sum(((L - me + R - 1) // R) * row * 2 * 2 for L in w.seq_lens.tolist())
+    share_bytes = kv_bytes + Bn * H * D * 2 + Bn * H * (D + 2) * 4          # K/V, q in, share out
+    merge_bytes = R * Bn * H * (D + 2) * 4 + Bn * H * D * 2                  # shares in, out
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        B.kv_cache_write(key_me, val_me, caches[me], slots_me, st.p)
+        if ev is not None:
+            ev[0].record(stream)
+        B.paged_attn_decode_dcp_partial(parts_o[me], parts_ml[me], st.query, caches[me],
+                                        tables[me], st.seq_lens, 1, mx, R, me, st.p, ws)
+        if ev is not None:
+            ev[1].record(stream)
+        B.paged_attn_dcp_combine(out, parts_o, parts_ml, st.p)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    B.check_device_error("dcp warmup")
+    sampler = ClockSampler(local)
+    sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    B.check_device_error("dcp timed region")
+    ms_step = t0.elapsed_time(t1) / args.steps
+    share_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
+    merge_ms = statistics.mean(b.elapsed_time(c) for _, b, c in evs)
+    achieved = share_bytes / (share_ms * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": Bn / (ms_step * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"llama3_8b_decode as rank 0 of a 2-rank decode context "
+                                   f"parallel group: B={Bn} H={H} KVH={w.num_kv_heads} D={D} "
+                                   f"bs={bs} (peer share precomputed: the all-gather is not "
+                                   f"timed)", "seed": W.SEED_BASE + 2,
+                       "l2": f"inputs larger than L2 (KV read per step {kv_bytes / 1e9:.2f} GB)",
+                       "parallelism": "dcp2 rank share on 1 GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None,
+                         "kernel": "paged_attn_decode_dcp_partial (split pass + combine)",
+                         "peak_kind": peak_kind, "algorithmic_bytes_per_launch": share_bytes,
+                         "avg_launch_ms": share_ms},
+            "merge": {"ms": merge_ms, "gbs": merge_bytes / (merge_ms * 1e-3) / 1e9},
+            "clocks": clocks, "e2e": None, "gpu_launches": launches * args.steps,
+            "cpu_baseline": None}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -545,6 +639,8 @@ def main():
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.workload == "dcp2_share":
+        run_dcp_share(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -258,6 +258,61 @@ size_t paged_attn_decode_multi_workspace_size(int32_t num_seqs, int32_t query_le
                                               const pkv_attn_params *params);
 
 /*
+ * Decode context parallelism (backends.utils CommonAttentionMetadata
+ * dcp_local_seq_lens: the sequence lengths of the local rank in the decode
+ * context parallel world; AttentionMetadataBuilder._init_reorder_batch_threshold
+ * and use_cascade_attention take the group's size).  A group of
+ * dcp_world_size ranks shares each sequence's cached tokens: token j lives on
+ * rank j % dcp_world_size at local position j / dcp_world_size (the pages give
+ * only the local lengths; this placement keeps them within one of each other).
+ * Each rank computes its share with paged_attn_decode_dcp_partial, the ranks
+ * all-gather the shares (rank-major), and paged_attn_dcp_combine merges them
+ * into the output.
+ *
+ * paged_attn_decode_dcp_partial -- this rank's share of a (single- or
+ * multi-token) decode: for every query row (as paged_attn_decode_multi:
+ * rows b * query_len + t at positions seq_lens[b] - query_len + t) and head,
+ * attention over the keys this rank holds, as
+ *   part_o   fp32 [num_seqs * query_len * num_heads][head_size]: the
+ *            softmax-normalised output over those keys (0 if none visible)
+ *   part_ml  fp32 [num_seqs * query_len * num_heads][2]: the score maximum m
+ *            (base-2 logits: scale * log2(e) * q.k + log2(e) * ALiBi) and the
+ *            sum l of 2^(score - m); (-inf, 0) if no key is visible here.
+ *   kv_cache, num_blocks, block_tables, max_blocks_per_seq: the rank's own
+ *            pool and tables over its local positions
+ *   seq_lens      int32[num_seqs]: GLOBAL lengths (the rank derives its local
+ *                 lengths from them), max_seq_len their host bound
+ *   dcp_world_size 1 .. 1024, dcp_rank 0 .. dcp_world_size - 1
+ *   workspace     >= paged_attn_decode_dcp_workspace_size(...) bytes
+ * Other arguments and errors as paged_attn_decode_multi.
+ */
+pkv_status paged_attn_decode_dcp_partial(float *part_o, float *part_ml, const void *query,
+                                         int32_t num_seqs, int32_t query_len,
+                                         const void *kv_cache, int64_t num_blocks,
+                                         const int32_t *block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                         int32_t max_seq_len, int32_t dcp_world_size,
+                                         int32_t dcp_rank, const pkv_attn_params *params,
+                                         void *workspace, size_t workspace_bytes,
+                                         pkv_stream_t stream);
+
+size_t paged_attn_decode_dcp_workspace_size(int32_t num_seqs, int32_t query_len,
+                                            int32_t max_seq_len, int32_t dcp_world_size,
+                                            const pkv_attn_params *params);
+
+/*
+ * paged_attn_dcp_combine -- merge num_parts shares (the split combine, a3,
+ * across ranks): out [num_rows][num_heads * head_size] elements from
+ * part_o fp32 [num_parts][num_rows * num_heads][head_size] and part_ml fp32
+ * [num_parts][num_rows * num_heads][2], rank-major as an all-gather of the
+ * ranks' paged_attn_decode_dcp_partial outputs lays them out.  Shares with
+ * l = 0 drop out; a row no share sees is zero.
+ */
+pkv_status paged_attn_dcp_combine(void *out, const float *part_o, const float *part_ml,
+                                  int32_t num_parts, int64_t num_rows,
+                                  const pkv_attn_params *params, pkv_stream_t stream);
+
+/*
  * paged_attn_prefill_varlen -- packed prompts or prompt chunks attending
  * causally to their cached context plus themselves, all K/V read from the
  * paged cache (the chunk's own K/V are stored by kv_cache_write first).

@@ -25,7 +25,8 @@ _DTYPES = {torch.float16: PKV_FP16, torch.bfloat16: PKV_BF16}
 # Every function include/pkv.h declares.
 EXPORTS = ("kv_cache_write", "paged_attn_decode", "paged_attn_decode_workspace_size",
            "paged_attn_decode_noalloc", "paged_attn_decode_multi",
-           "paged_attn_decode_multi_workspace_size",
+           "paged_attn_decode_multi_workspace_size", "paged_attn_decode_dcp_partial",
+           "paged_attn_decode_dcp_workspace_size", "paged_attn_dcp_combine",
            "paged_attn_prefill_varlen", "kv_copy_blocks", "kv_swap_blocks",
            "pkv_status_string", "pkv_device_error", "pkv_abi_version")
 
@@ -67,6 +68,10 @@ def lib() -> ctypes.CDLL:
             "paged_attn_decode_multi": (i32, [vp, vp, i32, i32, vp, i64, vp, i32, vp, i32, P, vp,
                                               sz, vp]),
             "paged_attn_decode_multi_workspace_size": (sz, [i32, i32, i32, P]),
+            "paged_attn_decode_dcp_partial": (i32, [vp, vp, vp, i32, i32, vp, i64, vp, i32, vp,
+                                                    i32, i32, i32, P, vp, sz, vp]),
+            "paged_attn_decode_dcp_workspace_size": (sz, [i32, i32, i32, i32, P]),
+            "paged_attn_dcp_combine": (i32, [vp, vp, vp, i32, i64, P, vp]),
             "paged_attn_prefill_varlen": (i32, [vp, vp, i64, i32, vp, vp, i32, i32, vp, i64, vp,
                                                 i32, P, vp]),
             "kv_copy_blocks": (i32, [vp, i32, i64, vp, i64, P, vp]),
@@ -250,6 +255,63 @@ def paged_attn_decode_multi(out: torch.Tensor, query: torch.Tensor, kv_cache: to
                                          int(max_seq_len), ctypes.byref(params), ws_ptr, ws_bytes,
                                          _stream(stream)),
            "paged_attn_decode_multi")
+
+
+def paged_attn_decode_dcp_workspace_size(num_seqs: int, query_len: int, max_seq_len: int,
+                                         dcp_world_size: int, params: AttnParams) -> int:
+    return int(lib().paged_attn_decode_dcp_workspace_size(num_seqs, query_len, max_seq_len,
+                                                          dcp_world_size, ctypes.byref(params)))
+
+
+def paged_attn_decode_dcp_partial(part_o: torch.Tensor, part_ml: torch.Tensor,
+                                  query: torch.Tensor, kv_cache: torch.Tensor,
+                                  block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                                  query_len: int, max_seq_len: int, dcp_world_size: int,
+                                  dcp_rank: int, params: AttnParams,
+                                  workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """This rank's share (fp32 o [rows * heads, head_size], (m, l) [rows * heads, 2])
+    of a decode whose sequences' tokens are spread over dcp_world_size ranks;
+    seq_lens are the global lengths, kv_cache / block_tables the rank's own."""
+    for t, n in ((query, "query"), (kv_cache, "kv_cache")):
+        _need(t, n)
+    _need(part_o, "part_o", torch.float32)
+    _need(part_ml, "part_ml", torch.float32)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    nb = _cache_blocks(kv_cache, params)
+    B = seq_lens.numel()
+    rows = B * int(query_len)
+    hd = params.num_heads * params.head_size
+    if (query.numel() != rows * hd or part_o.numel() != rows * hd or
+            part_ml.numel() != rows * params.num_heads * 2 or block_tables.shape[0] != B):
+        raise ValueError("query/part_o/part_ml/block_tables sizes disagree")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need(workspace, "workspace")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(lib().paged_attn_decode_dcp_partial(
+        part_o.data_ptr(), part_ml.data_ptr(), query.data_ptr(), B, int(query_len),
+        kv_cache.data_ptr(), nb, block_tables.data_ptr(), int(block_tables.shape[1]),
+        seq_lens.data_ptr(), int(max_seq_len), int(dcp_world_size), int(dcp_rank),
+        ctypes.byref(params), ws_ptr, ws_bytes, _stream(stream)), "paged_attn_decode_dcp_partial")
+
+
+def paged_attn_dcp_combine(out: torch.Tensor, parts_o: torch.Tensor, parts_ml: torch.Tensor,
+                           params: AttnParams, stream=None) -> None:
+    """out [rows, heads * head_size] from the ranks' shares stacked rank-major:
+    parts_o [P, rows * heads, head_size], parts_ml [P, rows * heads, 2]."""
+    _need(out, "out")
+    _need(parts_o, "parts_o", torch.float32)
+    _need(parts_ml, "parts_ml", torch.float32)
+    P = int(parts_o.shape[0])
+    rh = params.num_heads
+    rows = out.numel() // (rh * params.head_size)
+    if (parts_o.numel() != P * rows * rh * params.head_size or
+            parts_ml.numel() != P * rows * rh * 2):
+        raise ValueError("parts_o/parts_ml sizes disagree with out")
+    _check(lib().paged_attn_dcp_combine(out.data_ptr(), parts_o.data_ptr(), parts_ml.data_ptr(),
+                                        P, rows, ctypes.byref(params), _stream(stream)),
+           "paged_attn_dcp_combine")
 
 
 def paged_attn_prefill_varlen(out: torch.Tensor, query: torch.Tensor, cu_seqlens_q: torch.Tensor,

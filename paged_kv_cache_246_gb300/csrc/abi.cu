@@ -288,6 +288,82 @@ pkv_status paged_attn_decode_multi(void *out, const void *query, int32_t num_seq
                                  max_blocks_per_seq, seq_lens, g, plan, workspace, s));
 }
 
+constexpr int32_t kMaxDcpWorld = 1024;
+
+size_t paged_attn_decode_dcp_workspace_size(int32_t num_seqs, int32_t query_len,
+                                            int32_t max_seq_len, int32_t dcp_world_size,
+                                            const pkv_attn_params *params) {
+  Geometry g;
+  if (make_geometry(params, 1, &g) != PKV_OK || num_seqs <= 0 || max_seq_len < 0 ||
+      !multi_args_supported(g, query_len) || dcp_world_size < 1 || dcp_world_size > kMaxDcpWorld)
+    return 0;
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) dev.sms = 152;
+  return plan_decode(num_seqs, query_len, max_seq_len, g, dev.sms, dcp_world_size)
+      .workspace_bytes;
+}
+
+pkv_status paged_attn_decode_dcp_partial(float *part_o, float *part_ml, const void *query,
+                                         int32_t num_seqs, int32_t query_len,
+                                         const void *kv_cache, int64_t num_blocks,
+                                         const int32_t *block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                         int32_t max_seq_len, int32_t dcp_world_size,
+                                         int32_t dcp_rank, const pkv_attn_params *params,
+                                         void *workspace, size_t workspace_bytes,
+                                         pkv_stream_t stream) {
+  Geometry g;
+  pkv_status st = make_geometry(params, num_blocks, &g);
+  if (st != PKV_OK) return st;
+  if (query_len < 1 || num_seqs < 0 || num_seqs > 65535 || max_seq_len < 0 ||
+      max_blocks_per_seq <= 0 || dcp_world_size < 1 || dcp_world_size > kMaxDcpWorld ||
+      dcp_rank < 0 || dcp_rank >= dcp_world_size)
+    return PKV_ERR_INVALID;
+  if (!multi_args_supported(g, query_len)) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (static_cast<int64_t>(num_seqs) * query_len > 0x7fffffffLL / g.H) return PKV_ERR_UNSUPPORTED;
+  if (!part_o || !part_ml || !query || !kv_cache || !block_tables || !seq_lens)
+    return PKV_ERR_INVALID;
+  if (!aligned(part_o, 16) || !aligned(part_ml, 8) || !aligned(query, 16) ||
+      !aligned(kv_cache, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+    return PKV_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = select_device(s);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  DeviceInfo dev;
+  e = current_device_info(&dev);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  const DecodePlan plan =
+      plan_decode(num_seqs, query_len, max_seq_len, g, dev.sms, dcp_world_size);
+  if (plan.workspace_bytes > 0 &&
+      (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16)))
+    return PKV_ERR_INVALID;
+  DcpShare share;
+  share.world = dcp_world_size;
+  share.rank = dcp_rank;
+  share.res_o = part_o;
+  share.res_ml = part_ml;
+  return from_cuda(launch_decode(nullptr, query, num_seqs, query_len, kv_cache, block_tables,
+                                 max_blocks_per_seq, seq_lens, g, plan, workspace, s, share));
+}
+
+pkv_status paged_attn_dcp_combine(void *out, const float *part_o, const float *part_ml,
+                                  int32_t num_parts, int64_t num_rows,
+                                  const pkv_attn_params *params, pkv_stream_t stream) {
+  Geometry g;
+  pkv_status st = make_geometry(params, 1, &g);
+  if (st != PKV_OK) return st;
+  if (num_parts < 1 || num_parts > kMaxDcpWorld || num_rows < 0) return PKV_ERR_INVALID;
+  if (num_rows == 0) return PKV_OK;
+  if (num_rows > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  if (!out || !part_o || !part_ml) return PKV_ERR_INVALID;
+  if (!aligned(out, 16) || !aligned(part_o, 16) || !aligned(part_ml, 8)) return PKV_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = select_device(s);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  return from_cuda(launch_dcp_combine(out, part_o, part_ml, num_parts, num_rows, g, s));
+}
+
 pkv_status paged_attn_prefill_varlen(void *out, const void *query, int64_t num_query_tokens,
                                      int32_t num_seqs,
                                      const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,

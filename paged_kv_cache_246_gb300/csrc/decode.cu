@@ -85,20 +85,28 @@ struct Args {
   int BS, window, split_units, max_splits;
   float scale_log2;  // scale * log2(e) (* k_scale over an fp8 cache)
   float v_scale;     // 1, or the fp8 cache's value scale
+  // decode context parallelism: this rank holds token j of a sequence when
+  // j % dcp_world == dcp_rank, at local position j / dcp_world (1, 0: off)
+  int dcp_world, dcp_rank;
+  // partial output (a rank's share): normalised o [rows * H][D] and (m, l)
+  // [rows * H][2] in fp32 instead of `out` (null: write `out`)
+  float *res_o, *res_ml;
 };
 
 struct Span {
   int L;           // length (0: padding, or a bad length that was reported)
-  int first_unit;  // unit of the first visible key of token 0
-  int nunits;      // units up to position L - 1
+  int first_unit;  // unit (of this rank's local tokens) of the first visible key
+  int nunits;      // units up to the rank's last token (0: it holds no visible key)
   int nsplit;
 };
 
 __device__ __forceinline__ Span span_of(const Args &a, int b, bool report) {
   Span s{};
   int L = __ldg(a.seq_lens + b);
-  const int cap = a.max_blocks_per_seq * a.BS;
-  if (L < 0 || L > cap || (L > 0 && L < a.q)) {  // the decode must fit its sequence
+  const int R = a.dcp_world, r = a.dcp_rank;
+  const int cap = a.max_blocks_per_seq * a.BS;  // local tokens the table can hold
+  const int Lr = L > r ? (L - r + R - 1) / R : 0;  // this rank's tokens
+  if (L < 0 || Lr > cap || (L > 0 && L < a.q)) {  // the decode must fit its sequence
     if (report) record_error(PKV_ERR_BOUNDS, b);
     L = 0;
   }
@@ -106,8 +114,10 @@ __device__ __forceinline__ Span span_of(const Args &a, int b, bool report) {
   if (L == 0) return s;
   const int i0 = L - a.q;  // token 0: its window starts first
   const int lo = a.window > 0 ? max(0, i0 - a.window + 1) : 0;
-  s.first_unit = lo / kUnit;
-  s.nunits = (L - 1) / kUnit - s.first_unit + 1;
+  const int first = lo > r ? (lo - r + R - 1) / R : 0;  // first local token at or past lo
+  if (first >= Lr) return s;  // nothing visible on this rank: nunits = 0
+  s.first_unit = first / kUnit;
+  s.nunits = (Lr - 1) / kUnit - s.first_unit + 1;
   s.nsplit = (s.nunits + a.split_units - 1) / a.split_units;
   if (s.nsplit > a.max_splits) {  // seq_len above the host's max_seq_len
     if (report) record_error(PKV_ERR_BOUNDS, b);
@@ -243,13 +253,25 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
     slope[x] = (a.alibi && valid[x]) ? __ldg(a.alibi + head) * kLog2e : 0.f;
   }
 
-  if (sp.L == 0) {  // padding (or a reported bad length): zero rows
+  if (sp.L == 0 || sp.nunits == 0) {
+    // padding (or a reported bad length): zero rows; a rank holding no
+    // visible key: the empty partial (o = 0, m = -inf, l = 0)
     if (split == 0 && warp == 0) {
-      uint16_t *o16 = static_cast<uint16_t *>(a.out);
 #pragma unroll
       for (int x = 0; x < 2; ++x)
-        if (valid[x])
-          for (int d = tq; d < D; d += 4) o16[static_cast<int64_t>(orow[x]) * D + d] = 0;
+        if (valid[x]) {
+          const int64_t hh = orow[x];
+          if (a.res_o) {
+            for (int d = tq; d < D; d += 4) a.res_o[hh * D + d] = 0.f;
+            if (tq == 0) {
+              a.res_ml[hh * 2] = -INFINITY;
+              a.res_ml[hh * 2 + 1] = 0.f;
+            }
+          } else {
+            uint16_t *o16 = static_cast<uint16_t *>(a.out);
+            for (int d = tq; d < D; d += 4) o16[hh * D + d] = 0;
+          }
+        }
     }
     return;
   }
@@ -374,7 +396,8 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   const int pos_min = sp.L - q;  // token 0
   const int lo_max = a.window > 0 ? max(0, sp.L - a.window) : 0;  // last token's window start
   const bool has_alibi = a.alibi != nullptr;
-  const float tq2 = static_cast<float>(2 * tq);
+  const int RW = a.dcp_world;  // local key k sits at position k * RW + dcp_rank
+  const float tq2 = static_cast<float>(2 * tq * RW);
 
   // ldmatrix row addresses: lane -> (matrix mi, row rr)
   const int mi = lane >> 3, rr = lane & 7;
@@ -394,7 +417,8 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
     consumed = k + 1;
     const uint32_t kt = smem_u32(wt + st * L::STAGE);
     uint32_t vt = kt + L::TILE;
-    const int j0 = (u_begin + warp + k * kWarps) * kUnit;  // position of the unit's key 0
+    // position of the unit's key 0 (its keys are R positions apart)
+    const int j0 = (u_begin + warp + k * kWarps) * kUnit * RW + a.dcp_rank;
 
     // ---- S = Q K^T: two n-tiles of 8 keys ---------------------------------
     // Even and odd k-steps accumulate apart (summed below): four independent
@@ -463,7 +487,7 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
       for (int c = 0; c < 2 * NR; ++c) sc[n][c] += sc2[n][c];
     // A unit inside [lo_max, pos_min] needs no mask (rows past a.rows hold
     // zero queries; their results are never stored).
-    const bool interior = j0 >= lo_max && j0 + kUnit - 1 <= pos_min;
+    const bool interior = j0 >= lo_max && j0 + (kUnit - 1) * RW <= pos_min;
     float x[2][4];  // [row][n * 2 + (e & 1)]
     bool grow = false;
 #pragma unroll
@@ -474,9 +498,9 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           float v = sc[n][2 * r + c] * sl2;
-          if (has_alibi) v = fmaf(slope[r], rel + static_cast<float>(8 * n + c), v);
+          if (has_alibi) v = fmaf(slope[r], rel + static_cast<float>((8 * n + c) * RW), v);
           if (!interior) {
-            const int j = j0 + 8 * n + 2 * tq + c;
+            const int j = j0 + (8 * n + 2 * tq + c) * RW;
             if (!valid[r] || j < lo[r] || j > pos[r]) v = -INFINITY;
           }
           x[r][n * 2 + c] = v;
@@ -588,7 +612,13 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
     const float val = den > 0.f ? num / den * a.v_scale : 0.f;
     const int t = Rr / QPK, h = Rr % QPK;
     const int64_t hh = static_cast<int64_t>(b * q + t) * H + kvh * QPK + h;
-    if (single) {
+    if (single && a.res_o) {  // this rank's share, whole: its (o, m, l)
+      a.res_o[hh * D + d] = val;
+      if (d == 0) {
+        a.res_ml[hh * 2] = M;
+        a.res_ml[hh * 2 + 1] = den;
+      }
+    } else if (single) {
       uint16_t *o16 = static_cast<uint16_t *>(a.out);
       o16[hh * D + d] = static_cast<uint16_t>(T::from_f2(val, 0.f) & 0xffffu);
     } else {
@@ -624,7 +654,41 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const Args a) {
     }
   }
   const float val = den > 0.f ? num / den : 0.f;
+  if (a.res_o) {  // this rank's share: its merged (o, m, l)
+    a.res_o[hh * D + d] = val;
+    if (d == 0) {
+      a.res_ml[hh * 2] = M;
+      a.res_ml[hh * 2 + 1] = den;
+    }
+    return;
+  }
   uint16_t *o16 = static_cast<uint16_t *>(a.out);
+  o16[hh * D + d] = static_cast<uint16_t>(T::from_f2(val, 0.f) & 0xffffu);
+}
+
+// Decode context parallelism: merge the ranks' (o, m, l) of each (row, head)
+// (a3 across ranks).  parts_o [P][rows * H][D], parts_ml [P][rows * H][2],
+// rank-major as an all-gather lays them out.  One CTA per (row, head).
+template <class T, int D>
+__global__ void __launch_bounds__(D)
+dcp_combine_kernel(void *out, const float *parts_o, const float *parts_ml, int num_parts,
+                   int64_t rows_heads, int H) {
+  const int64_t hh = static_cast<int64_t>(blockIdx.x) * H + blockIdx.y;
+  float M = -INFINITY;
+  for (int p = 0; p < num_parts; ++p) M = fmaxf(M, parts_ml[(p * rows_heads + hh) * 2]);
+  const int d = threadIdx.x;
+  float num = 0.f, den = 0.f;
+  if (M != -INFINITY) {
+    for (int p = 0; p < num_parts; ++p) {
+      const float l = parts_ml[(p * rows_heads + hh) * 2 + 1];
+      if (l <= 0.f) continue;  // the rank holds no visible key
+      const float w = fast_exp2(parts_ml[(p * rows_heads + hh) * 2] - M) * l;
+      num = fmaf(w, parts_o[(p * rows_heads + hh) * D + d], num);
+      den += w;
+    }
+  }
+  const float val = den > 0.f ? num / den : 0.f;
+  uint16_t *o16 = static_cast<uint16_t *>(out);
   o16[hh * D + d] = static_cast<uint16_t>(T::from_f2(val, 0.f) & 0xffffu);
 }
 
@@ -647,13 +711,14 @@ static cudaError_t launch_typed(const Args &a, const CUtensorMap &tmap, int KVH,
 
 }  // namespace dec
 
-DecodePlan plan_decode(int num_seqs, int query_len, int max_seq_len,
-                                  const Geometry &g, int sms) {
+DecodePlan plan_decode(int num_seqs, int query_len, int max_seq_len, const Geometry &g, int sms,
+                       int dcp_world) {
   DecodePlan p{};
   const int U = dec::kUnit;
-  // keys the batch's widest row set can see
+  // keys (of this rank) the batch's widest row set can see
   int eff = std::max(max_seq_len, 1);
   if (g.window > 0 && g.window + query_len - 1 < eff) eff = g.window + query_len - 1;
+  eff = (eff + dcp_world - 1) / dcp_world + (dcp_world > 1 ? 1 : 0);
   const int units = (eff + U - 1) / U + 1;  // a window start can straddle a unit
   p.row_groups = (query_len * g.QPK + dec::kRows - 1) / dec::kRows;
   const int64_t items = static_cast<int64_t>(num_seqs) * g.KVH * p.row_groups;
@@ -677,10 +742,10 @@ DecodePlan plan_decode(int num_seqs, int query_len, int max_seq_len,
 }
 
 cudaError_t launch_decode(void *out, const void *query, int num_seqs, int query_len,
-                                const void *kv_cache, const int32_t *block_tables,
-                                int max_blocks_per_seq, const int32_t *seq_lens,
-                                const Geometry &g, const DecodePlan &plan, void *workspace,
-                                cudaStream_t stream) {
+                          const void *kv_cache, const int32_t *block_tables,
+                          int max_blocks_per_seq, const int32_t *seq_lens, const Geometry &g,
+                          const DecodePlan &plan, void *workspace, cudaStream_t stream,
+                          const DcpShare &dcp) {
   CUtensorMap tmap;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.D), static_cast<cuuint64_t>(g.KVH),
                               static_cast<cuuint64_t>(g.num_blocks * g.BS), 2};
@@ -726,6 +791,10 @@ cudaError_t launch_decode(void *out, const void *query, int num_seqs, int query_
   a.max_splits = plan.max_splits;
   a.scale_log2 = g.scale * kLog2e * g.k_scale;
   a.v_scale = g.v_scale;
+  a.dcp_world = dcp.world;
+  a.dcp_rank = dcp.rank;
+  a.res_o = dcp.res_o;
+  a.res_ml = dcp.res_ml;
 #define PKV_MT(TT, DD)                                                             \
   if (g.D == DD)                                                                   \
     return g.fp8 ? dec::launch_typed<TT, DD, true>(a, tmap, g.KVH, num_seqs, stream) \
@@ -739,6 +808,25 @@ cudaError_t launch_decode(void *out, const void *query, int num_seqs, int query_
   return cudaErrorInvalidValue;
 }
 
+
+cudaError_t launch_dcp_combine(void *out, const float *parts_o, const float *parts_ml,
+                              int num_parts, int64_t num_rows, const Geometry &g,
+                              cudaStream_t stream) {
+  if (num_rows > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(num_rows), static_cast<unsigned>(g.H));
+  const int64_t rh = num_rows * g.H;
+  const bool bf = g.dtype == PKV_BF16;
+  if (g.D == 128) {
+    if (bf) dec::dcp_combine_kernel<BF16, 128><<<grid, 128, 0, stream>>>(out, parts_o, parts_ml, num_parts, rh, g.H);
+    else dec::dcp_combine_kernel<FP16, 128><<<grid, 128, 0, stream>>>(out, parts_o, parts_ml, num_parts, rh, g.H);
+  } else if (g.D == 64) {
+    if (bf) dec::dcp_combine_kernel<BF16, 64><<<grid, 64, 0, stream>>>(out, parts_o, parts_ml, num_parts, rh, g.H);
+    else dec::dcp_combine_kernel<FP16, 64><<<grid, 64, 0, stream>>>(out, parts_o, parts_ml, num_parts, rh, g.H);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
 
 // ---------------------------------------------------------------------------
 // Static decode scratch for callers that cannot allocate device memory.

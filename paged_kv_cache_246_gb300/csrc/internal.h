@@ -58,11 +58,23 @@ struct DecodePlan {
   int max_splits;   // grid extent over splits (1 = no split, no workspace)
   size_t workspace_bytes;
 };
-DecodePlan plan_decode(int num_seqs, int query_len, int max_seq_len, const Geometry &g, int sms);
+// Decode context parallelism: this rank's place in the group and, for a
+// rank's share, where its (o, m, l) go instead of the output (world 1, rank
+// 0 and null pointers: a plain decode).
+struct DcpShare {
+  int world = 1, rank = 0;
+  float *res_o = nullptr, *res_ml = nullptr;
+};
+DecodePlan plan_decode(int num_seqs, int query_len, int max_seq_len, const Geometry &g, int sms,
+                       int dcp_world = 1);
 cudaError_t launch_decode(void *out, const void *query, int num_seqs, int query_len,
                           const void *kv_cache, const int32_t *block_tables,
                           int max_blocks_per_seq, const int32_t *seq_lens, const Geometry &g,
-                          const DecodePlan &plan, void *workspace, cudaStream_t stream);
+                          const DecodePlan &plan, void *workspace, cudaStream_t stream,
+                          const DcpShare &dcp = DcpShare{});
+cudaError_t launch_dcp_combine(void *out, const float *parts_o, const float *parts_ml,
+                              int num_parts, int64_t num_rows, const Geometry &g,
+                              cudaStream_t stream);
 cudaError_t read_device_error_decode(unsigned long long *out);
 // Device address and size of the static decode scratch of the current device
 // (looked up on the first call per device).
