@@ -394,6 +394,18 @@ const char *pkv_status_string(pkv_status status);
  */
 pkv_status pkv_device_error(int64_t *detail);
 
+/*
+ * pkv_check_wait_timeout -- a diagnostic of the library's failure handling.
+ * Every wait in the kernels (on a TMA copy, an MMA, another warp) gives up
+ * after a bound of one second, records PKV_ERR_TIMEOUT in the device error
+ * word, releases what it holds and lets its CTA end, so a lost arrival
+ * surfaces as a status instead of a hang.  This call launches one CTA whose
+ * wait is on a barrier nothing will complete: about one second later the
+ * error word holds PKV_ERR_TIMEOUT with detail `tag` (read it with
+ * pkv_device_error), and the device stays usable.  No fault is involved.
+ */
+pkv_status pkv_check_wait_timeout(int64_t tag, pkv_stream_t stream);
+
 /* PKV_ABI_VERSION of the built library. */
 int32_t pkv_abi_version(void);
 

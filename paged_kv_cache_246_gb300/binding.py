@@ -28,7 +28,8 @@ EXPORTS = ("kv_cache_write", "paged_attn_decode", "paged_attn_decode_workspace_s
            "paged_attn_decode_multi_workspace_size", "paged_attn_decode_dcp_partial",
            "paged_attn_decode_dcp_workspace_size", "paged_attn_dcp_combine",
            "paged_attn_prefill_varlen", "kv_copy_blocks", "kv_swap_blocks",
-           "pkv_status_string", "pkv_device_error", "pkv_abi_version")
+           "pkv_status_string", "pkv_device_error", "pkv_abi_version",
+           "pkv_check_wait_timeout")
 
 
 class PkvError(RuntimeError):
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
             "pkv_status_string": (ctypes.c_char_p, [i32]),
             "pkv_device_error": (i32, [ctypes.POINTER(ctypes.c_int64)]),
             "pkv_abi_version": (i32, []),
+            "pkv_check_wait_timeout": (i32, [i64, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -372,6 +374,11 @@ def kv_swap_blocks(src_cache: torch.Tensor, dst_cache: torch.Tensor, pairs: torc
                                 pairs.data_ptr(), int(pairs.shape[0]), ctypes.byref(params),
                                 _stream(stream)),
            "kv_swap_blocks")
+
+
+def check_wait_timeout(tag: int, stream=None) -> None:
+    """Launch the bounded wait that nothing completes (pkv_check_wait_timeout)."""
+    _check(lib().pkv_check_wait_timeout(int(tag), _stream(stream)), "pkv_check_wait_timeout")
 
 
 def device_error() -> tuple[int, int]:

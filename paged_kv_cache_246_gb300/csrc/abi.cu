@@ -458,6 +458,12 @@ pkv_status kv_swap_blocks(const void *src_cache, int64_t src_num_blocks, void *d
       launch_kv_swap(src_dev, src_num_blocks, dst_dev, dst_num_blocks, pairs, num_pairs, g, s));
 }
 
+pkv_status pkv_check_wait_timeout(int64_t tag, pkv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (select_device(s) != cudaSuccess) return PKV_ERR_CUDA;
+  return from_cuda(launch_wait_timeout_check(tag, s));
+}
+
 pkv_status pkv_device_error(int64_t *detail) {
   constexpr int kUnits = 3;
   unsigned long long words[kUnits] = {0, 0, 0};

@@ -50,6 +50,7 @@ cudaError_t launch_kv_swap(const void *src, int64_t src_blocks, void *dst, int64
                            const int64_t *pairs_host, int64_t num_pairs, const Geometry &g,
                            cudaStream_t stream);
 cudaError_t read_device_error_kv_ops(unsigned long long *out);
+cudaError_t launch_wait_timeout_check(int64_t tag, cudaStream_t stream);
 
 // decode.cu (single- and multi-token decode)
 struct DecodePlan {

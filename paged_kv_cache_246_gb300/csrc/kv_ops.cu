@@ -217,6 +217,23 @@ cudaError_t launch_kv_swap(const void *src, int64_t src_blocks, void *dst, int64
   return cudaSuccess;
 }
 
+// A wait on an mbarrier that nothing will complete, bounded like every wait
+// of the library: it gives up after kWaitLimitNs, records PKV_ERR_TIMEOUT with
+// `tag` and returns; nothing else is in flight, so the CTA simply ends.
+__global__ void wait_timeout_check_kernel(int64_t tag) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_wait_bounded(&bar, 0, tag);
+  }
+}
+
+cudaError_t launch_wait_timeout_check(int64_t tag, cudaStream_t stream) {
+  wait_timeout_check_kernel<<<1, 32, 0, stream>>>(tag);
+  return cudaGetLastError();
+}
+
 cudaError_t read_device_error_kv_ops(unsigned long long *out) {
   return read_and_clear_unit_error(out);
 }

@@ -533,3 +533,23 @@ def test_fp8_dtype_mismatch_rejected():
     with pytest.raises(ValueError):
         r.p.kv_cache_dtype = B.PKV_CACHE_AUTO
         B.kv_cache_write(r.key, r.value, r.cache, r.slots, r.p)
+
+
+def test_a_wait_that_runs_out_reports_timeout_and_the_device_stays_usable():
+    """Failure detection without a fault: a bounded wait on a barrier nothing
+    completes gives up after its one-second bound and records
+    PKV_ERR_TIMEOUT; work launched afterwards still matches the oracle."""
+    assert B.device_error()[0] == B.PKV_OK
+    B.check_wait_timeout(4242)
+    torch.cuda.synchronize()
+    st, detail = B.device_error()
+    assert st == B.PKV_ERR_TIMEOUT and detail == 4242
+    assert B.device_error()[0] == B.PKV_OK   # reading cleared it
+    w = small(150, H=32, KVH=8, seq_lens=rand_lens(30, 6, 1, 700))
+    r = GpuRun(w)
+    r.write()
+    out = r.decode()
+    assert_no_device_error("after the timeout")
+    q, bt, sl, _ = w.decode_slices()
+    ref = O.paged_attn_decode(q, oracle_cache_after_write(w), bt, sl, oracle_params(w))
+    assert_close(out, ref, "after the timeout")
