@@ -632,38 +632,58 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   }
 }
 
-// One CTA per (decode token row, query head) of a sequence with several splits.
+// Merge of a row's split partials (a3): one warp per (decode token row,
+// query head), four heads per CTA; lane l owns dims l * D/32 ...
 template <class T, int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const Args a) {
-  const int row = blockIdx.x, h = blockIdx.y;  // row = b * q + t
-  const int b = row / a.q;
-  const Span sp = span_of(a, b, false);
-  if (sp.L == 0 || sp.nsplit <= 1) return;  // written by the split kernel
+__global__ void __launch_bounds__(128) decode_combine_kernel(const Args a) {
+  constexpr int EPL = D / 32;  // dims per lane
+  const int row = blockIdx.x;  // row = b * q + t
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 4 + warp;
+  const Span sp = span_of(a, row / a.q, false);
+  if (h >= a.H || sp.L == 0 || sp.nsplit <= 1) return;  // else written by the split kernel
   const int64_t hh = static_cast<int64_t>(row) * a.H + h;
   const float *ml = a.part_ml + hh * a.max_splits * 2;
   float M = -INFINITY;
-  for (int s = 0; s < sp.nsplit; ++s) M = fmaxf(M, ml[2 * s]);
-  const int d = threadIdx.x;
-  const float *po = a.part_o + hh * a.max_splits * D + d;
-  float num = 0.f, den = 0.f;
+  for (int s = lane; s < sp.nsplit; s += 32) M = fmaxf(M, ml[2 * s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float num[EPL], den = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) num[e] = 0.f;
   if (M != -INFINITY) {
+    const float *po = a.part_o + hh * a.max_splits * D + lane * EPL;
     for (int s = 0; s < sp.nsplit; ++s) {
       const float w = fast_exp2(ml[2 * s] - M) * ml[2 * s + 1];
-      num = fmaf(w, po[static_cast<int64_t>(s) * D], num);
+      float v[EPL];
+      if constexpr (EPL == 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(s) * D);
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(s) * D);
+        v[0] = t.x; v[1] = t.y;
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) num[e] = fmaf(w, v[e], num[e]);
       den += w;
     }
   }
-  const float val = den > 0.f ? num / den : 0.f;
+  float val[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) val[e] = den > 0.f ? num[e] / den : 0.f;
   if (a.res_o) {  // this rank's share: its merged (o, m, l)
-    a.res_o[hh * D + d] = val;
-    if (d == 0) {
+    float *ro = a.res_o + hh * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) ro[e] = val[e];
+    if (lane == 0) {
       a.res_ml[hh * 2] = M;
       a.res_ml[hh * 2 + 1] = den;
     }
     return;
   }
-  uint16_t *o16 = static_cast<uint16_t *>(a.out);
-  o16[hh * D + d] = static_cast<uint16_t>(T::from_f2(val, 0.f) & 0xffffu);
+  uint32_t *o32 = reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(a.out) + hh * D + lane * EPL);
+#pragma unroll
+  for (int e = 0; e < EPL; e += 2) o32[e / 2] = T::from_f2(val[e], val[e + 1]);
 }
 
 // Decode context parallelism: merge the ranks' (o, m, l) of each (row, head)
@@ -705,7 +725,7 @@ static cudaError_t launch_typed(const Args &a, const CUtensorMap &tmap, int KVH,
   kern<<<grid, kThreads, smem, stream>>>(a, tmap);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.max_splits <= 1) return e;
-  decode_combine_kernel<T, D><<<dim3(num_seqs * a.q, a.H), D, 0, stream>>>(a);
+  decode_combine_kernel<T, D><<<dim3(num_seqs * a.q, (a.H + 3) / 4), 128, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
