@@ -48,6 +48,14 @@
 // fp16 x 2^-e, e chosen from the row group's largest magnitude (exact
 // power-of-two scaling); 2^e and k_scale join the softmax scale, v_scale
 // multiplies the output.
+//
+// Decode context parallelism (backends.utils CommonAttentionMetadata
+// dcp_local_seq_lens): a rank of a group of R holds token j of each sequence
+// when j % R is its rank, at local position j / R.  The same kernel runs over
+// the rank's own cache and tables with local key k at position k * R + rank
+// (masks, ALiBi, the mask-free test), and writes the rank's share, its fp32
+// (o, m, l) per row and head, instead of the output; dcp_combine_kernel
+// merges the all-gathered shares.
 #include <algorithm>
 #include <mutex>
 #include <type_traits>
@@ -688,28 +696,39 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const Args a) {
 
 // Decode context parallelism: merge the ranks' (o, m, l) of each (row, head)
 // (a3 across ranks).  parts_o [P][rows * H][D], parts_ml [P][rows * H][2],
-// rank-major as an all-gather lays them out.  One CTA per (row, head).
+// rank-major as an all-gather lays them out.  One warp per (row, head), four
+// heads per CTA, lane l owning dims l * D/32 ...
 template <class T, int D>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(128)
 dcp_combine_kernel(void *out, const float *parts_o, const float *parts_ml, int num_parts,
                    int64_t rows_heads, int H) {
-  const int64_t hh = static_cast<int64_t>(blockIdx.x) * H + blockIdx.y;
+  constexpr int EPL = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 4 + warp;
+  if (h >= H) return;
+  const int64_t hh = static_cast<int64_t>(blockIdx.x) * H + h;
   float M = -INFINITY;
-  for (int p = 0; p < num_parts; ++p) M = fmaxf(M, parts_ml[(p * rows_heads + hh) * 2]);
-  const int d = threadIdx.x;
-  float num = 0.f, den = 0.f;
+  for (int p = lane; p < num_parts; p += 32) M = fmaxf(M, parts_ml[(p * rows_heads + hh) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float num[EPL], den = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) num[e] = 0.f;
   if (M != -INFINITY) {
     for (int p = 0; p < num_parts; ++p) {
       const float l = parts_ml[(p * rows_heads + hh) * 2 + 1];
       if (l <= 0.f) continue;  // the rank holds no visible key
       const float w = fast_exp2(parts_ml[(p * rows_heads + hh) * 2] - M) * l;
-      num = fmaf(w, parts_o[(p * rows_heads + hh) * D + d], num);
+      const float *po = parts_o + (p * rows_heads + hh) * D + lane * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) num[e] = fmaf(w, po[e], num[e]);
       den += w;
     }
   }
-  const float val = den > 0.f ? num / den : 0.f;
-  uint16_t *o16 = static_cast<uint16_t *>(out);
-  o16[hh * D + d] = static_cast<uint16_t>(T::from_f2(val, 0.f) & 0xffffu);
+  uint32_t *o32 = reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(out) + hh * D + lane * EPL);
+#pragma unroll
+  for (int e = 0; e < EPL; e += 2)
+    o32[e / 2] = T::from_f2(den > 0.f ? num[e] / den : 0.f, den > 0.f ? num[e + 1] / den : 0.f);
 }
 
 template <class T, int D, bool KV8>
@@ -833,15 +852,15 @@ cudaError_t launch_dcp_combine(void *out, const float *parts_o, const float *par
                               int num_parts, int64_t num_rows, const Geometry &g,
                               cudaStream_t stream) {
   if (num_rows > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(num_rows), static_cast<unsigned>(g.H));
+  const dim3 grid(static_cast<unsigned>(num_rows), static_cast<unsigned>((g.H + 3) / 4));
   const int64_t rh = num_rows * g.H;
   const bool bf = g.dtype == PKV_BF16;
   if (g.D == 128) {
     if (bf) dec::dcp_combine_kernel<BF16, 128><<<grid, 128, 0, stream>>>(out, parts_o, parts_ml, num_parts, rh, g.H);
     else dec::dcp_combine_kernel<FP16, 128><<<grid, 128, 0, stream>>>(out, parts_o, parts_ml, num_parts, rh, g.H);
   } else if (g.D == 64) {
-    if (bf) dec::dcp_combine_kernel<BF16, 64><<<grid, 64, 0, stream>>>(out, parts_o, parts_ml, num_parts, rh, g.H);
-    else dec::dcp_combine_kernel<FP16, 64><<<grid, 64, 0, stream>>>(out, parts_o, parts_ml, num_parts, rh, g.H);
+    if (bf) dec::dcp_combine_kernel<BF16, 64><<<grid, 128, 0, stream>>>(out, parts_o, parts_ml, num_parts, rh, g.H);
+    else dec::dcp_combine_kernel<FP16, 64><<<grid, 128, 0, stream>>>(out, parts_o, parts_ml, num_parts, rh, g.H);
   } else {
     return cudaErrorInvalidValue;
   }
