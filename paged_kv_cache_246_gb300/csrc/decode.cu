@@ -203,9 +203,10 @@ struct Lay {
   static constexpr int V16 = (D / 64) * BOX;  // one unit of K or V as 16-bit values
   static constexpr int TILE = KV8 ? kUnit * D : V16;  // one unit as stored in the cache
   static constexpr int STAGE = 2 * TILE;
-  // per-warp rings, then (fp8) each warp's widened V tile
+  // per-warp rings, then (fp8) each warp's widened V tile, then a zero tile
   static constexpr int NST = Ring<KV8>::stages;
-  static constexpr int TILES = kWarps * NST * STAGE + (KV8 ? kWarps * V16 : 0);
+  static constexpr int ZERO = kWarps * NST * STAGE + (KV8 ? kWarps * V16 : 0);
+  static constexpr int TILES = ZERO + V16;
   static constexpr int MERGE = kWarps * kRows * (D + 2) * 4;  // reuses the tiles
   static_assert(MERGE <= TILES, "merge buffers fit in the tile area");
 };
@@ -306,6 +307,8 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
     }
     coord[k] = pb * a.BS + p0 % a.BS;
   }
+  for (int i = threadIdx.x; i < L::V16 / 16; i += kThreads)
+    reinterpret_cast<uint4 *>(tiles + L::ZERO)[i] = make_uint4(0u, 0u, 0u, 0u);
   uint64_t *wbar = bars + warp * L::NST;
   if (lane == 0) {
     for (int st = 0; st < L::NST; ++st) mbar_init(&wbar[st], 1);
@@ -548,6 +551,12 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
       pa[2 + r] = MT::from_f2(p[2], p[3]);  // keys 8 + 2tq, 9 + 2tq
     }
     if constexpr (KV8) __syncwarp();  // the widened V tile is complete
+    // Slots past the rank's last token in its last cache block hold whatever
+    // the cache holds there, possibly non-finite: their P is exactly 0, but
+    // 0 * NaN is NaN, so the lanes whose V row (token v_tok) is such a slot
+    // read that row from the zero tile instead (fp8: instead of the widened
+    // tile).  Stale K rows need nothing: their scores are masked to -inf.
+    if (j0 + v_tok * RW >= pos_min + q) vt = smem_u32(tiles + L::ZERO);
     // ---- O += P V: n-tiles of 8 dims, two per ldmatrix ---------------------
 #pragma unroll
     for (int n2 = 0; n2 < NT / 2; ++n2) {

@@ -46,8 +46,37 @@ CASES = {
 }
 
 
+def poison_past_local_ends(shards, seq_lens, bs, R):
+    """Copies of the per-rank caches with NaN (fp8: the NaN code 0x7F) in
+    every slot past a rank's last token in its last local block."""
+    out = []
+    for r, (lc, lt) in enumerate(shards):
+        lc = lc.clone()
+        row = lc.shape[2] // bs
+        for b, L in enumerate(seq_lens.tolist()):
+            Lr = max(0, (L - r + R - 1) // R)
+            if Lr == 0 or Lr % bs == 0:
+                continue
+            seg = lc[:, int(lt[b, (Lr - 1) // bs]), (Lr % bs) * row:]
+            if lc.dtype == torch.uint8:
+                seg.fill_(0x7F)
+            else:
+                seg.fill_(float("nan"))
+        out.append((lc, lt))
+    return out
+
+
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_dcp_shares_merge_to_the_decode(case):
+    _check_dcp(case, poison=False)
+
+
+@pytest.mark.parametrize("case", ["r2_fp8", "r2_qpk4", "r3_q4_window_alibi"])
+def test_dcp_non_finite_unused_slots_do_not_leak(case):
+    _check_dcp(case, poison=True)
+
+
+def _check_dcp(case, poison):
     w, R = CASES[case]()
     if w.kv_cache_dtype == "fp8_e4m3":   # context codes as the fp8 workloads draw them
         g = torch.Generator().manual_seed(9)
@@ -66,7 +95,8 @@ def test_dcp_shares_merge_to_the_decode(case):
     mx = int(w.seq_lens.max())
     parts_o = torch.empty((R, rows * H, D), dtype=torch.float32, device=DEV)
     parts_ml = torch.empty((R, rows * H, 2), dtype=torch.float32, device=DEV)
-    for k, (lc, lt) in enumerate(shards):
+    for k, (lc, lt) in enumerate(poison_past_local_ends(shards, w.seq_lens, w.block_size, R)
+                                 if poison else shards):
         n = B.paged_attn_decode_dcp_workspace_size(w.num_seqs, q, mx, R, r.p)
         ws = torch.empty(max(n, 256), dtype=torch.uint8, device=DEV)
         B.paged_attn_decode_dcp_partial(parts_o[k], parts_ml[k], r.query, lc.to(DEV),

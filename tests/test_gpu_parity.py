@@ -553,3 +553,57 @@ def test_a_wait_that_runs_out_reports_timeout_and_the_device_stays_usable():
     q, bt, sl, _ = w.decode_slices()
     ref = O.paged_attn_decode(q, oracle_cache_after_write(w), bt, sl, oracle_params(w))
     assert_close(out, ref, "after the timeout")
+
+
+# ---------------------------------------------------------------------------
+# Non-finite values in unused slots (the tail of each sequence's last block)
+# must not reach any output: their weights are exactly 0, and 0 * NaN = NaN
+# ---------------------------------------------------------------------------
+
+def poison_stale_slots(w, cache):
+    """NaN (fp8: the NaN code 0x7F) in every slot past a sequence's end in its
+    last block, in both halves of the device cache."""
+    bs = w.block_size
+    row = w.kv_cache.shape[2] // bs
+    for b, L in enumerate(w.seq_lens.tolist()):
+        if L == 0 or L % bs == 0:
+            continue
+        pb = int(w.block_tables[b, (L - 1) // bs])
+        seg = cache[:, pb, (L % bs) * row:]
+        if cache.dtype == torch.uint8:
+            seg.fill_(0x7F)
+        else:
+            seg.fill_(float("nan"))
+
+
+STALE_CASES = {
+    "decode": lambda: small(160, H=32, KVH=8, seq_lens=[5, 17, 40, 301, 999]),
+    "decode_fp8": lambda: fp8(small(161, H=32, KVH=8, seq_lens=[5, 17, 40, 301, 999])),
+    "multi_q4": lambda: small(162, H=32, KVH=8, multi=4, seq_lens=[5, 17, 40, 301, 999]),
+    "multi_q3_fp8_bs32": lambda: fp8(small(163, bs=32, multi=3, seq_lens=[4, 33, 70, 501])),
+    "prefill": lambda: chunked(164, [0, 5, 100], [17, 60, 29]),
+    "prefill_fp8": lambda: fp8(chunked(165, [0, 5, 100], [17, 60, 29])),
+}
+
+
+@pytest.mark.parametrize("case", sorted(STALE_CASES))
+def test_non_finite_unused_slots_do_not_leak(case):
+    w = STALE_CASES[case]()
+    r = GpuRun(w)
+    r.write()
+    poison_stale_slots(w, r.cache)
+    if case.startswith("prefill"):
+        out = r.prefill()
+        q, cuq, cuk, bt, _, _ = w.prefill_slices()
+        ref = O.paged_attn_prefill_varlen(q, cuq, cuk, oracle_cache_after_write(w), bt,
+                                          oracle_params(w))
+    elif case.startswith("multi"):
+        out = r.decode_multi()
+        ref = O.paged_attn_decode_multi(w.query, oracle_cache_after_write(w), w.block_tables,
+                                        w.seq_lens, w.multi_query_len, oracle_params(w))
+    else:
+        out = r.decode()
+        q, bt, sl, _ = w.decode_slices()
+        ref = O.paged_attn_decode(q, oracle_cache_after_write(w), bt, sl, oracle_params(w))
+    assert_no_device_error(case)
+    assert_close(out, ref, case)   # includes the finiteness check
