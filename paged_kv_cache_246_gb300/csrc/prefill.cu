@@ -601,52 +601,73 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
         for (int e = 0; e < BN; ++e)
           if (kv0 + e > hi || kv0 + e < lo) raw[e] = __float_as_uint(-INFINITY);
       }
-      // 8 independent 3-input max chains, then a small tree
-      float pm[8];
+      const float unit = ALIBI ? 1.f : sl2;  // log2 units per unit of m
+      // p = 2^(x - mu) over the tile, written to TMEM as P; returns the row
+      // sum.  With ALiBi x is already scaled; without, the scale is folded
+      // into the pair FMA.
+      auto exps = [&](float mu) -> float {
+        const unsigned long long mul2 = ALIBI ? f2pack(1.f, 1.f) : f2pack(sl2, sl2);
+        const unsigned long long negmu2 = f2pack(-mu, -mu);
+        unsigned long long ps2[4] = {0ull, 0ull, 0ull, 0ull};  // packed partial sums
 #pragma unroll
-      for (int q = 0; q < 8; ++q) pm[q] = -INFINITY;
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < BN; e += 2)
-        pm[(e / 2) & 7] =
-            fmax3(pm[(e / 2) & 7], __uint_as_float(raw[e]), __uint_as_float(raw[e + 1]));
-      const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
-                             fmaxf(pm[6], pm[7]));
-      // move the max only when it grows by more than 8 (2^8 in p)
+          for (int e = 0; e < 32; e += 2) {
+            float x0, x1;
+            f2unpack(ffma2(f2pack(__uint_as_float(raw[32 * c + e]),
+                                  __uint_as_float(raw[32 * c + e + 1])),
+                           mul2, negmu2),
+                     x0, x1);
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            ps2[(e / 2) & 3] = fadd2(ps2[(e / 2) & 3], f2pack(p0, p1));
+            pk[e / 2] = OPT::from_f2(p0, p1);
+          }
+          tc5::tmem_st16(sb + 16 * c, pk);
+        }
+        float ps0, ps1;
+        f2unpack(fadd2(fadd2(ps2[0], ps2[1]), fadd2(ps2[2], ps2[3])), ps0, ps1);
+        return ps0 + ps1;
+      };
+      // The reference m moves lazily, so the tile's max only decides
+      // whether it must move: the exponents are first taken against m as it
+      // stands, and only a row whose sum is out of range (m not set yet, or a
+      // p too large for an fp16 P) sends its warp through the max and a
+      // second pass.  With ALiBi the scores climb with the key position, so
+      // m moves every few tiles and the max always comes first.
       float alpha = 1.f;
       bool resc = false;
-      const float unit = ALIBI ? 1.f : sl2;  // log2 units per unit of m
-      if (m == -INFINITY) {
-        m = mx;
-      } else if ((mx - m) * unit > 8.f) {
-        alpha = fast_exp2((m - mx) * unit);
-        m = mx;
-        resc = true;
-      }
-      const float mu = m == -INFINITY ? 0.f : m * unit;
-      // p = 2^(x - mu): with ALiBi x is already scaled; without, the scale is
-      // folded into the pair FMA
-      const unsigned long long mul2 = ALIBI ? f2pack(1.f, 1.f) : f2pack(sl2, sl2);
-      const unsigned long long negmu2 = f2pack(-mu, -mu);
-      unsigned long long ps2[4] = {0ull, 0ull, 0ull, 0ull};  // packed partial sums
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float x0, x1;
-          f2unpack(ffma2(f2pack(__uint_as_float(raw[32 * c + e]),
-                                __uint_as_float(raw[32 * c + e + 1])),
-                         mul2, negmu2),
-                   x0, x1);
-          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          ps2[(e / 2) & 3] = fadd2(ps2[(e / 2) & 3], f2pack(p0, p1));
-          pk[e / 2] = OPT::from_f2(p0, p1);
+      float ps = 0.f;
+      bool slow = ALIBI || m == -INFINITY;
+      if constexpr (!ALIBI) {
+        if (!__any_sync(0xffffffffu, slow)) {
+          ps = exps(m * unit);
+          slow = !(ps <= 32768.f);
         }
-        tc5::tmem_st16(sb + 16 * c, pk);
       }
-      float ps0, ps1;
-      f2unpack(fadd2(fadd2(ps2[0], ps2[1]), fadd2(ps2[2], ps2[3])), ps0, ps1);
-      l = l * alpha + (ps0 + ps1);
+      if (ALIBI || __any_sync(0xffffffffu, slow)) {
+        // 8 independent 3-input max chains, then a small tree
+        float pm[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pm[q] = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < BN; e += 2)
+          pm[(e / 2) & 7] =
+              fmax3(pm[(e / 2) & 7], __uint_as_float(raw[e]), __uint_as_float(raw[e + 1]));
+        const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                               fmaxf(pm[6], pm[7]));
+        // move the max when it grows by more than 8 (2^8 in p)
+        if (m == -INFINITY) {
+          m = mx;
+        } else if ((mx - m) * unit > 8.f) {
+          alpha = fast_exp2((m - mx) * unit);
+          m = mx;
+          resc = true;
+        }
+        if constexpr (!ALIBI) tc5::tmem_st_wait();  // a first pass's P is written before it is replaced
+        ps = exps(m == -INFINITY ? 0.f : m * unit);
+      }
+      l = l * alpha + ps;
       if (__any_sync(0xffffffffu, resc)) {
         // O_x holds PV of the previous key tile once it has completed
         if (!warp_wait(&bars[L::B_O + x], (k - 1) & 1, abort_flag, where)) {
