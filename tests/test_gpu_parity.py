@@ -87,6 +87,7 @@ DECODE_CASES = {
                                        seq_lens=rand_lens(9, 8, 1, 700)),
     "one_token_seqs": lambda: small(30, seq_lens=[1, 1, 2, 17]),
     "long_single": lambda: small(31, H=32, KVH=8, seq_lens=[5000]),
+    "climbing_scores": lambda: climbing(small(33, H=32, KVH=8, seq_lens=[40, 700, 2100])),
     "window_ge_len": lambda: small(32, window=4096, seq_lens=rand_lens(10, 4, 1, 300)),
     "qpk3": lambda: small(35, H=24, KVH=8, seq_lens=rand_lens(12, 6, 1, 700)),
     "qpk6_fp16_d64": lambda: small(36, dtype=torch.float16, H=12, KVH=2, D=64,
@@ -246,6 +247,24 @@ def chunked(seed, ctx, q, **kw):
     return small(seed, seq_lens=[c + n for c, n in zip(ctx, q)], query_lens=q, P=len(q), **kw)
 
 
+def climbing(w, q_gain=2.0, per_pos=1 / 40):
+    """Scores that climb with the key position: every cached context key row
+    scaled by 1 + j * per_pos (j its position), queries by q_gain.  The
+    running max then grows by far more than 2^8 in p from key tile to key
+    tile, which drives the kernels' rescaling (and, in prefill, the pass that
+    redoes a tile whose exponents were taken against a stale max)."""
+    bs = w.block_size
+    row = w.kv_cache.shape[2] // bs
+    ctx = (w.seq_lens - w.query_lens).tolist()
+    for b, c in enumerate(ctx):
+        for j in range(c):
+            blk, off = int(w.block_tables[b, j // bs]), j % bs
+            seg = w.kv_cache[0, blk, off * row:(off + 1) * row]
+            seg.copy_((seg.float() * (1 + j * per_pos)).to(seg.dtype))
+    w.query = (w.query.float() * q_gain).to(w.query.dtype)
+    return w
+
+
 PREFILL_CASES = {
     "varlen_qpk4": lambda: small(41, H=32, KVH=8, seq_lens=[1, 17, 64, 65, 130, 300],
                                  query_lens=[1, 17, 64, 65, 130, 300], P=6),
@@ -257,6 +276,9 @@ PREFILL_CASES = {
     "block32_qpk1": lambda: chunked(47, [40, 0], [90, 200], bs=32, H=4, KVH=4),
     "qpk8": lambda: chunked(48, [10, 300], [257, 3], H=16, KVH=2),
     "single_row_chunks": lambda: chunked(49, [0, 10, 99, 500], [1, 1, 1, 1]),
+    "climbing_scores": lambda: climbing(chunked(53, [0, 300, 700], [200, 129, 64])),
+    "climbing_scores_fp16_qpk8": lambda: climbing(chunked(54, [450, 30], [100, 250],
+                                                          dtype=torch.float16, H=16, KVH=2)),
     "noncausal_varlen": lambda: small(51, H=32, KVH=8, causal=False, seq_lens=[1, 17, 129, 300],
                                       query_lens=[1, 17, 129, 300], P=4),
     "noncausal_chunked_alibi": lambda: chunked(52, [0, 70, 200], [150, 33, 257], causal=False,
