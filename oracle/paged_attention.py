@@ -21,7 +21,7 @@ Sources (cited by page title and the class, function or comment on it):
   ``CommonAttentionMetadata`` (query_start_loc, seq_lens,
   num_computed_tokens).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * cache block layout: the pages print only the flat size
   ``block_size * num_kv_heads * head_size`` of one block.  Read token-major,

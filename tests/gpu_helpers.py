@@ -21,7 +21,7 @@ def oracle_params(w: W.Workload) -> O.AttnParams:
                         w.sliding_window, w.causal, w.kv_cache_dtype, w.k_scale, w.v_scale)
 
 
-class GpuRun:
+class CudaRun:
     """Device copies of a workload plus the library's params."""
 
     def __init__(self, w: W.Workload):

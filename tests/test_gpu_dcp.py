@@ -15,7 +15,7 @@ from paged_kv_cache_246_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
-    from gpu_helpers import (DEV, GpuRun, assert_close, assert_no_device_error,  # noqa: E402
+    from gpu_helpers import (DEV, CudaRun, assert_close, assert_no_device_error,  # noqa: E402
                              oracle_cache_after_write, oracle_params)
 
 
@@ -85,7 +85,7 @@ def _check_dcp(case, poison):
             w.kv_cache[half].view(-1).copy_(
                 x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8))
     q = w.multi_query_len
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()                                   # the new tokens, into the whole cache
     assert_no_device_error(case + " write")
     whole = r.cache.cpu()
@@ -120,7 +120,7 @@ def _check_dcp(case, poison):
 
 def test_dcp_decode_module_single_rank_is_plain_decode():
     w, _ = batch(207, world=1, H=32, KVH=8, lens=lens_of(7, 5, 1, 800))
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     out = torch.full_like(r.query, float("nan"))
     DCP.dcp_decode(out, r.query, r.cache, r.tables, w.seq_lens.to(DEV), 1,

@@ -12,7 +12,7 @@ from paged_kv_cache_246_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
-    from gpu_helpers import (DEV, GpuRun, assert_close, assert_no_device_error,  # noqa: E402
+    from gpu_helpers import (DEV, CudaRun, assert_close, assert_no_device_error,  # noqa: E402
                              oracle_params)
 
 
@@ -48,7 +48,7 @@ def _write_and_check(w, r):
 
 def test_llama3_8b_decode_full():
     w = W.make_config(2)
-    r = GpuRun(w)
+    r = CudaRun(w)
     ref_cache = _write_and_check(w, r)
     out = r.decode()
     assert_no_device_error("decode")
@@ -60,7 +60,7 @@ def test_llama3_8b_decode_full():
 
 def test_varlen_prefill_full():
     w = W.make_config(3)
-    r = GpuRun(w)
+    r = CudaRun(w)
     ref_cache = _write_and_check(w, r)
     out = r.prefill()
     assert_no_device_error("prefill")
@@ -72,7 +72,7 @@ def test_varlen_prefill_full():
 
 def test_encoder_varlen_prefill_full():
     w = W.make_config(6)
-    r = GpuRun(w)
+    r = CudaRun(w)
     ref_cache = _write_and_check(w, r)
     out = r.prefill()
     assert_no_device_error("encoder prefill")
@@ -84,7 +84,7 @@ def test_encoder_varlen_prefill_full():
 
 def test_llama3_8b_decode_fp8_full():
     w = W.make_config(7)
-    r = GpuRun(w)
+    r = CudaRun(w)
     ref_cache = _write_and_check(w, r)
     out = r.decode()
     assert_no_device_error("fp8 decode")
@@ -96,7 +96,7 @@ def test_llama3_8b_decode_fp8_full():
 
 def test_varlen_prefill_fp8_full():
     w = W.make_config(8)
-    r = GpuRun(w)
+    r = CudaRun(w)
     ref_cache = _write_and_check(w, r)
     out = r.prefill()
     assert_no_device_error("fp8 prefill")
@@ -108,7 +108,7 @@ def test_varlen_prefill_fp8_full():
 
 def test_llama3_8b_spec_decode_full():
     w = W.make_config(9)
-    r = GpuRun(w)
+    r = CudaRun(w)
     ref_cache = _write_and_check(w, r)
     out = r.decode_multi()
     assert_no_device_error("spec decode")
@@ -122,7 +122,7 @@ def test_llama3_8b_spec_decode_full():
 
 def test_mixed_chunked_alibi_full():
     w = W.make_config(4)
-    r = GpuRun(w)
+    r = CudaRun(w)
     ref_cache = _write_and_check(w, r)
     pre = r.prefill()
     dec = r.decode()
@@ -140,7 +140,7 @@ def test_mixed_chunked_alibi_full():
 
 def test_swa_long_decode_and_block_ops_full():
     w = W.make_config(5)
-    r = GpuRun(w)
+    r = CudaRun(w)
     ref_cache = _write_and_check(w, r)
     out = r.decode()
     assert_no_device_error("swa decode")

@@ -12,7 +12,7 @@ from paged_kv_cache_246_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
-    from gpu_helpers import DEV, GpuRun, assert_no_device_error  # noqa: E402
+    from gpu_helpers import DEV, CudaRun, assert_no_device_error  # noqa: E402
 
 
 def _mixed_and_spec():
@@ -23,7 +23,7 @@ def _mixed_and_spec():
 
 def test_captured_step_replays_exactly():
     mixed, spec = _mixed_and_spec()
-    rm, rs = GpuRun(mixed), GpuRun(spec)
+    rm, rs = CudaRun(mixed), CudaRun(spec)
     P, Tp = mixed.num_prefill_seqs, mixed.num_prefill_tokens
     q, cuq, cuk, bt, mq, mk = mixed.prefill_slices()
     cuq, cuk = cuq.to(DEV), cuk.to(DEV)

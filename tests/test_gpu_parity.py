@@ -14,7 +14,7 @@ from paged_kv_cache_246_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
-    from gpu_helpers import (DEV, GpuRun, assert_close, assert_no_device_error,  # noqa: E402
+    from gpu_helpers import (DEV, CudaRun, assert_close, assert_no_device_error,  # noqa: E402
                              oracle_cache_after_write, oracle_params)
 
 
@@ -41,7 +41,7 @@ def rand_lens(seed, n, lo, hi):
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
 def test_kv_cache_write_bit_exact(cfg):
     w = W.make_config(cfg, scale_down=1 if cfg == 1 else 16)
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     assert_no_device_error("write")
     ref = oracle_cache_after_write(w)
@@ -51,7 +51,7 @@ def test_kv_cache_write_bit_exact(cfg):
 def test_kv_cache_write_padding_slots_and_empty():
     w = small(11, seq_lens=[5, 9, 33], query_lens=[5, 9, 33], P=3)
     w.slot_mapping[::3] = -1  # padding tokens
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     B.kv_cache_write(r.key[:0], r.value[:0], r.cache, r.slots[:0], r.p)  # empty: no-op
     assert_no_device_error("write padding")
@@ -63,7 +63,7 @@ def test_kv_cache_write_repeatable():
     w = W.make_config(2, scale_down=32)
     outs = []
     for _ in range(3):
-        r = GpuRun(w)
+        r = CudaRun(w)
         r.write()
         outs.append(r.cache.cpu())
     assert all(torch.equal(outs[0].view(torch.int16), o.view(torch.int16)) for o in outs[1:])
@@ -99,7 +99,7 @@ DECODE_CASES = {
 @pytest.mark.parametrize("case", sorted(DECODE_CASES))
 def test_decode_parity(case):
     w = DECODE_CASES[case]()
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     out = r.decode()
     assert_no_device_error(case)
@@ -111,7 +111,7 @@ def test_decode_parity(case):
 
 def test_decode_zero_length_rows_are_zero():
     w = small(33, seq_lens=[3, 40, 2])
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     P = 0
     sl = w.seq_lens.clone()
@@ -130,7 +130,7 @@ def test_decode_zero_length_rows_are_zero():
 def test_decode_split_invariance():
     """A loose max_seq_len changes the split plan, not the result."""
     w = small(34, H=32, KVH=8, seq_lens=rand_lens(11, 10, 200, 2000))
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     a = r.decode()
     b = r.decode(max_seq_len=8 * int(w.seq_lens.max()))
@@ -169,7 +169,7 @@ MULTI_CASES = {
 @pytest.mark.parametrize("case", sorted(MULTI_CASES))
 def test_decode_multi_parity(case):
     w = MULTI_CASES[case]()
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     out = r.decode_multi()
     assert_no_device_error(case)
@@ -196,7 +196,7 @@ FP8_MULTI_CASES = {
 @pytest.mark.parametrize("case", sorted(FP8_MULTI_CASES))
 def test_decode_multi_fp8_parity(case):
     w = FP8_MULTI_CASES[case]()
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     out = r.decode_multi()
     assert_no_device_error(case)
@@ -208,7 +208,7 @@ def test_decode_multi_fp8_parity(case):
 
 def test_decode_multi_q1_matches_decode_and_split_invariance():
     w = small(134, H=32, KVH=8, multi=1, seq_lens=mlens(12, 10, 1, 2000))
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     a = r.decode_multi()
     b = r.decode()
@@ -220,7 +220,7 @@ def test_decode_multi_q1_matches_decode_and_split_invariance():
 
 def test_decode_multi_padding_and_short_lengths():
     w = small(135, multi=4, seq_lens=[40, 9, 70])
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     sl = w.seq_lens.clone()
     sl[1] = 0                      # padding sequence: zero rows
@@ -291,7 +291,7 @@ PREFILL_CASES = {
 @pytest.mark.parametrize("case", sorted(PREFILL_CASES))
 def test_prefill_parity(case):
     w = PREFILL_CASES[case]()
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     out = r.prefill()
     assert_no_device_error(case)
@@ -305,7 +305,7 @@ def test_prefill_last_row_equals_decode():
     """Cross-path: the last prefill row of a sequence equals its decode."""
     lens = [33, 130, 257]
     w = small(50, H=32, KVH=8, seq_lens=lens, query_lens=lens, P=3)
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     pre = r.prefill()
     last = torch.tensor([sum(lens[:k + 1]) - 1 for k in range(3)])
@@ -331,7 +331,7 @@ def test_copy_blocks_bit_exact_all_layers():
         L.view(-1).copy_(torch.randn(L.numel(), generator=g).to(L.dtype))
     pairs = torch.tensor([[3, 20], [3, 21], [7, 30], [0, 39], [12, 22]], dtype=torch.int64)
     dev_layers = [L.to(DEV) for L in layers]
-    r = GpuRun(w)
+    r = CudaRun(w)
     B.kv_copy_blocks(dev_layers, pairs.to(DEV), r.p)
     assert_no_device_error("copy")
     O.kv_copy_blocks(layers, pairs.tolist())
@@ -341,7 +341,7 @@ def test_copy_blocks_bit_exact_all_layers():
 
 def test_swap_round_trip_pinned_host():
     w = small(61, seq_lens=[300, 200], num_blocks=64)
-    r = GpuRun(w)
+    r = CudaRun(w)
     host = torch.zeros((2, 16, w.kv_cache.shape[2]), dtype=w.dtype).pin_memory()
     out_pairs = torch.tensor([[5, 0], [17, 3], [40, 15], [63, 7]], dtype=torch.int64)
     B.kv_swap_blocks(r.cache, host, out_pairs, r.p)
@@ -359,7 +359,7 @@ def test_swap_round_trip_pinned_host():
 
 def test_swap_rejects_pageable_host():
     w = small(62, seq_lens=[20], num_blocks=4)
-    r = GpuRun(w)
+    r = CudaRun(w)
     pageable = torch.zeros((2, 4, w.kv_cache.shape[2]), dtype=w.dtype)
     with pytest.raises(ValueError):
         B.kv_swap_blocks(r.cache, pageable, torch.tensor([[0, 0]]), r.p)
@@ -371,7 +371,7 @@ def test_swap_rejects_pageable_host():
 
 def test_bad_slot_is_reported_not_written():
     w = small(70, seq_lens=[8], query_lens=[8], P=1, num_blocks=2)
-    r = GpuRun(w)
+    r = CudaRun(w)
     before = r.cache.clone()
     bad = r.slots.clone()
     bad[3] = 2 * 16 + 5  # beyond num_blocks * block_size
@@ -389,13 +389,13 @@ def test_bad_slot_is_reported_not_written():
 
 def test_bad_block_table_entry_is_reported():
     w = small(71, seq_lens=[40, 40])
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.tables[1, 1] = w.num_blocks + 7
     r.decode()
     torch.cuda.synchronize()
     assert B.device_error()[0] == B.PKV_ERR_BOUNDS
     w2 = small(72, seq_lens=[40], query_lens=[40], P=1)
-    r2 = GpuRun(w2)
+    r2 = CudaRun(w2)
     r2.tables[0, 2] = -5
     r2.prefill()
     torch.cuda.synchronize()
@@ -435,7 +435,7 @@ def test_kv_cache_write_fp8_bit_exact(case):
     w = FP8_WRITE_CASES[case]()
     if case == "prefill_bf16":
         w.slot_mapping[::4] = -1
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     assert_no_device_error(case)
     ref = oracle_cache_after_write(w)
@@ -462,7 +462,7 @@ FP8_DECODE_CASES = {
 @pytest.mark.parametrize("case", sorted(FP8_DECODE_CASES))
 def test_decode_fp8_parity(case):
     w = FP8_DECODE_CASES[case]()
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     out = r.decode()
     assert_no_device_error(case)
@@ -475,7 +475,7 @@ def test_decode_fp8_parity(case):
 
 def test_fp8_copy_and_swap_move_codes():
     w = fp8(small(98, seq_lens=[300, 200], num_blocks=64))
-    r = GpuRun(w)
+    r = CudaRun(w)
     pairs = torch.tensor([[3, 20], [7, 30], [0, 63]], dtype=torch.int64)
     B.kv_copy_blocks([r.cache], pairs.to(DEV), r.p)
     ref = w.kv_cache.clone()
@@ -519,7 +519,7 @@ FP8_PREFILL_CASES = {
 @pytest.mark.parametrize("case", sorted(FP8_PREFILL_CASES))
 def test_prefill_fp8_parity(case):
     w = FP8_PREFILL_CASES[case]()
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     out = r.prefill()
     assert_no_device_error(case)
@@ -533,7 +533,7 @@ def test_prefill_fp8_parity(case):
 def test_fp8_prefill_last_row_equals_fp8_decode():
     lens = [33, 130, 257]
     w = fp8(small(111, H=32, KVH=8, seq_lens=lens, query_lens=lens, P=3))
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     pre = r.prefill()
     last = torch.tensor([sum(lens[:k + 1]) - 1 for k in range(3)]).to(DEV)
@@ -548,7 +548,7 @@ def test_fp8_prefill_last_row_equals_fp8_decode():
 
 def test_fp8_dtype_mismatch_rejected():
     w = fp8(small(99, seq_lens=[40], query_lens=[40], P=1))
-    r = GpuRun(w)
+    r = CudaRun(w)
     wide = torch.zeros(w.kv_cache.shape, dtype=w.dtype, device=DEV)
     with pytest.raises(ValueError):   # a 2-byte cache under fp8 params
         B.kv_cache_write(r.key, r.value, wide, r.slots, r.p)
@@ -568,7 +568,7 @@ def test_a_wait_that_runs_out_reports_timeout_and_the_device_stays_usable():
     assert st == B.PKV_ERR_TIMEOUT and detail == 4242
     assert B.device_error()[0] == B.PKV_OK   # reading cleared it
     w = small(150, H=32, KVH=8, seq_lens=rand_lens(30, 6, 1, 700))
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     out = r.decode()
     assert_no_device_error("after the timeout")
@@ -611,7 +611,7 @@ STALE_CASES = {
 @pytest.mark.parametrize("case", sorted(STALE_CASES))
 def test_non_finite_unused_slots_do_not_leak(case):
     w = STALE_CASES[case]()
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     poison_stale_slots(w, r.cache)
     if case.startswith("prefill"):

@@ -15,7 +15,7 @@ from paged_kv_cache_246_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
-    from gpu_helpers import DEV, GpuRun, assert_no_device_error  # noqa: E402
+    from gpu_helpers import DEV, CudaRun, assert_no_device_error  # noqa: E402
 
 MAX_ABS, MEAN_ABS = 2e-2, 2e-3
 
@@ -29,7 +29,7 @@ def _noalloc(r, out):
 @pytest.mark.parametrize("cfg,scale_down", [(2, 2), (5, 4), (1, 1)])
 def test_noalloc_matches_workspace_decode_twice(cfg, scale_down):
     w = W.make_config(cfg, scale_down=scale_down)
-    r = GpuRun(w)
+    r = CudaRun(w)
     r.write()
     ref = r.decode().double()             # existing entry point, torch workspace
     assert_no_device_error("reference decode")
@@ -53,7 +53,7 @@ def test_noalloc_matches_workspace_decode_twice(cfg, scale_down):
 
 def test_noalloc_rejects_sizes_beyond_the_scratch():
     w = W.make_config(1)
-    r = GpuRun(w)
+    r = CudaRun(w)
     big_seqs, big_len = 4096, 65536
     assert B.paged_attn_decode_workspace_size(big_seqs, big_len, r.p) > 64 << 20
     out = torch.empty(big_seqs, w.num_heads * w.head_size, dtype=w.dtype, device=DEV)
