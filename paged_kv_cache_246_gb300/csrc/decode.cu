@@ -243,6 +243,11 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   const int kvh = blockIdx.y / a.row_groups, rg = blockIdx.y % a.row_groups;
   const int b = blockIdx.z;
   const int H = a.H, q = a.q, QPK = a.QPK;
+  // launched as a dependent of the stream's previous kernel: its outputs (the
+  // cache writes, the query) are read only past this wait; the split combine
+  // may be scheduled as soon as every CTA of this grid is running
+  grid_dependency_wait();
+  grid_launch_dependents();
   const Span sp = span_of(a, b, split == 0 && blockIdx.y == 0 && threadIdx.x == 0);
 
   // this lane's two rows of the m16 tile: g and g + 8
@@ -654,6 +659,7 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
 template <class T, int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const Args a) {
   constexpr int EPL = D / 32;  // dims per lane
+  grid_dependency_wait();  // the split kernel's partials are complete and visible
   const int row = blockIdx.x;  // row = b * q + t
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 4 + warp;
@@ -749,12 +755,25 @@ static cudaError_t launch_typed(const Args &a, const CUtensorMap &tmap, int KVH,
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(a.max_splits, KVH * a.row_groups, num_seqs);
-  kern<<<grid, kThreads, smem, stream>>>(a, tmap);
-  e = cudaGetLastError();
+  // both kernels are programmatic dependents of the kernel before them in the
+  // stream (each waits for it before its first global read), so their launch
+  // overlaps the previous kernel's tail
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.max_splits, KVH * a.row_groups, num_seqs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a, tmap);
   if (e != cudaSuccess || a.max_splits <= 1) return e;
-  decode_combine_kernel<T, D><<<dim3(num_seqs * a.q, (a.H + 3) / 4), 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(num_seqs * a.q, (a.H + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<T, D>, a);
 }
 
 }  // namespace dec
