@@ -17,7 +17,10 @@
  *   call and keeps no pointer after a call returns.
  * - Ordering: work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  *   default stream) and the call returns without synchronising.  No call
- *   reads device memory on the host.
+ *   reads device memory on the host.  The decode calls launch their kernels
+ *   as programmatic dependents of the kernel before them in the stream: they
+ *   may be scheduled while it finishes, but read nothing before it has
+ *   completed, so stream order holds as for ordinary launches.
  * - CUDA graphs: a call only launches kernels on `stream`, its arguments
  *   passed by value or living in device memory, so it can be captured in a
  *   CUDA graph and replayed on new contents of the same buffers (the
