@@ -1,13 +1,27 @@
 """Benchmark of the paged-KV attention path on GB300.
 
-Default workload: the Llama-3-8B-shaped decode step (bf16, 256 sequences,
+Headline workload: the Llama-3-8B-shaped decode step (bf16, 256 sequences,
 32 query / 8 KV heads, head 128, block 16, seq_len ~ U[512, 4096], pool =
 needed blocks + 10%, tables randomly permuted).  One step = kv_cache_write of
 the 256 new tokens, then paged_attn_decode (split-KV pass + combine).
 
+Beside it the default run measures, each with its own warm-up, timed steps
+and clock record, and reports in the line's ``workloads`` object:
+  varlen_prefill       16 causal prompts, log-uniform [128, 8192]: the write
+                       of all prompt tokens, then paged_attn_prefill_varlen
+                       (TFLOP/s against the bf16 tensor peak)
+  mixed_chunked_alibi  8 ALiBi prefill chunks over cached context, then 192
+                       decodes (prefill TFLOP/s and decode GB/s)
+  swa_long_decode      64 sequences of 16k-32k tokens under a 4096-token
+                       window (decode GB/s), then kv_copy_blocks of 2048
+                       pairs (HBM) and kv_swap_blocks of 4096 blocks out to
+                       pinned host memory and back (against a same-size
+                       pinned copy)
+Every record carries the cache write on its own (microseconds and GB/s).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload decode|prefill|mixed|swa|encoder|decode_fp8|prefill_fp8|
-                              spec_decode]
+                              spec_decode|dcp2_share] [--extra auto|none|a,b,...]
 
 Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own
 replica of the workload on its own GPU (the path has no exchange step), so
@@ -156,6 +170,9 @@ class Step:
 
     def run(self, mark=False):
         B = self.B
+        if mark:
+            ew = torch.cuda.Event(enable_timing=True)
+            ew.record()
         B.kv_cache_write(self.key, self.value, self.cache, self.slots, self.p)
         if mark:
             e0 = torch.cuda.Event(enable_timing=True)
@@ -177,7 +194,7 @@ class Step:
         if mark:
             e2 = torch.cuda.Event(enable_timing=True)
             e2.record()
-            self.ev.append((e0, e1, e2))
+            self.ev.append((ew, e0, e1, e2))
 
 
 def algorithmic(w: W.Workload):
@@ -326,9 +343,31 @@ def max_over_ranks(x: float, world: int) -> float:
 # ---------------------------------------------------------------------------
 # CPU oracle timing (the reported baseline; never the target)
 # ---------------------------------------------------------------------------
-def oracle_rate(w: W.Workload, budget_s: float):
+def host_cores() -> int:
+    """Cores this process may run on (its CPU affinity)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rate(w: W.Workload, budget_s: float, threads: int | None = None):
     """Oracle throughput on a bounded sample of the workload: decode
-    sequences (tokens/s) or prefill query rows (TFLOP/s-equivalent rows/s)."""
+    sequences (tokens/s) or prefill query rows (TFLOP/s-equivalent rows/s).
+    ``threads``: torch intra-op threads for the oracle's fp64 tensor ops
+    (None keeps the current setting); restored afterwards."""
+    prev = torch.get_num_threads()
+    if threads:
+        torch.set_num_threads(threads)
+    try:
+        r = _oracle_rate(w, budget_s)
+        r["threads"] = torch.get_num_threads()
+        return r
+    finally:
+        torch.set_num_threads(prev)
+
+
+def _oracle_rate(w: W.Workload, budget_s: float):
     import oracle as O
     op = O.AttnParams(w.num_heads, w.num_kv_heads, w.head_size, w.block_size, w.scale,
                       None if w.alibi_slopes is None else w.alibi_slopes.tolist(),
@@ -377,44 +416,81 @@ def oracle_rate(w: W.Workload, budget_s: float):
                       f"rows (random), scaled to the full step", "step_s": step_s}
 
 
+def cpu_baseline(w: W.Workload, budget_s: float) -> dict:
+    """The oracle on every core of this process's affinity, then on one core
+    (each a bounded sample of the same step)."""
+    cores = host_cores()
+    full = oracle_rate(w, budget_s, threads=cores)
+    one = oracle_rate(w, budget_s, threads=1)
+    return {"value": full["value"], "unit": full["unit"], "cores": cores, "kind": "oracle",
+            "sample": full["sample"], "threads": full["threads"],
+            "value_1core": one["value"], "sample_1core": one["sample"]}
+
+
+def config_of(w: W.Workload, cfg: int, world: int) -> dict:
+    """The ``config`` object of a line: the same for both arms."""
+    dec_bytes, _ = algorithmic(w)
+    has_decode = w.num_seqs > w.num_prefill_seqs
+    return {"workload": f"{w.name}: B={w.num_seqs} H={w.num_heads} KVH={w.num_kv_heads} "
+                        f"D={w.head_size} bs={w.block_size}",
+            "seed": W.SEED_BASE + cfg, "num_blocks": w.num_blocks,
+            "l2": "inputs larger than L2 (KV read per step "
+                  f"{dec_bytes / 1e9:.2f} GB)" if has_decode else prefill_footprint(w),
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    w = W.make_config(CFG_OF[args.workload])
-    cores = torch.get_num_threads()
+    cfg = CFG_OF[args.workload]
+    w = W.make_config(cfg)
+    cores = host_cores()
     for _ in range(args.warmup):
         pass  # the oracle has no warm state
     vals = []
     sample = None
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        r = oracle_rate(w, budget_s=max(2.0, 20.0 / max(1, args.steps)))
+        r = oracle_rate(w, budget_s=max(2.0, 20.0 / max(1, args.steps)), threads=cores)
         vals.append(r["value"])
         sample = r["sample"]
         unit = r["unit"]
+        threads = r["threads"]
     elapsed = time.perf_counter() - t0
     value = statistics.median(vals)
+    one = oracle_rate(w, budget_s=5.0, threads=1)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": elapsed * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "seed": W.SEED_BASE + CFG_OF[args.workload]},
+            "config": config_of(w, cfg, world),
             "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "threads": threads,
+                             "value_1core": one["value"], "sample_1core": one["sample"]},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
+    return line
 
 
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def run_ours(args, world, rank, local):
-    from paged_kv_cache_246_gb300 import binding as B
+def write_bytes(w: W.Workload) -> int:
+    """Bytes kv_cache_write reads and writes: every new token's key and value
+    rows in (2-byte elements), the same rows out in the cache's element size."""
+    kv_el = 1 if w.kv_cache_dtype == "fp8_e4m3" else 2
+    n = int((w.slot_mapping >= 0).sum()) * w.num_kv_heads * w.head_size * 2   # K and V elements
+    return n * (2 + kv_el)
+
+
+def measure(args, cfg: int, world: int, rank: int, local: int, B, full: bool) -> dict:
+    """One workload on this GPU: W untimed warm-up steps, then K steps timed
+    with CUDA events on the launching stream between barriers (max over
+    ranks), each call of the step bracketed by its own events.  ``full``
+    adds the end-to-end run through host buffers and the oracle baseline."""
     dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    cfg = CFG_OF[args.workload]
     w = W.make_config(cfg, scale_down=args.scale_down)
     st = Step(w, dev, B)
     hbm, bf16_burst, bf16_sust, peak_kind = peaks()
@@ -424,7 +500,7 @@ def run_ours(args, world, rank, local):
     for _ in range(args.warmup):
         st.run()
     torch.cuda.synchronize()
-    B.check_device_error("warmup")
+    B.check_device_error(f"{w.name} warmup")
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
@@ -441,103 +517,156 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if sampler else None
-    ms_total = t_start.elapsed_time(t_end)
-    ms_total = max_over_ranks(ms_total, world)
-    ms_step = ms_total / args.steps
-    pre_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in st.ev)
-    dec_ms = statistics.mean(b.elapsed_time(c) for _, b, c in st.ev)
-    B.check_device_error("timed region")
+    ms_step = max_over_ranks(t_start.elapsed_time(t_end), world) / args.steps
+    write_ms = statistics.mean(a.elapsed_time(b) for a, b, _, _ in st.ev)
+    pre_ms = statistics.mean(b.elapsed_time(c) for _, b, c, _ in st.ev)
+    dec_ms = statistics.mean(c.elapsed_time(d) for _, _, c, d in st.ev)
+    B.check_device_error(f"{w.name} timed region")
 
-    # ---- end to end through host buffers ----------------------------------
-    pin = lambda t: t.cpu().pin_memory()
-    h_in = [pin(t) for t in (st.query, st.key, st.value, st.slots, st.tables, st.seq_lens)]
-    d_in = [st.query, st.key, st.value, st.slots, st.tables, st.seq_lens]
-    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h2d, d2h = step_io_bytes(st)
-    for _ in range(max(1, args.warmup)):
-        for h, d in zip(h_in, d_in):
-            d.copy_(h, non_blocking=True)
-        st.run()
-        h_out.copy_(st.out, non_blocking=True)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        for h, d in zip(h_in, d_in):
-            d.copy_(h, non_blocking=True)
-        st.run()
-        h_out.copy_(st.out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    e2e = None
+    if full:
+        pin = lambda t: t.cpu().pin_memory()
+        d_in = [st.query, st.key, st.value, st.slots, st.tables, st.seq_lens]
+        h_in = [pin(t) for t in d_in]
+        h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+        h2d, d2h = step_io_bytes(st)
+        for _ in range(max(1, args.warmup)):
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            st.run()
+            h_out.copy_(st.out, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            st.run()
+            h_out.copy_(st.out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+        e2e = {"ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    # ---- metric ------------------------------------------------------------
+    # ---- metric and per-call figures ---------------------------------------
+    traffic = (profiled_traffic(*PROFILE_OF[cfg])
+               if cfg in PROFILE_OF and args.scale_down == 1 else None)
+    decode = prefill = None
+    if st.has_decode:
+        gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+        decode = {"kernel": ("paged_attn_decode_multi (tensor-core split pass + combine)"
+                             if w.multi_query_len else
+                             "paged_attn_decode (split-KV pass + combine)"),
+                  "gbs": gbs, "frac_of_hbm": gbs / hbm, "avg_launch_ms": dec_ms,
+                  "algorithmic_bytes_per_launch": dec_bytes}
+    if st.has_prefill:
+        tf = flops / (pre_ms * 1e-3) / 1e12
+        prefill = {"kernel": "paged_attn_prefill_varlen", "tflops": tf,
+                   "frac_of_bf16_burst": tf / bf16_burst, "frac_of_bf16_sustained": tf / bf16_sust,
+                   "avg_launch_ms": pre_ms, "algorithmic_flops_per_launch": flops}
     if st.has_decode:
         units = (w.num_seqs - w.num_prefill_seqs) * max(1, w.multi_query_len) * world
-        value = units / (ms_step * 1e-3)
-        unit = "tokens/s"
-        e2e_value = units / (e2e_ms * 1e-3)
-        achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm,
-                "traffic": profiled_traffic(*PROFILE_OF[cfg])
-                if cfg in PROFILE_OF and args.scale_down == 1 else None,
-                "kernel": ("paged_attn_decode_multi (tensor-core split pass + combine)"
-                           if w.multi_query_len else
-                           "paged_attn_decode (split-KV pass + combine)"),
+        value, unit = units / (ms_step * 1e-3), "tokens/s"
+        e2e_value = units / (e2e["ms_per_step"] * 1e-3) if e2e else None
+    else:
+        value, unit = flops * world / (ms_step * 1e-3) / 1e12, "TFLOP/s"
+        e2e_value = flops * world / (e2e["ms_per_step"] * 1e-3) / 1e12 if e2e else None
+    # the roofline object describes the call that takes most of the step
+    if decode and (not prefill or dec_ms >= pre_ms):
+        roof = {"bound": "hbm", "achieved": decode["gbs"], "peak": hbm, "unit": "GB/s",
+                "frac": decode["frac_of_hbm"], "traffic": traffic, "kernel": decode["kernel"],
                 "peak_kind": peak_kind, "algorithmic_bytes_per_launch": dec_bytes,
                 "avg_launch_ms": dec_ms}
     else:
-        value = flops * world / (ms_step * 1e-3) / 1e12
-        unit = "TFLOP/s"
-        e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
-        achieved = flops / (pre_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_burst, "unit": "TFLOP/s",
-                "frac": achieved / bf16_burst,
-                "traffic": profiled_traffic(*PROFILE_OF[cfg])
-                if cfg in PROFILE_OF and args.scale_down == 1 else None,
-                "kernel": "paged_attn_prefill_varlen", "peak_kind": peak_kind,
+        roof = {"bound": "tensor", "achieved": prefill["tflops"], "peak": bf16_burst,
+                "unit": "TFLOP/s", "frac": prefill["frac_of_bf16_burst"], "traffic": traffic,
+                "kernel": prefill["kernel"], "peak_kind": peak_kind,
                 "algorithmic_flops_per_launch": flops, "avg_launch_ms": pre_ms,
-                "frac_of_sustained": achieved / bf16_sust}
-    extra = {}
-    if st.has_prefill and st.has_decode:
-        extra = {"prefill_tflops": flops / (pre_ms * 1e-3) / 1e12,
-                 "prefill_frac_of_bf16": flops / (pre_ms * 1e-3) / 1e12 / bf16_burst,
-                 "decode_gbs": dec_bytes / (dec_ms * 1e-3) / 1e9,
-                 "decode_frac_of_hbm": dec_bytes / (dec_ms * 1e-3) / 1e9 / hbm}
+                "frac_of_sustained": prefill["frac_of_bf16_sustained"]}
+    wb = write_bytes(w)
+    write = {"tokens": int(w.slot_mapping.numel()), "us": write_ms * 1e3,
+             "gbs": wb / (write_ms * 1e-3) / 1e9, "frac_of_hbm": wb / (write_ms * 1e-3) / 1e9 / hbm,
+             "algorithmic_bytes_per_launch": wb}
 
     block_moves = time_block_moves(st, w, B, args, hbm) if w.copy_pairs.numel() else None
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r = oracle_rate(w, budget_s=args.cpu_budget)
-        cpu = {"value": r["value"], "unit": r["unit"], "cores": torch.get_num_threads(),
-               "kind": "oracle", "sample": r["sample"]}
+    if full and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_budget)
 
-    if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "bf16" if w.dtype == torch.bfloat16 else "fp16", "data": "synthetic",
-                "config": {"workload": f"{w.name}: B={w.num_seqs} H={w.num_heads} "
-                                       f"KVH={w.num_kv_heads} D={w.head_size} bs={w.block_size}",
-                           "seed": W.SEED_BASE + cfg, "num_blocks": w.num_blocks,
-                           "l2": "inputs larger than L2 (KV read per step "
-                                 f"{dec_bytes / 1e9:.2f} GB)" if st.has_decode else
-                                 prefill_footprint(w),
-                           "parallelism": f"replicas x{world}"},
-                "roofline": roof, "clocks": clocks,
-                "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
-                        "d2h_bytes_per_step": d2h},
-                "gpu_launches": st.launches_per_step() * args.steps,
-                "cpu_baseline": cpu}
-        line.update(extra)
-        if block_moves:
-            line["block_moves"] = block_moves
-        print(json.dumps(line), flush=True)
+    rec = {"value": value, "unit": unit, "ms_per_step": ms_step, "steps": args.steps,
+           "warmup": args.warmup, "config": config_of(w, cfg, world), "roofline": roof,
+           "kv_cache_write": write, "clocks": clocks,
+           "gpu_launches": st.launches_per_step() * args.steps}
+    if decode:
+        rec["decode"] = decode
+    if prefill:
+        rec["prefill"] = prefill
+    if block_moves:
+        rec["block_moves"] = block_moves
+    if full:
+        rec["e2e"] = {"value": e2e_value, "unit": unit,
+                      "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                      "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]}
+        rec["cpu_baseline"] = cpu
+    rec["dtype"] = "bf16" if w.dtype == torch.bfloat16 else "fp16"
+    del st
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+# Workloads the default run measures beside the headline decode, by name in
+# the line's ``workloads`` object.
+EXTRA_OF = {"prefill": "varlen_prefill", "mixed": "mixed_chunked_alibi",
+            "swa": "swa_long_decode", "encoder": "encoder_varlen_prefill",
+            "decode_fp8": "llama3_8b_decode_fp8", "prefill_fp8": "varlen_prefill_fp8",
+            "spec_decode": "llama3_8b_spec_decode"}
+
+
+def extra_workloads(args) -> list:
+    if args.extra == "auto":
+        return (["prefill", "mixed", "swa"]
+                if args.workload == "decode" and args.scale_down == 1 else [])
+    if args.extra in ("", "none"):
+        return []
+    names = [x.strip() for x in args.extra.split(",") if x.strip()]
+    for n in names:
+        if n not in EXTRA_OF:
+            raise SystemExit(f"--extra: unknown workload {n!r} (choose from {sorted(EXTRA_OF)})")
+    return names
+
+
+def run_ours(args, world, rank, local):
+    from paged_kv_cache_246_gb300 import binding as B
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = CFG_OF[args.workload]
+    head = measure(args, cfg, world, rank, local, B, full=True)
+    subs = {}
+    for name in extra_workloads(args):
+        rec = measure(args, CFG_OF[name], world, rank, local, B, full=False)
+        rec.pop("dtype", None)
+        subs[EXTRA_OF[name]] = rec
+    if rank != 0:
+        return None
+    line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": head["dtype"], "data": "synthetic", "config": head["config"],
+            "roofline": head["roofline"], "clocks": head["clocks"], "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"], "cpu_baseline": head["cpu_baseline"],
+            "kv_cache_write": head["kv_cache_write"]}
+    for k in ("decode", "prefill", "block_moves"):
+        if k in head:
+            line[k] = head[k]
+    if subs:
+        line["workloads"] = subs
+    print(json.dumps(line), flush=True)
+    return line
 
 
 def run_dcp_share(args, world, rank, local):
@@ -641,7 +770,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(CFG_OF), default="decode")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--extra", default="auto",
+                    help="comma list of workloads measured after the headline and reported in "
+                         "its line's 'workloads' object (auto: prefill,mixed,swa beside the "
+                         "default decode; none: only the headline)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work per timing (all cores, then one core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scale-down", type=int, default=1,
                     help="divide the batch (for small profiling captures only)")

@@ -15,6 +15,13 @@
  *   into the device's address space where stated) unless marked "host".  The
  *   caller owns and allocates all buffers; the library allocates nothing per
  *   call and keeps no pointer after a call returns.
+ * - Device: the kernels run on the device that owns `stream`; a call makes
+ *   it current while it launches and restores the calling thread's previous
+ *   current device before it returns.  The legacy and per-thread default
+ *   streams belong to the current device.  While `stream` is being captured
+ *   into a CUDA graph the library cannot ask it for its device (the query
+ *   would end the capture), so it uses the current device: capture with the
+ *   stream's device current.
  * - Ordering: work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  *   default stream) and the call returns without synchronising.  No call
  *   reads device memory on the host.  The decode calls launch their kernels
@@ -200,9 +207,12 @@ pkv_status paged_attn_decode(void *out, const void *query, int32_t num_seqs,
  *   - Sizes whose workspace (paged_attn_decode_workspace_size) exceeds
  *     PKV_DECODE_STATIC_SCRATCH_BYTES return PKV_ERR_UNSUPPORTED, nothing
  *     enqueued.
+ *   - The array used is the one of the device the kernels run on (the
+ *     stream's device; while `stream` is being captured, the current device,
+ *     which must then be the stream's device, as for every call).
  *   - The first call on a device looks up the array's device address (a
- *     one-time set-up per device); make that first call before any stream
- *     capture.
+ *     one-time set-up per device, with that device current); make that
+ *     first call before any stream capture.
  *   - All calls share the one array, which keeps the last call's contents.
  *     Nothing in it needs to start at zero, but calls that overlap on the GPU
  *     (on different streams, or otherwise unordered) race on it.

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
 PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_BOUNDS, PKV_ERR_TIMEOUT = range(6)
 PKV_FP16, PKV_BF16 = 0, 1
 PKV_CACHE_AUTO, PKV_CACHE_FP8_E4M3 = 0, 1
+PKV_DECODE_STATIC_SCRATCH_BYTES = 64 << 20   # include/pkv.h: paged_attn_decode_noalloc's limit
 _DTYPES = {torch.float16: PKV_FP16, torch.bfloat16: PKV_BF16}
 
 # Every function include/pkv.h declares.

@@ -39,26 +39,51 @@ cudaError_t current_device_info(DeviceInfo *out) {
   return cudaSuccess;
 }
 
-// The library runs on the device that owns the caller's stream.  A stream
-// that is being captured into a CUDA graph is left alone: asking it for its
-// device invalidates the capture, and a capture runs with the stream's device
-// current.
-static cudaError_t select_device(cudaStream_t stream) {
-  const uintptr_t s = reinterpret_cast<uintptr_t>(stream);
-  if (s == 0 || s == reinterpret_cast<uintptr_t>(cudaStreamLegacy) ||
-      s == reinterpret_cast<uintptr_t>(cudaStreamPerThread))
+// The library runs on the device that owns the caller's stream and leaves
+// the calling thread's current device as it found it: a DeviceScope makes the
+// stream's device current for the launches of one call and restores the
+// previous device when the call returns.  The legacy and per-thread default
+// streams belong to the current device.  A stream that is being captured into
+// a CUDA graph is not asked for its device (that query ends the capture): the
+// current device is used, so captures run with the stream's device current.
+class DeviceScope {
+ public:
+  DeviceScope() = default;
+  DeviceScope(const DeviceScope &) = delete;
+  DeviceScope &operator=(const DeviceScope &) = delete;
+  ~DeviceScope() {
+    if (restore_ >= 0) (void)cudaSetDevice(restore_);
+  }
+
+  cudaError_t enter(cudaStream_t stream) {
+    cudaError_t e = cudaGetDevice(&device_);
+    if (e != cudaSuccess) return e;
+    const uintptr_t s = reinterpret_cast<uintptr_t>(stream);
+    if (s == 0 || s == reinterpret_cast<uintptr_t>(cudaStreamLegacy) ||
+        s == reinterpret_cast<uintptr_t>(cudaStreamPerThread))
+      return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return e;
+    if (cs != cudaStreamCaptureStatusNone) return cudaSuccess;
+    int dev = -1;
+    e = cudaStreamGetDevice(stream, &dev);
+    if (e != cudaSuccess) return e;
+    if (dev == device_) return cudaSuccess;
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    restore_ = device_;
+    device_ = dev;
     return cudaSuccess;
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
-  if (e != cudaSuccess) return e;
-  if (cs != cudaStreamCaptureStatusNone) return cudaSuccess;
-  int dev = -1, cur = -1;
-  e = cudaStreamGetDevice(stream, &dev);
-  if (e != cudaSuccess) return e;
-  e = cudaGetDevice(&cur);
-  if (e != cudaSuccess) return e;
-  return dev == cur ? cudaSuccess : cudaSetDevice(dev);
-}
+  }
+
+  // The device the call's kernels are launched on.
+  int device() const { return device_; }
+
+ private:
+  int device_ = -1;
+  int restore_ = -1;
+};
 
 // ---------------------------------------------------------------------------
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
@@ -172,7 +197,8 @@ pkv_status kv_cache_write(const void *key, const void *value, int64_t num_tokens
       !aligned(slot_mapping, 8))
     return PKV_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = select_device(s);
+  DeviceScope scope;
+  cudaError_t e = scope.enter(s);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return from_cuda(launch_kv_write(key, value, num_tokens, kv_cache, slot_mapping, g, s));
 }
@@ -202,7 +228,8 @@ pkv_status paged_attn_decode(void *out, const void *query, int32_t num_seqs, con
       !aligned(block_tables, 4) || !aligned(seq_lens, 4))
     return PKV_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = select_device(s);
+  DeviceScope scope;
+  cudaError_t e = scope.enter(s);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   DeviceInfo dev;
   e = current_device_info(&dev);
@@ -226,14 +253,19 @@ pkv_status paged_attn_decode_noalloc(void *out, const void *query, int32_t num_s
   if (num_seqs < 0 || num_seqs > 65535 || max_seq_len < 0 || max_blocks_per_seq <= 0)
     return PKV_ERR_INVALID;
   if (num_seqs == 0) return PKV_OK;
-  cudaError_t e = select_device(reinterpret_cast<cudaStream_t>(stream));
+  // The scratch array of the device the kernels will run on: the stream's
+  // device, current for the rest of this call (a capturing stream: the
+  // current device, which the capture must run on).
+  DeviceScope scope;
+  cudaError_t e = scope.enter(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   if (paged_attn_decode_workspace_size(num_seqs, max_seq_len, params) >
       PKV_DECODE_STATIC_SCRATCH_BYTES)
     return PKV_ERR_UNSUPPORTED;
   void *scratch = nullptr;
   size_t scratch_bytes = 0;
-  if (static_decode_scratch(&scratch, &scratch_bytes) != cudaSuccess) return PKV_ERR_CUDA;
+  if (static_decode_scratch(scope.device(), &scratch, &scratch_bytes) != cudaSuccess)
+    return PKV_ERR_CUDA;
   return paged_attn_decode(out, query, num_seqs, kv_cache, num_blocks, block_tables,
                            max_blocks_per_seq, seq_lens, max_seq_len, params, scratch,
                            scratch_bytes, stream);
@@ -275,7 +307,8 @@ pkv_status paged_attn_decode_multi(void *out, const void *query, int32_t num_seq
       !aligned(block_tables, 4) || !aligned(seq_lens, 4))
     return PKV_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = select_device(s);
+  DeviceScope scope;
+  cudaError_t e = scope.enter(s);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   DeviceInfo dev;
   e = current_device_info(&dev);
@@ -328,7 +361,8 @@ pkv_status paged_attn_decode_dcp_partial(float *part_o, float *part_ml, const vo
       !aligned(kv_cache, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
     return PKV_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = select_device(s);
+  DeviceScope scope;
+  cudaError_t e = scope.enter(s);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   DeviceInfo dev;
   e = current_device_info(&dev);
@@ -359,7 +393,8 @@ pkv_status paged_attn_dcp_combine(void *out, const float *part_o, const float *p
   if (!out || !part_o || !part_ml) return PKV_ERR_INVALID;
   if (!aligned(out, 16) || !aligned(part_o, 16) || !aligned(part_ml, 8)) return PKV_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = select_device(s);
+  DeviceScope scope;
+  cudaError_t e = scope.enter(s);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return from_cuda(launch_dcp_combine(out, part_o, part_ml, num_parts, num_rows, g, s));
 }
@@ -385,7 +420,8 @@ pkv_status paged_attn_prefill_varlen(void *out, const void *query, int64_t num_q
       !aligned(block_tables, 4) || !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
     return PKV_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = select_device(s);
+  DeviceScope scope;
+  cudaError_t e = scope.enter(s);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return from_cuda(launch_prefill(out, query, num_query_tokens, num_seqs, cu_seqlens_q,
                                   cu_seqlens_k, max_query_len, max_seq_len, kv_cache,
@@ -404,7 +440,8 @@ pkv_status kv_copy_blocks(void *const *kv_caches, int32_t num_layers, int64_t nu
   for (int l = 0; l < num_layers; ++l)
     if (!kv_caches[l] || !aligned(kv_caches[l], 16)) return PKV_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = select_device(s);
+  DeviceScope scope;
+  cudaError_t e = scope.enter(s);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   return from_cuda(launch_kv_copy(kv_caches, num_layers, pairs, num_pairs, g, s));
 }
@@ -449,7 +486,8 @@ pkv_status kv_swap_blocks(const void *src_cache, int64_t src_num_blocks, void *d
     dst_used[d] = 1;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = select_device(s);
+  DeviceScope scope;
+  cudaError_t e = scope.enter(s);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   void *src_dev = device_view(src_cache);
   void *dst_dev = device_view(dst_cache);
@@ -460,7 +498,8 @@ pkv_status kv_swap_blocks(const void *src_cache, int64_t src_num_blocks, void *d
 
 pkv_status pkv_check_wait_timeout(int64_t tag, pkv_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (select_device(s) != cudaSuccess) return PKV_ERR_CUDA;
+  DeviceScope scope;
+  if (scope.enter(s) != cudaSuccess) return PKV_ERR_CUDA;
   return from_cuda(launch_wait_timeout_check(tag, s));
 }
 

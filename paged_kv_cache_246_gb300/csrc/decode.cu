@@ -915,11 +915,12 @@ static void *g_scratch_addr[64];
 static bool g_scratch_known[64];
 static std::mutex g_scratch_mu;
 
-cudaError_t static_decode_scratch(void **ptr, size_t *bytes) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
+cudaError_t static_decode_scratch(int dev, void **ptr, size_t *bytes) {
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  // the symbol's address is looked up with its own device current
+  if (dev < 0 || dev >= 64 || dev != cur) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
   if (!g_scratch_known[dev]) {
     void *p = nullptr;

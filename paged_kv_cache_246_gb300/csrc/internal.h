@@ -77,9 +77,9 @@ cudaError_t launch_dcp_combine(void *out, const float *parts_o, const float *par
                               int num_parts, int64_t num_rows, const Geometry &g,
                               cudaStream_t stream);
 cudaError_t read_device_error_decode(unsigned long long *out);
-// Device address and size of the static decode scratch of the current device
-// (looked up on the first call per device).
-cudaError_t static_decode_scratch(void **ptr, size_t *bytes);
+// Device address and size of the static decode scratch of `device`, which
+// must be the current device (looked up on the first call per device).
+cudaError_t static_decode_scratch(int device, void **ptr, size_t *bytes);
 
 // prefill.cu
 cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, int num_seqs,

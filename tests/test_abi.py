@@ -34,6 +34,12 @@ def test_header_lists_the_calls():
     assert set(names) == set(B.EXPORTS)
 
 
+def test_static_scratch_limit_matches_the_header():
+    m = re.search(r"#define PKV_DECODE_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)",
+                  open(HEADER).read())
+    assert m and int(m.group(1)) << int(m.group(2)) == B.PKV_DECODE_STATIC_SCRATCH_BYTES
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name

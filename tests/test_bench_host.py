@@ -2,8 +2,10 @@
 behind every roofline number, checked against closed forms, and the guard
 that drops a profiled DRAM traffic figure once the kernel source changed."""
 import hashlib
+import json
 import os
 
+import pytest
 import torch
 
 import bench
@@ -83,3 +85,42 @@ def test_every_profiled_workload_names_a_committed_summary():
     for cfg, (src, summary) in bench.PROFILE_OF.items():
         assert os.path.exists(os.path.join(here, "paged_kv_cache_246_gb300", "csrc", src)), cfg
         assert os.path.exists(os.path.join(here, "profiles", summary)), cfg
+
+
+def test_write_bytes_closed_form():
+    lens = [3, 40]
+    for fp8, out_el in ((False, 2), (True, 1)):
+        w = _decode_workload(lens, fp8=fp8)
+        # 2 new tokens: K and V rows of 2 x 64 elements, read as bf16, written
+        # in the cache's element size
+        assert bench.write_bytes(w) == 2 * 2 * 2 * 64 * (2 + out_el)
+
+
+def test_extra_workloads_default_and_list():
+    class A:
+        extra, workload, scale_down = "auto", "decode", 1
+    assert bench.extra_workloads(A) == ["prefill", "mixed", "swa"]
+    A.workload = "prefill"
+    assert bench.extra_workloads(A) == []
+    A.extra = "swa,spec_decode"
+    assert bench.extra_workloads(A) == ["swa", "spec_decode"]
+    A.extra = "none"
+    assert bench.extra_workloads(A) == []
+    A.extra = "bogus"
+    with pytest.raises(SystemExit):
+        bench.extra_workloads(A)
+
+
+def test_reference_line_uses_the_gpu_arms_config_and_affinity_cores(monkeypatch, capsys):
+    # the tiny decode stands in for the headline workload to keep this quick
+    monkeypatch.setitem(bench.CFG_OF, "decode", 1)
+
+    class A:
+        workload, steps, warmup, gpus = "decode", 1, 3, 1
+    line = bench.run_reference(A, 1, 0)
+    printed = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert printed == json.loads(json.dumps(line))
+    assert line["config"] == bench.config_of(W.make_config(1), 1, 1)
+    assert line["impl"] == "reference" and line["value"] > 0
+    cpu = line["cpu_baseline"]
+    assert cpu["cores"] == len(os.sched_getaffinity(0)) and cpu["value_1core"] > 0
