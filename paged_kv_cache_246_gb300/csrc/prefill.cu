@@ -117,7 +117,8 @@ struct Lay {
                        B_Q2 = B_FIN + 1, B_QS = B_Q2 + 2, B_K8F = B_QS + 2, B_V8F = B_K8F + N8K,
                        B_E8K = B_V8F + N8V, B_E8V = B_E8K + N8K, NBAR = B_E8V + N8V;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int BYTES = OFF_MISC + 64;
+  static constexpr int OFF_RAMP = OFF_MISC + 64;  // fp32 0, 1, .., BN-1 (ALiBi key offsets)
+  static constexpr int BYTES = OFF_RAMP + BN * 4;
   // + alignment slack; at least ~118 KB so that one CTA owns an SM (and all
   // of its tensor memory)
   static constexpr int ALLOC = (BYTES + 1024) > 118 * 1024 ? (BYTES + 1024) : 118 * 1024;
@@ -222,6 +223,13 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
   }
   const int kv_start = kv_lo / BN * BN;
   const int ntiles = (kv_end - kv_start + BN - 1) / BN;
+  // Key tiles are visited in step order 0 .. ntiles-1.  With ALiBi the step
+  // order runs from the nearest key tile back to the farthest: the bias
+  // slope * (j - i) falls tile by tile in that order, so a row's reference
+  // max is set on its first (diagonal) tile and rarely has to move again,
+  // where the far-to-near order moved it, and rescaled O, every tile of a
+  // steep head.  phys(step) is the tile's index from kv_start.
+  auto phys = [ntiles](int step) { return ALIBI ? ntiles - 1 - step : step; };
 #pragma unroll
   for (int x = 0; x < 2; ++x) {
     if (qt[x].rows > 0) {
@@ -255,6 +263,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     prefetch_tensormap(&qmap);
     prefetch_tensormap(&kvmap);
   }
+  if (ALIBI && threadIdx.x < BN)
+    reinterpret_cast<float *>(smem + L::OFF_RAMP)[threadIdx.x] = static_cast<float>(threadIdx.x);
   if (warp == 1) tc5::tmem_alloc<512>(misc);
   tc5::fence_before_sync();
   __syncthreads();
@@ -278,7 +288,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     auto coord_of = [&](int j) -> int {
       int coord = -BS;
       if (lane < TB && j < ntiles) {
-        const int lb = (kv_start + j * BN) / BS + lane;
+        const int lb = (kv_start + phys(j) * BN) / BS + lane;
         const int p0 = lb * BS;
         if (p0 < kv_end && p0 + BS > kv_lo) {
           const int pb = __ldg(trow + lb);
@@ -360,7 +370,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     const uint64_t v_desc = tc5::sdesc_sw128(sbase + L::OFF_V, L::REG, 1024);
     const int j0A = qt[0].j0, j1A = qt[0].j1, j0B = qt[1].j0, j1B = qt[1].j1;
     auto active = [&](int x, int j) {
-      return x == 0 ? (j >= j0A && j < j1A) : (j >= j0B && j < j1B);
+      const int p = phys(j);
+      return x == 0 ? (p >= j0A && p < j1A) : (p >= j0B && p < j1B);
     };
     int k_ready = -1;  // highest key tile known to have landed
     auto need_k = [&](int j) -> bool {
@@ -422,7 +433,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       // whatever the cache holds there (possibly non-finite); their P is
       // exactly 0, but 0 * NaN is NaN, so those V rows are zeroed before the
       // PV product reads them.  Whole blocks past the end came in as zeros.
-      const int kv0 = kv_start + j * BN;
+      const int kv0 = kv_start + phys(j) * BN;
       const int zr = Lb - kv0;
       if (zr > 0 && zr < BN && zr % BS != 0) {
         const int ze = min(BN, (zr / BS + 1) * BS);
@@ -566,7 +577,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     }
     const int n = t.j1 - t.j0;
     for (int k = 0; ok && k < n; ++k) {
-      const int j = t.j0 + k;
+      const int j = ALIBI ? t.j1 - 1 - k : t.j0 + k;  // this tile's k-th key tile
       if (!warp_wait(&bars[L::B_SF + x], k & 1, abort_flag, where)) {
         ok = false;
         break;
@@ -579,23 +590,6 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       tc5::tmem_ld_wait();
       const int kv0 = kv_start + j * BN;
       const bool full = (kv0 + BN - 1 <= hi) && (kv0 >= lo);
-      if constexpr (ALIBI) {
-        // x = s * scale * log2e + slope * log2e * (j - i), in pairs
-        const float b0 = slope * static_cast<float>(kv0 - pos);
-        const unsigned long long sl2x2 = f2pack(sl2, sl2), slope2 = f2pack(slope, slope),
-                                 b0x2 = f2pack(b0, b0);
-#pragma unroll
-        for (int e = 0; e < BN; e += 2) {
-          const unsigned long long bias =
-              ffma2(slope2, f2pack(static_cast<float>(e), static_cast<float>(e + 1)), b0x2);
-          float v0, v1;
-          f2unpack(ffma2(f2pack(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1])), sl2x2,
-                         bias),
-                   v0, v1);
-          raw[e] = __float_as_uint(v0);
-          raw[e + 1] = __float_as_uint(v1);
-        }
-      }
       if (!full) {
 #pragma unroll
         for (int e = 0; e < BN; ++e)
@@ -603,8 +597,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       }
       const float unit = ALIBI ? 1.f : sl2;  // log2 units per unit of m
       // p = 2^(x - mu) over the tile, written to TMEM as P; returns the row
-      // sum.  With ALiBi x is already scaled; without, the scale is folded
-      // into the pair FMA.
+      // sum.  With ALiBi x is already scaled (and biased); without, the scale
+      // is folded into the pair FMA.
       auto exps = [&](float mu) -> float {
         const unsigned long long mul2 = ALIBI ? f2pack(1.f, 1.f) : f2pack(sl2, sl2);
         const unsigned long long negmu2 = f2pack(-mu, -mu);
@@ -629,23 +623,76 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
         f2unpack(fadd2(fadd2(ps2[0], ps2[1]), fadd2(ps2[2], ps2[3])), ps0, ps1);
         return ps0 + ps1;
       };
+      // ALiBi: p = 2^(s * sl2 + slope * e + A) for the tile's key offsets
+      // e = j - kv0 (read from the shared ramp), A = slope * (kv0 - i) - mu:
+      // the bias is folded into the exponent's FMA, raw scores untouched.
+      auto exps_alibi = [&](float A) -> float {
+        const unsigned long long mul2 = f2pack(sl2, sl2), slope2 = f2pack(slope, slope),
+                                 a2 = f2pack(A, A);
+        const float4 *ramp = reinterpret_cast<const float4 *>(smem + L::OFF_RAMP);
+        unsigned long long ps2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 r = ramp[(32 * c + e) / 4];
+            const unsigned long long b01 = ffma2(slope2, f2pack(r.x, r.y), a2);
+            const unsigned long long b23 = ffma2(slope2, f2pack(r.z, r.w), a2);
+            float x0, x1, x2, x3;
+            f2unpack(ffma2(f2pack(__uint_as_float(raw[32 * c + e]),
+                                  __uint_as_float(raw[32 * c + e + 1])),
+                           mul2, b01),
+                     x0, x1);
+            f2unpack(ffma2(f2pack(__uint_as_float(raw[32 * c + e + 2]),
+                                  __uint_as_float(raw[32 * c + e + 3])),
+                           mul2, b23),
+                     x2, x3);
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            const float p2 = fast_exp2(x2), p3 = fast_exp2(x3);
+            ps2[(e / 2) & 3] = fadd2(ps2[(e / 2) & 3], f2pack(p0, p1));
+            ps2[(e / 2 + 1) & 3] = fadd2(ps2[(e / 2 + 1) & 3], f2pack(p2, p3));
+            pk[e / 2] = OPT::from_f2(p0, p1);
+            pk[e / 2 + 1] = OPT::from_f2(p2, p3);
+          }
+          tc5::tmem_st16(sb + 16 * c, pk);
+        }
+        float ps0, ps1;
+        f2unpack(fadd2(fadd2(ps2[0], ps2[1]), fadd2(ps2[2], ps2[3])), ps0, ps1);
+        return ps0 + ps1;
+      };
       // The reference m moves lazily, so the tile's max only decides
       // whether it must move: the exponents are first taken against m as it
       // stands, and only a row whose sum is out of range (m not set yet, or a
       // p too large for an fp16 P) sends its warp through the max and a
-      // second pass.  With ALiBi the scores climb with the key position, so
-      // m moves every few tiles and the max always comes first.
+      // second pass.  With ALiBi the nearest key tile comes first, so m is
+      // set where the bias peaks and the later (farther) tiles rarely pass it.
       float alpha = 1.f;
       bool resc = false;
       float ps = 0.f;
-      bool slow = ALIBI || m == -INFINITY;
-      if constexpr (!ALIBI) {
-        if (!__any_sync(0xffffffffu, slow)) {
-          ps = exps(m * unit);
-          slow = !(ps <= 32768.f);
-        }
+      bool slow = m == -INFINITY;
+      if (!__any_sync(0xffffffffu, slow)) {
+        ps = ALIBI ? exps_alibi(slope * static_cast<float>(kv0 - pos) - m) : exps(m * unit);
+        slow = !(ps <= 32768.f);
       }
-      if (ALIBI || __any_sync(0xffffffffu, slow)) {
+      if (__any_sync(0xffffffffu, slow)) {
+        if constexpr (ALIBI) {
+          // x = s * scale * log2e + slope * log2e * (j - i), in pairs
+          const float b0 = slope * static_cast<float>(kv0 - pos);
+          const unsigned long long sl2x2 = f2pack(sl2, sl2), slope2 = f2pack(slope, slope),
+                                   b0x2 = f2pack(b0, b0);
+#pragma unroll
+          for (int e = 0; e < BN; e += 2) {
+            const unsigned long long bias =
+                ffma2(slope2, f2pack(static_cast<float>(e), static_cast<float>(e + 1)), b0x2);
+            float v0, v1;
+            f2unpack(ffma2(f2pack(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1])), sl2x2,
+                           bias),
+                     v0, v1);
+            raw[e] = __float_as_uint(v0);
+            raw[e + 1] = __float_as_uint(v1);
+          }
+        }
         // 8 independent 3-input max chains, then a small tree
         float pm[8];
 #pragma unroll
@@ -664,7 +711,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
           m = mx;
           resc = true;
         }
-        if constexpr (!ALIBI) tc5::tmem_st_wait();  // a first pass's P is written before it is replaced
+        tc5::tmem_st_wait();  // a first pass's P is written before it is replaced
         ps = exps(m == -INFINITY ? 0.f : m * unit);
       }
       l = l * alpha + ps;

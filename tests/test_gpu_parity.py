@@ -265,6 +265,25 @@ def climbing(w, q_gain=2.0, per_pos=1 / 40):
     return w
 
 
+def falling(w, q_gain=2.0, per_pos=1 / 40):
+    """Scores that fall with the key position: every cached context key row
+    scaled by 1 + (c - 1 - j) * per_pos (c the context length), queries by
+    q_gain, so the farthest keys score highest.  With ALiBi the kernel visits
+    the nearest key tile first; these rows then pass the reference max on
+    later (farther) tiles, which drives the max-first pass and the rescale in
+    that order."""
+    bs = w.block_size
+    row = w.kv_cache.shape[2] // bs
+    ctx = (w.seq_lens - w.query_lens).tolist()
+    for b, c in enumerate(ctx):
+        for j in range(c):
+            blk, off = int(w.block_tables[b, j // bs]), j % bs
+            seg = w.kv_cache[0, blk, off * row:(off + 1) * row]
+            seg.copy_((seg.float() * (1 + (c - 1 - j) * per_pos)).to(seg.dtype))
+    w.query = (w.query.float() * q_gain).to(w.query.dtype)
+    return w
+
+
 PREFILL_CASES = {
     "varlen_qpk4": lambda: small(41, H=32, KVH=8, seq_lens=[1, 17, 64, 65, 130, 300],
                                  query_lens=[1, 17, 64, 65, 130, 300], P=6),
@@ -279,6 +298,12 @@ PREFILL_CASES = {
     "climbing_scores": lambda: climbing(chunked(53, [0, 300, 700], [200, 129, 64])),
     "climbing_scores_fp16_qpk8": lambda: climbing(chunked(54, [450, 30], [100, 250],
                                                           dtype=torch.float16, H=16, KVH=2)),
+    "alibi_falling_scores": lambda: falling(chunked(55, [600, 1500, 40], [130, 64, 257],
+                                                    alibi=True, H=8, KVH=2)),
+    "alibi_climbing_scores": lambda: climbing(chunked(57, [300, 900], [200, 70], alibi=True,
+                                                      H=8, KVH=2)),
+    "alibi_qpk4_long_context": lambda: chunked(56, [1000, 2500], [300, 129], alibi=True, H=32,
+                                               KVH=8),
     "noncausal_varlen": lambda: small(51, H=32, KVH=8, causal=False, seq_lens=[1, 17, 129, 300],
                                       query_lens=[1, 17, 129, 300], P=4),
     "noncausal_chunked_alibi": lambda: chunked(52, [0, 70, 200], [150, 33, 257], causal=False,

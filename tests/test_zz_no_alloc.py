@@ -25,7 +25,7 @@ def _allocations():
     return torch.cuda.memory_stats(DEV).get("allocation.all.allocated", 0)
 
 
-@pytest.mark.parametrize("cfg,scale_down", [(2, 2), (5, 4), (1, 1)])
+@pytest.mark.parametrize("cfg,scale_down", [(2, 4), (5, 4), (1, 1)])
 def test_noalloc_matches_workspace_decode_twice(cfg, scale_down):
     w = W.make_config(cfg, scale_down=scale_down)
     r = CudaRun(w)
