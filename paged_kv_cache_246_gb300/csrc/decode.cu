@@ -37,17 +37,22 @@
 // PKV_ERR_TIMEOUT, drains the warp's copies in flight and leaves the output
 // unwritten for that CTA).
 //
-// Over an fp8 (E4M3) cache (KV8) the MMAs run on fp16 operands: the boxes
-// carry the 8-bit codes (16 tokens x D bytes, no swizzle); a lane's K
-// fragments come straight from its codes with cvt.rn.f16x2.e4m3x2, taking
-// the head dimension in a fixed permuted order (lane tq of a k-step covers
-// dims tq * D/4 + 4s .. + 3, one 32-bit word of codes) that the queries'
-// fragments follow too (a dot product does not depend on the order of its
-// terms); each unit's V codes are widened by the warp into a swizzled fp16
-// tile read by the same ldmatrix.trans as a 16-bit cache.  Queries are
-// fp16 x 2^-e, e chosen from the row group's largest magnitude (exact
-// power-of-two scaling); 2^e and k_scale join the softmax scale, v_scale
-// multiplies the output.
+// Over an fp8 (E4M3) cache (KV8) the boxes carry the 8-bit codes (16 tokens x
+// D bytes, 128-byte swizzle; 64-byte for D = 64).  q.k runs on the codes as
+// they are: mma.sync m16n8k32 on E4M3 operands, each query row scaled by a
+// power of two 2^-e (e from the row group's largest magnitude, largest
+// |q| in [2^7, 2^8)) and split into two E4M3 terms hi + lo, which hold every
+// component within 2^10 of the largest exactly (a bf16 value has 8
+// significant bits; hi takes 4, the remainder fits lo's 4); the head
+// dimension is taken in a fixed permuted order (lane tq of k-step s covers
+// dims tq * D/4 + 8s .. + 7, its own 16-byte chunk of each key row) that the
+// query fragments follow too (a dot product does not depend on the order of
+// its terms).  p.V runs transposed, O^T += V^T P^T on fp16 operands: the
+// P fragments of the score tile are already the B operand, and a lane builds
+// its V^T fragments from the codes of keys 2tq, 2tq+1, 2tq+8, 2tq+9 (its
+// dims 16g .. 16g+15, one 16-byte chunk per key row) with byte permutes and
+// cvt.rn.f16x2.e4m3x2, so the codes never go back to shared memory.  2^e
+// and k_scale join the softmax scale, v_scale multiplies the output.
 //
 // Decode context parallelism (backends.utils CommonAttentionMetadata
 // dcp_local_seq_lens): a rank of a group of R holds token j of each sequence
@@ -203,16 +208,70 @@ struct Lay {
   static constexpr int V16 = (D / 64) * BOX;  // one unit of K or V as 16-bit values
   static constexpr int TILE = KV8 ? kUnit * D : V16;  // one unit as stored in the cache
   static constexpr int STAGE = 2 * TILE;
-  // per-warp rings, then (fp8) each warp's widened V tile, then a zero tile
+  // per-warp rings, then (16-bit cache) a zero V tile; the merge buffers
+  // reuse the area once the rings are drained
   static constexpr int NST = Ring<KV8>::stages;
-  static constexpr int ZERO = kWarps * NST * STAGE + (KV8 ? kWarps * V16 : 0);
-  static constexpr int TILES = ZERO + V16;
-  static constexpr int MERGE = kWarps * kRows * (D + 2) * 4;  // reuses the tiles
-  static_assert(MERGE <= TILES, "merge buffers fit in the tile area");
+  static constexpr int ZERO = kWarps * NST * STAGE;
+  static constexpr int MERGE = kWarps * kRows * (D + 2) * 4;
+  static constexpr int TILES = (ZERO + (KV8 ? 0 : V16)) > MERGE ? ZERO + (KV8 ? 0 : V16) : MERGE;
 };
 
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Byte offset, inside a unit's tile of E4M3 codes (16 key rows of D bytes,
+// loaded with the 128-byte swizzle for D = 128 and the 64-byte one for
+// D = 64), of 16-byte chunk `chunk` of key row `row`.
+template <int D>
+__device__ __forceinline__ uint32_t swz8(int row, int chunk) {
+  if constexpr (D == 128)
+    return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+  else
+    return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
+// D[16x8] += A[16x32] B[32x8] on E4M3 operands, fp32 accumulate.
+__device__ __forceinline__ void mma16832_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// The same with rows 8..15 of A zero (their results discarded).
+__device__ __forceinline__ void mma16832_e4m3_top(float (&d)[2], uint32_t a0, uint32_t a2,
+                                                  uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "{\n\t.reg .f32 z0, z1;\n\t"
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, z0, z1}, "
+      "{%2, %4, %3, %4}, {%5, %6}, {%0, %1, %7, %7};\n\t}"
+      : "+f"(d[0]), "+f"(d[1])
+      : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Four floats (first in the low byte) as E4M3 codes, nearest even,
+// saturating: hi; and the codes of what hi leaves over: lo.
+__device__ __forceinline__ void split_e4m3x4(float v0, float v1, float v2, float v3, uint32_t &hi,
+                                             uint32_t &lo) {
+  auto pack = [](float a, float b, float c, float d) -> uint32_t {
+    uint16_t p01, p23;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(p01) : "f"(a), "f"(b));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(p23) : "f"(c), "f"(d));
+    return static_cast<uint32_t>(p01) | (static_cast<uint32_t>(p23) << 16);
+  };
+  hi = pack(v0, v1, v2, v3);
+  const uint2 h = e4m3x4_to_h4(hi);  // exact: every E4M3 value is an fp16 value
+  const float2 f01 = FP16::to_f2(h.x), f23 = FP16::to_f2(h.y);
+  lo = pack(v0 - f01.x, v1 - f01.y, v2 - f23.x, v3 - f23.y);
+}
+
+// Bytes {a.b[j], b.b[j], a.b[j+1], b.b[j+1]} for j = 0 (even m-tile) or 2.
+__device__ __forceinline__ uint32_t interleave2(uint32_t a, uint32_t b, int j) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(j ? 0x7362u : 0x5140u));
+  return r;
 }
 
 // Byte offset, inside a unit's K or V tile, of the 16-byte chunk `chunk`
@@ -312,8 +371,9 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
     }
     coord[k] = pb * a.BS + p0 % a.BS;
   }
-  for (int i = threadIdx.x; i < L::V16 / 16; i += kThreads)
-    reinterpret_cast<uint4 *>(tiles + L::ZERO)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if constexpr (!KV8)  // the zero V tile (16-bit cache only)
+    for (int i = threadIdx.x; i < L::V16 / 16; i += kThreads)
+      reinterpret_cast<uint4 *>(tiles + L::ZERO)[i] = make_uint4(0u, 0u, 0u, 0u);
   uint64_t *wbar = bars + warp * L::NST;
   if (lane == 0) {
     for (int st = 0; st < L::NST; ++st) mbar_init(&wbar[st], 1);
@@ -347,47 +407,53 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   uint32_t qa[KS][4];
   float sl2 = a.scale_log2;
   if constexpr (KV8) {
-    // permuted dims: k-step s, positions 2tq, 2tq+1 -> dims tq * D/4 + 4s + 0, 1
-    // and positions 8 + 2tq, 9 + 2tq -> + 2, 3: four consecutive elements
-    uint2 raw[2][KS];
+    // E4M3 terms: qa[s] = hi, qa[KS8 + s] = lo of k-step s (32 positions):
+    // positions 4tq .. 4tq+3 -> dims tq * D/4 + 8s + 0..3, positions
+    // 16 + 4tq .. -> dims tq * D/4 + 8s + 4..7 (eight consecutive elements)
+    constexpr int KS8 = D / 32;
+    auto qchunk = [&](int x, int s) -> uint4 {  // this lane's dims tq * D/4 + 8s .. + 7 of row x
+      const uint4 *qp = reinterpret_cast<const uint4 *>(a.query) +
+                        (static_cast<int64_t>(orow[x]) * D + tq * (D / 4)) / 8;
+      return valid[x] ? __ldg(qp + s) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    uint32_t am = 0;  // largest |q| bit pattern (fp32)
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      const uint2 *qp = reinterpret_cast<const uint2 *>(a.query) +
-                        (static_cast<int64_t>(orow[x]) * D + tq * (D / 4)) / 4;
+    for (int x = 0; x < NR; ++x)
 #pragma unroll
-      for (int s = 0; s < KS; ++s) raw[x][s] = valid[x] ? __ldg(qp + s) : make_uint2(0u, 0u);
-    }
-    if constexpr (std::is_same<T, BF16>::value) {
-      uint32_t am = 0;  // per-halfword max of |bf16| bit patterns
+      for (int s = 0; s < KS8; ++s) {
+        const uint4 u = qchunk(x, s);
 #pragma unroll
-      for (int x = 0; x < 2; ++x)
-#pragma unroll
-        for (int s = 0; s < KS; ++s)
-          am = __vmaxu2(am, __vmaxu2(raw[x][s].x & 0x7fff7fffu, raw[x][s].y & 0x7fff7fffu));
-      // every warp holds the whole row group, so a warp's max is the group's
-      am = __reduce_max_sync(0xffffffffu, max(am & 0xffffu, am >> 16));
-      const int E = static_cast<int>(am >> 7);
-      // largest |q| * 2^-e in [2^14, 2^15): inside fp16's range, full precision
-      const int e = E == 0 ? 0 : min(64, max(-64, E - 141));
-      const float mul = __int_as_float((127 - e) << 23);
-      sl2 *= __int_as_float((127 + e) << 23);
-#pragma unroll
-      for (int x = 0; x < 2; ++x)
-#pragma unroll
-        for (int s = 0; s < KS; ++s) {
-          const float2 f0 = BF16::to_f2(raw[x][s].x), f1 = BF16::to_f2(raw[x][s].y);
-          qa[s][x] = FP16::from_f2(f0.x * mul, f0.y * mul);
-          qa[s][2 + x] = FP16::from_f2(f1.x * mul, f1.y * mul);
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = T::to_f2(word_of(u, k));
+          am = max(am, max(__float_as_uint(fabsf(f.x)), __float_as_uint(fabsf(f.y))));
         }
-    } else {
+      }
+    // every warp holds the whole row group, so a warp's max is the group's
+    am = __reduce_max_sync(0xffffffffu, am);
+    const int E = static_cast<int>(am >> 23);
+    // largest |q| * 2^-e in [2^7, 2^8): hi and lo inside E4M3's range
+    const int e = E == 0 ? 0 : min(64, max(-64, E - 134));
+    const float mul = __int_as_float((127 - e) << 23);
+    sl2 *= __int_as_float((127 + e) << 23);
 #pragma unroll
-      for (int x = 0; x < 2; ++x)
+    for (int s = 0; s < KS; ++s)
 #pragma unroll
-        for (int s = 0; s < KS; ++s) {
-          qa[s][x] = raw[x][s].x;
-          qa[s][2 + x] = raw[x][s].y;
+      for (int c = 0; c < 4; ++c) qa[s][c] = 0u;
+#pragma unroll
+    for (int x = 0; x < NR; ++x)
+#pragma unroll
+      for (int s = 0; s < KS8; ++s) {
+        const uint4 u = qchunk(x, s);
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = T::to_f2(word_of(u, k));
+          v[2 * k] = f.x * mul;
+          v[2 * k + 1] = f.y * mul;
         }
-    }
+        split_e4m3x4(v[0], v[1], v[2], v[3], qa[s][x], qa[KS8 + s][x]);
+        split_e4m3x4(v[4], v[5], v[6], v[7], qa[s][2 + x], qa[KS8 + s][2 + x]);
+      }
   } else {
     const uint32_t *q0 = reinterpret_cast<const uint32_t *>(a.query) +
                          (static_cast<int64_t>(orow[0]) * D) / 2;
@@ -408,6 +474,10 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   for (int n = 0; n < NT; ++n)
 #pragma unroll
     for (int c = 0; c < 2 * NR; ++c) o[n][c] = 0.f;
+  // fp8 cache: the same registers as O^T tiles: ot[mt][nt][c] holds dims
+  // dm(mt) + (c >> 1) (dm(mt) = 16g + 2mt for D = 128, 8g + 2mt for D = 64)
+  // of query rows 8nt + 2tq + (c & 1)
+  float(&ot)[D / 16][NR][4] = *reinterpret_cast<float(*)[D / 16][NR][4]>(&o[0][0]);
   // keys every row of the CTA sees: no masking needed on a unit inside them
   const int pos_min = sp.L - q;  // token 0
   const int lo_max = a.window > 0 ? max(0, sp.L - a.window) : 0;  // last token's window start
@@ -421,7 +491,6 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   const int v_tok = (mi & 1) * 8 + rr, v_half = mi >> 1;  // V^T: token halves x dims
   bool ok = true;
   int consumed = 0;
-  uint8_t *v16 = tiles + kWarps * L::NST * L::STAGE + warp * L::V16;  // fp8: widened V
 
   for (int k = 0; k < my_count; ++k) {
     const int st = k % L::NST;
@@ -454,38 +523,36 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
       }
     };
     if constexpr (KV8) {
-      // keys g and g + 8: this lane's D/4 codes of each, widened per k-step
+      // keys g and g + 8: this lane's D/4 codes of each (its chunks of the
+      // swizzled rows), straight into the E4M3 products, hi then lo terms
+      constexpr int KS8 = D / 32, KC = D / 64;
       const uint8_t *kc = wt + st * L::STAGE;
-      uint4 kk[2][D / 64];
+      uint4 kk[2][KC];
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          kk[n][c] = *reinterpret_cast<const uint4 *>(kc + (g + 8 * n) * D + tq * (D / 4) + 16 * c);
+        for (int c = 0; c < KC; ++c)
+          kk[n][c] = *reinterpret_cast<const uint4 *>(kc + swz8<D>(g + 8 * n, tq * KC + c));
 #pragma unroll
-      for (int s = 0; s < KS; ++s)
+      for (int s = 0; s < KS8; ++s)
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
-          const uint2 kb = e4m3x4_to_h4(word_of(kk[n][s / 4], s % 4));
-          mma_s(n, s, qa[s], kb.x, kb.y);
+          const uint32_t b0 = word_of(kk[n][(2 * s) / 4], (2 * s) % 4);
+          const uint32_t b1 = word_of(kk[n][(2 * s + 1) / 4], (2 * s + 1) % 4);
+          if constexpr (HALF) {
+            float d2[2] = {sc[n][0], sc[n][1]};
+            mma16832_e4m3_top(d2, qa[s][0], qa[s][2], b0, b1);
+            sc[n][0] = d2[0];
+            sc[n][1] = d2[1];
+            float e2[2] = {sc2[n][0], sc2[n][1]};
+            mma16832_e4m3_top(e2, qa[KS8 + s][0], qa[KS8 + s][2], b0, b1);
+            sc2[n][0] = e2[0];
+            sc2[n][1] = e2[1];
+          } else {
+            mma16832_e4m3(sc[n], qa[s], b0, b1);
+            mma16832_e4m3(sc2[n], qa[KS8 + s], b0, b1);
+          }
         }
-      // this unit's V codes -> the warp's swizzled fp16 tile: lane (token
-      // vt_, half vh) widens D/2 codes, 16 at a time, reads rotated by token
-      const uint8_t *vc = kc + L::TILE;
-      const int vt_ = lane >> 1, vh = lane & 1;
-      constexpr int NI = D / 32;  // 16-code pieces per lane
-#pragma unroll 2  // (fully unrolled, the half-tile fp8 variant spills)
-      for (int i = 0; i < NI; ++i) {
-        const int ip = (i + vt_) % NI;
-        const int d0 = vh * (D / 2) + 16 * ip;
-        const uint4 u = *reinterpret_cast<const uint4 *>(vc + vt_ * D + d0);
-        const uint2 h0 = e4m3x4_to_h4(u.x), h1 = e4m3x4_to_h4(u.y);
-        const uint2 h2 = e4m3x4_to_h4(u.z), h3 = e4m3x4_to_h4(u.w);
-        *reinterpret_cast<uint4 *>(v16 + swz(vt_, d0 / 8)) = make_uint4(h0.x, h0.y, h1.x, h1.y);
-        *reinterpret_cast<uint4 *>(v16 + swz(vt_, d0 / 8 + 1)) =
-            make_uint4(h2.x, h2.y, h3.x, h3.y);
-      }
-      vt = smem_u32(v16);
     } else {
 #pragma unroll
       for (int s = 0; s < KS; ++s) {
@@ -525,6 +592,7 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
     }
     if (__any_sync(0xffffffffu, grow)) {
       // move the references to the true row maxima (4 lanes hold a row)
+      float al[2] = {1.f, 1.f};
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
         float mx = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
@@ -535,10 +603,28 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
           const float alpha = m[r] == -INFINITY ? 0.f : fast_exp2(m[r] - mn);
           m[r] = mn;
           l[r] *= alpha;
+          al[r] = alpha;
+          if constexpr (!KV8) {
 #pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            o[n][2 * r] *= alpha;
-            o[n][2 * r + 1] *= alpha;
+            for (int n = 0; n < NT; ++n) {
+              o[n][2 * r] *= alpha;
+              o[n][2 * r + 1] *= alpha;
+            }
+          }
+        }
+      }
+      if constexpr (KV8) {
+        // O^T columns are query rows 8nt + 2tq, + 1, owned by lanes 8tq, 8tq + 4
+#pragma unroll
+        for (int nt = 0; nt < NR; ++nt) {
+          const float a0 = __shfl_sync(0xffffffffu, al[nt], 8 * tq);
+          const float a1 = __shfl_sync(0xffffffffu, al[nt], 8 * tq + 4);
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            ot[mt][nt][0] *= a0;
+            ot[mt][nt][1] *= a1;
+            ot[mt][nt][2] *= a0;
+            ot[mt][nt][3] *= a1;
           }
         }
       }
@@ -555,24 +641,63 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
       pa[r] = MT::from_f2(p[0], p[1]);      // keys 2tq, 2tq + 1
       pa[2 + r] = MT::from_f2(p[2], p[3]);  // keys 8 + 2tq, 9 + 2tq
     }
-    if constexpr (KV8) __syncwarp();  // the widened V tile is complete
     // Slots past the rank's last token in its last cache block hold whatever
     // the cache holds there, possibly non-finite: their P is exactly 0, but
-    // 0 * NaN is NaN, so the lanes whose V row (token v_tok) is such a slot
-    // read that row from the zero tile instead (fp8: instead of the widened
-    // tile).  Stale K rows need nothing: their scores are masked to -inf.
-    if (j0 + v_tok * RW >= pos_min + q) vt = smem_u32(tiles + L::ZERO);
-    // ---- O += P V: n-tiles of 8 dims, two per ldmatrix ---------------------
+    // 0 * NaN is NaN, so V rows of such slots are read as zeros (16-bit
+    // cache: the lanes whose ldmatrix row is such a slot read the zero tile;
+    // fp8: the codes of such rows are replaced by zeros).  Stale K rows need
+    // nothing: their scores are masked to -inf.
+    if constexpr (KV8) {
+      // ---- O^T += V^T P^T: m-tiles of 16 dims, P fragments as the B operand
+      constexpr int VW = D / 32;  // words of this lane's chunk of a key row
+      const uint8_t *vc = wt + st * L::STAGE + L::TILE;
+      const bool tail = j0 + (kUnit - 1) * RW >= pos_min + q;
+      uint32_t vw[4][VW];  // keys 2tq, 2tq + 1, 2tq + 8, 2tq + 9
 #pragma unroll
-    for (int n2 = 0; n2 < NT / 2; ++n2) {
-      uint32_t vb[4];
-      ldsm_x4_t(vt + swz(v_tok, 2 * n2 + v_half), vb);
-      if constexpr (HALF) {
-        mma16816_top<MT>(o[2 * n2], pa[0], pa[2], vb[0], vb[1]);
-        mma16816_top<MT>(o[2 * n2 + 1], pa[0], pa[2], vb[2], vb[3]);
-      } else {
-        mma16816<MT>(o[2 * n2], pa, vb[0], vb[1]);
-        mma16816<MT>(o[2 * n2 + 1], pa, vb[2], vb[3]);
+      for (int kk = 0; kk < 4; ++kk) {
+        const int kr = 2 * tq + (kk & 1) + 8 * (kk >> 1);
+        if constexpr (D == 128) {
+          const uint4 u = *reinterpret_cast<const uint4 *>(vc + swz8<D>(kr, g));
+          vw[kk][0] = u.x;
+          vw[kk][1] = u.y;
+          vw[kk][2] = u.z;
+          vw[kk][3] = u.w;
+        } else {
+          const uint2 u =
+              *reinterpret_cast<const uint2 *>(vc + swz8<D>(kr, g >> 1) + 8 * (g & 1));
+          vw[kk][0] = u.x;
+          vw[kk][1] = u.y;
+        }
+        if (tail && j0 + kr * RW >= pos_min + q) {
+#pragma unroll
+          for (int w = 0; w < VW; ++w) vw[kk][w] = 0u;
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        // A rows g / g + 8 = dims dm(mt) / dm(mt) + 1: bytes 2mt, 2mt + 1 of
+        // the lane's chunk, keys paired as the fragment wants them
+        const int w = mt >> 1, j = (mt & 1) * 2;
+        const uint2 h01 = e4m3x4_to_h4(interleave2(vw[0][w], vw[1][w], j));
+        const uint2 h89 = e4m3x4_to_h4(interleave2(vw[2][w], vw[3][w], j));
+        const uint32_t av[4] = {h01.x, h01.y, h89.x, h89.y};
+        mma16816<FP16>(ot[mt][0], av, pa[0], pa[2]);
+        if constexpr (!HALF) mma16816<FP16>(ot[mt][1], av, pa[1], pa[3]);
+      }
+    } else {
+      if (j0 + v_tok * RW >= pos_min + q) vt = smem_u32(tiles + L::ZERO);
+      // ---- O += P V: n-tiles of 8 dims, two per ldmatrix -------------------
+#pragma unroll
+      for (int n2 = 0; n2 < NT / 2; ++n2) {
+        uint32_t vb[4];
+        ldsm_x4_t(vt + swz(v_tok, 2 * n2 + v_half), vb);
+        if constexpr (HALF) {
+          mma16816_top<MT>(o[2 * n2], pa[0], pa[2], vb[0], vb[1]);
+          mma16816_top<MT>(o[2 * n2 + 1], pa[0], pa[2], vb[2], vb[3]);
+        } else {
+          mma16816<MT>(o[2 * n2], pa, vb[0], vb[1]);
+          mma16816<MT>(o[2 * n2 + 1], pa, vb[2], vb[3]);
+        }
       }
     }
     __syncwarp();  // every lane has read the stage: refill it
@@ -603,14 +728,27 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
     sL[warp * kRows + g] = ok ? l[0] : 0.f;
     sL[warp * kRows + g + 8] = ok ? l[1] : 0.f;
   }
+  if constexpr (KV8) {
 #pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    float *r0 = sO + (warp * kRows + g) * D + 8 * n + 2 * tq;
-    r0[0] = o[n][0];
-    r0[1] = o[n][1];
-    if constexpr (!HALF) {
-      r0[8 * D] = o[n][2];
-      r0[8 * D + 1] = o[n][3];
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NR; ++nt) {
+        float *r0 = sO + (warp * kRows + 8 * nt + 2 * tq) * D + (D == 128 ? 16 : 8) * g + 2 * mt;
+        r0[0] = ot[mt][nt][0];
+        r0[D] = ot[mt][nt][1];
+        r0[1] = ot[mt][nt][2];
+        r0[D + 1] = ot[mt][nt][3];
+      }
+  } else {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      float *r0 = sO + (warp * kRows + g) * D + 8 * n + 2 * tq;
+      r0[0] = o[n][0];
+      r0[1] = o[n][1];
+      if constexpr (!HALF) {
+        r0[8 * D] = o[n][2];
+        r0[8 * D + 1] = o[n][3];
+      }
     }
   }
   __syncthreads();
@@ -821,15 +959,16 @@ cudaError_t launch_decode(void *out, const void *query, int num_seqs, int query_
                                  static_cast<cuuint64_t>(g.row_elems) * eb,
                                  static_cast<cuuint64_t>(g.num_blocks * g.block_elems) * eb};
   // 16-bit cache: 64-dim boxes, 128-byte swizzle (ldmatrix reads them);
-  // fp8 cache: one plain box of D codes per row
+  // fp8 cache: one box of D codes per row, swizzled by its row length
   const cuuint32_t box[4] = {g.fp8 ? static_cast<cuuint32_t>(g.D) : 64u, 1,
                              static_cast<cuuint32_t>(dec::kUnit), 1};
   const bool bf = g.dtype == PKV_BF16;
   const CUtensorMapDataType dt =
       g.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
             : (bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
-  if (encode_tensor_map(&tmap, dt, 4, const_cast<void *>(kv_cache), dims, strides, box,
-                        g.fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B) !=
+  const CUtensorMapSwizzle swz = !g.fp8 || g.D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                     : CU_TENSOR_MAP_SWIZZLE_64B;
+  if (encode_tensor_map(&tmap, dt, 4, const_cast<void *>(kv_cache), dims, strides, box, swz) !=
       CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   dec::Args a{};

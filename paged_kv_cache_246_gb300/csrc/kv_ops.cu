@@ -15,35 +15,55 @@
 namespace pkv {
 
 // ---------------------------------------------------------------------------
-// kv_cache_write: thread i copies 16-byte chunk (i % row_chunks) of token
-// (i / row_chunks) into K and V halves at its slot.
+// kv_cache_write: warp w of the grid copies tokens w, w + warps, ...: its
+// lanes take the row's 16-byte chunks lane, lane + 32, ..., U of them in
+// flight per lane for each half; the slot is read once per token.  No
+// per-chunk index arithmetic beyond an add.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
+constexpr int kWriteThreads = 256;
+constexpr int kWriteWarps = kWriteThreads / 32;
+
+template <int U>
+__global__ void __launch_bounds__(kWriteThreads)
 kv_write_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value, int64_t num_tokens,
                 uint4 *__restrict__ k_half, uint4 *__restrict__ v_half,
                 const int64_t *__restrict__ slots, int64_t num_slots, int row_chunks) {
-  const int64_t total = num_tokens * row_chunks;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += stride) {
-    const int64_t t = i / row_chunks;
-    const int64_t c = i - t * row_chunks;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * kWriteWarps;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWriteWarps + (threadIdx.x >> 5);
+       t < num_tokens; t += warps) {
     const int64_t s = __ldg(slots + t);
     if (s < 0) continue;  // padding token
     if (s >= num_slots) {
-      record_error(PKV_ERR_BOUNDS, t);
+      if (lane == 0) record_error(PKV_ERR_BOUNDS, t);
       continue;
     }
-    const uint4 kv = __ldg(key + i);
-    const uint4 vv = __ldg(value + i);
-    k_half[s * row_chunks + c] = kv;
-    v_half[s * row_chunks + c] = vv;
+    const uint4 *kr = key + t * row_chunks, *vr = value + t * row_chunks;
+    uint4 *kd = k_half + s * row_chunks, *vd = v_half + s * row_chunks;
+    int c = lane;
+    for (; c + 32 * (U - 1) < row_chunks; c += 32 * U) {
+      uint4 kk[U], vv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        kk[u] = __ldg(kr + c + 32 * u);
+        vv[u] = __ldg(vr + c + 32 * u);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        kd[c + 32 * u] = kk[u];
+        vd[c + 32 * u] = vv[u];
+      }
+    }
+    for (; c < row_chunks; c += 32) {
+      kd[c] = __ldg(kr + c);
+      vd[c] = __ldg(vr + c);
+    }
   }
 }
 
-// fp8 cache: thread i produces 16-byte chunk (i % row_chunks) of codes of
-// token (i / row_chunks), from 16 input elements: code = nearest E4M3 to
-// x / scale (IEEE fp32 division, round to nearest even, saturating at 448).
+// fp8 cache: lane chunk c of a token is 16 codes, made from 16 input
+// elements (two 16-byte input chunks): code = nearest E4M3 to x / scale
+// (IEEE fp32 division, round to nearest even, saturating at 448).
 template <class T>
 __device__ __forceinline__ uint32_t quant4(uint2 in, float scale) {
   float2 a = T::to_f2(in.x), b = T::to_f2(in.y);
@@ -55,31 +75,35 @@ __device__ __forceinline__ uint32_t quant4(uint2 in, float scale) {
 }
 
 template <class T>
-__global__ void __launch_bounds__(256)
+__device__ __forceinline__ uint4 quant16(uint4 a, uint4 b, float scale) {
+  return make_uint4(quant4<T>(make_uint2(a.x, a.y), scale), quant4<T>(make_uint2(a.z, a.w), scale),
+                    quant4<T>(make_uint2(b.x, b.y), scale), quant4<T>(make_uint2(b.z, b.w), scale));
+}
+
+template <class T>
+__global__ void __launch_bounds__(kWriteThreads)
 kv_write_fp8_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
                     int64_t num_tokens, uint4 *__restrict__ k_half, uint4 *__restrict__ v_half,
                     const int64_t *__restrict__ slots, int64_t num_slots, int row_chunks,
                     float k_scale, float v_scale) {
-  const int64_t total = num_tokens * row_chunks;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += stride) {
-    const int64_t t = i / row_chunks;
-    const int64_t c = i - t * row_chunks;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * kWriteWarps;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWriteWarps + (threadIdx.x >> 5);
+       t < num_tokens; t += warps) {
     const int64_t s = __ldg(slots + t);
     if (s < 0) continue;  // padding token
     if (s >= num_slots) {
-      record_error(PKV_ERR_BOUNDS, t);
+      if (lane == 0) record_error(PKV_ERR_BOUNDS, t);
       continue;
     }
-    const uint4 k0 = __ldg(key + 2 * i), k1 = __ldg(key + 2 * i + 1);
-    const uint4 v0 = __ldg(value + 2 * i), v1 = __ldg(value + 2 * i + 1);
-    k_half[s * row_chunks + c] =
-        make_uint4(quant4<T>(make_uint2(k0.x, k0.y), k_scale), quant4<T>(make_uint2(k0.z, k0.w), k_scale),
-                   quant4<T>(make_uint2(k1.x, k1.y), k_scale), quant4<T>(make_uint2(k1.z, k1.w), k_scale));
-    v_half[s * row_chunks + c] =
-        make_uint4(quant4<T>(make_uint2(v0.x, v0.y), v_scale), quant4<T>(make_uint2(v0.z, v0.w), v_scale),
-                   quant4<T>(make_uint2(v1.x, v1.y), v_scale), quant4<T>(make_uint2(v1.z, v1.w), v_scale));
+    const uint4 *kr = key + 2 * t * row_chunks, *vr = value + 2 * t * row_chunks;
+    uint4 *kd = k_half + s * row_chunks, *vd = v_half + s * row_chunks;
+    for (int c = lane; c < row_chunks; c += 32) {
+      const uint4 k0 = __ldg(kr + 2 * c), k1 = __ldg(kr + 2 * c + 1);
+      const uint4 v0 = __ldg(vr + 2 * c), v1 = __ldg(vr + 2 * c + 1);
+      kd[c] = quant16<T>(k0, k1, k_scale);
+      vd[c] = quant16<T>(v0, v1, v_scale);
+    }
   }
 }
 
@@ -88,41 +112,177 @@ cudaError_t launch_kv_write(const void *key, const void *value, int64_t num_toke
   DeviceInfo dev;
   cudaError_t e = current_device_info(&dev);
   if (e != cudaSuccess) return e;
-  if (g.fp8) {
-    const int row_chunks = static_cast<int>(g.row_bytes / 16);  // 16 codes per chunk
-    const int64_t num_slots = g.num_blocks * g.BS;
-    uint4 *k_half = static_cast<uint4 *>(kv_cache);
-    uint4 *v_half = k_half + num_slots * row_chunks;
-    const int64_t total = num_tokens * row_chunks;
-    const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, int64_t(dev.sms) * 8));
-    auto kern = g.dtype == PKV_BF16 ? kv_write_fp8_kernel<BF16> : kv_write_fp8_kernel<FP16>;
-    kern<<<blocks, 256, 0, stream>>>(static_cast<const uint4 *>(key),
-                                     static_cast<const uint4 *>(value), num_tokens, k_half, v_half,
-                                     slot_mapping, num_slots, row_chunks, g.k_scale, g.v_scale);
-    return cudaGetLastError();
-  }
-  const int row_chunks = static_cast<int>(g.row_elems * 2 / 16);
+  const int row_chunks = static_cast<int>(g.row_bytes / 16);  // 16-byte chunks of a cache row
   const int64_t num_slots = g.num_blocks * g.BS;
   uint4 *k_half = static_cast<uint4 *>(kv_cache);
   uint4 *v_half = k_half + num_slots * row_chunks;
-  const int64_t total = num_tokens * row_chunks;
-  const int threads = 256;
-  const int64_t want = (total + threads - 1) / threads;
-  const int blocks = static_cast<int>(std::min<int64_t>(want, int64_t(dev.sms) * 8));
-  kv_write_kernel<<<blocks, threads, 0, stream>>>(
-      static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), num_tokens, k_half,
-      v_half, slot_mapping, num_slots, row_chunks);
+  // one warp per token, up to 8 CTAs per SM
+  const int blocks = static_cast<int>(std::min<int64_t>(
+      (num_tokens + kWriteWarps - 1) / kWriteWarps, int64_t(dev.sms) * 8));
+  const uint4 *k = static_cast<const uint4 *>(key), *v = static_cast<const uint4 *>(value);
+  if (g.fp8) {
+    auto kern = g.dtype == PKV_BF16 ? kv_write_fp8_kernel<BF16> : kv_write_fp8_kernel<FP16>;
+    kern<<<blocks, kWriteThreads, 0, stream>>>(k, v, num_tokens, k_half, v_half, slot_mapping,
+                                               num_slots, row_chunks, g.k_scale, g.v_scale);
+  } else {
+    kv_write_kernel<4><<<blocks, kWriteThreads, 0, stream>>>(k, v, num_tokens, k_half, v_half,
+                                                             slot_mapping, num_slots, row_chunks);
+  }
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// kv_copy_blocks: CTA (pair, layer) copies one block in both halves.
+// kv_copy_blocks: bulk copies through shared memory.  The work is cut into
+// pieces of up to kCopyPiece bytes, index ((pair * layers + layer) * 2 +
+// half) * pieces_per_half + part, and CTA c takes the contiguous range
+// [c * P / G, (c + 1) * P / G) of the P pieces (G CTAs, one per SM), so
+// every CTA moves the same bytes to within one piece.  One thread per CTA
+// streams them through a ring of kCopyStages shared-memory stages:
+// cp.async.bulk loads (completed on an mbarrier each) and cp.async.bulk
+// stores back out.  A store reads its stage only as it drains towards
+// memory, so a stage is refilled kCopyLag pieces after its store was issued:
+// about kCopyLag stores and kCopyStages - kCopyLag loads stay in flight.
 // ---------------------------------------------------------------------------
 constexpr int kMaxLayers = 256;
 struct LayerPtrs {
-  uint4 *p[kMaxLayers];
+  uint8_t *p[kMaxLayers];
 };
+constexpr int kCopyStages = 12;
+constexpr int kCopyLag = 6;
+constexpr int kCopyPiece = 16384;
+constexpr int kCopySmem = kCopyStages * kCopyPiece + 128;
 
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *dst, const void *smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// all but the newest N committed groups have finished reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// every committed group has completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(32, 1)
+kv_copy_kernel(const __grid_constant__ LayerPtrs caches, const int64_t *__restrict__ pairs,
+               int num_layers, int64_t num_blocks, int64_t block_bytes, int64_t pieces_per_half,
+               int64_t total_pieces) {
+  extern __shared__ uint8_t copy_smem_raw[];
+  __shared__ uint64_t bars[kCopyStages];
+  if (threadIdx.x != 0) return;
+  uint8_t *stages = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(copy_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  const int64_t p0 = total_pieces * blockIdx.x / gridDim.x;
+  const int64_t n = total_pieces * (blockIdx.x + 1) / gridDim.x - p0;
+  for (int s = 0; s < kCopyStages; ++s) mbar_init(&bars[s], 1);
+  fence_mbar_init();
+
+  // source, destination and size of piece k of this CTA; false for a bad
+  // pair (recorded, never dereferenced)
+  auto locate = [&](int64_t k, const uint8_t *&src, uint8_t *&dst, uint32_t &bytes) -> bool {
+    const int64_t p = p0 + k;
+    const int64_t hb = p / pieces_per_half;
+    const int64_t part = p - hb * pieces_per_half;
+    const int64_t pl = hb >> 1;
+    const int layer = static_cast<int>(pl % num_layers);
+    const int64_t pair = pl / num_layers;
+    const int64_t s = __ldg(pairs + 2 * pair), d = __ldg(pairs + 2 * pair + 1);
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+      record_error(PKV_ERR_BOUNDS, pair);
+      return false;
+    }
+    const int64_t off = part * kCopyPiece;
+    bytes = static_cast<uint32_t>(min(static_cast<int64_t>(kCopyPiece), block_bytes - off));
+    uint8_t *base = caches.p[layer] + (hb & 1) * num_blocks * block_bytes;
+    src = base + s * block_bytes + off;
+    dst = base + d * block_bytes + off;
+    return true;
+  };
+  uint32_t loaded = 0;  // bit s: stage s has a load in flight (or landed, not stored)
+  uint32_t phase = 0;   // bit s: parity of stage s's next completion
+  auto load = [&](int64_t k) {
+    const int s = static_cast<int>(k % kCopyStages);
+    const uint8_t *src;
+    uint8_t *dst;
+    uint32_t bytes;
+    if (!locate(k, src, dst, bytes)) return;
+    mbar_arrive_expect_tx(&bars[s], bytes);
+    bulk_load(stages + s * kCopyPiece, src, bytes, &bars[s]);
+    loaded |= 1u << s;
+  };
+  for (int64_t k = 0; k < min(static_cast<int64_t>(kCopyStages), n); ++k) load(k);
+  bool ok = true;
+  for (int64_t k = 0; ok && k < n; ++k) {
+    const int s = static_cast<int>(k % kCopyStages);
+    if (loaded & (1u << s)) {
+      ok = mbar_wait_bounded(&bars[s], (phase >> s) & 1u, p0 + k);
+      if (!ok) break;
+      phase ^= 1u << s;
+      loaded &= ~(1u << s);
+      const uint8_t *src;
+      uint8_t *dst;
+      uint32_t bytes;
+      locate(k, src, dst, bytes);
+      bulk_store(dst, stages + s * kCopyPiece, bytes);
+    }
+    bulk_commit();  // one group per piece (empty for a skipped one)
+    // the stage of piece k - kCopyLag takes the piece kCopyStages after it,
+    // once that piece's store has read the stage
+    if (k >= kCopyLag && k - kCopyLag + kCopyStages < n) {
+      bulk_wait_read<kCopyLag>();
+      load(k - kCopyLag + kCopyStages);
+    }
+  }
+  if (!ok) {  // a load never landed: let the others land before leaving
+    for (int s = 0; s < kCopyStages; ++s)
+      if (loaded & (1u << s)) (void)mbar_wait_bounded(&bars[s], (phase >> s) & 1u, p0);
+  }
+  bulk_wait_all();  // stores complete (and the stages read) before the CTA ends
+}
+
+cudaError_t launch_kv_copy(void *const *caches, int num_layers, const int64_t *pairs,
+                           int64_t num_pairs, const Geometry &g, cudaStream_t stream) {
+  DeviceInfo dev;
+  cudaError_t e = current_device_info(&dev);
+  if (e != cudaSuccess) return e;
+  LayerPtrs lp;
+  for (int l = 0; l < kMaxLayers; ++l)
+    lp.p[l] = l < num_layers ? static_cast<uint8_t *>(caches[l]) : nullptr;
+  const int64_t pph = (g.block_bytes + kCopyPiece - 1) / kCopyPiece;
+  const int64_t total = num_pairs * num_layers * 2 * pph;
+  e = cudaFuncSetAttribute(kv_copy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kCopySmem);
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(std::min<int64_t>(total, dev.sms));
+  kv_copy_kernel<<<grid, 32, kCopySmem, stream>>>(lp, pairs, num_layers, g.num_blocks,
+                                                  g.block_bytes, pph, total);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// kv_swap_blocks: the pair list is host memory, so it travels in the kernel's
+// parameter space (kSwapChunk pairs per launch, already range-checked on
+// the host).  CTA (k, half) moves block src[k] -> dst[k] of that half.
+// One side is normally pinned host memory reached over the chip-to-host
+// link; the many outstanding 16-byte requests of 256 threads x UNROLL keep
+// the link busy.
+// ---------------------------------------------------------------------------
+constexpr int kSwapChunk = 1536;
 template <int UNROLL>
 __device__ __forceinline__ void copy_chunks(uint4 *__restrict__ dst, const uint4 *__restrict__ src,
                                             int64_t n) {
@@ -137,50 +297,6 @@ __device__ __forceinline__ void copy_chunks(uint4 *__restrict__ dst, const uint4
   for (; c < n; c += blockDim.x) dst[c] = src[c];
 }
 
-__global__ void __launch_bounds__(256)
-kv_copy_kernel(const __grid_constant__ LayerPtrs caches, const int64_t *__restrict__ pairs,
-               int64_t num_blocks, int64_t block_chunks) {
-  const int64_t pair = blockIdx.x;
-  const int layer = blockIdx.y;
-  const int64_t s = __ldg(pairs + 2 * pair);
-  const int64_t d = __ldg(pairs + 2 * pair + 1);
-  if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
-    if (threadIdx.x == 0) record_error(PKV_ERR_BOUNDS, pair);
-    return;
-  }
-  uint4 *base = caches.p[layer];
-  const int64_t half = num_blocks * block_chunks;
-  copy_chunks<4>(base + d * block_chunks, base + s * block_chunks, block_chunks);
-  copy_chunks<4>(base + half + d * block_chunks, base + half + s * block_chunks, block_chunks);
-}
-
-cudaError_t launch_kv_copy(void *const *caches, int num_layers, const int64_t *pairs,
-                           int64_t num_pairs, const Geometry &g, cudaStream_t stream) {
-  LayerPtrs lp;
-  for (int l = 0; l < kMaxLayers; ++l)
-    lp.p[l] = l < num_layers ? static_cast<uint4 *>(caches[l]) : nullptr;
-  const int64_t block_chunks = g.block_bytes / 16;
-  // grid.x may go up to 2^31-1: pairs beyond that are split over launches
-  const int64_t max_x = 0x7fffffff;
-  for (int64_t a = 0; a < num_pairs; a += max_x) {
-    const int64_t n = std::min(max_x, num_pairs - a);
-    dim3 grid(static_cast<unsigned>(n), num_layers);
-    kv_copy_kernel<<<grid, 256, 0, stream>>>(lp, pairs + 2 * a, g.num_blocks, block_chunks);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
-
-// ---------------------------------------------------------------------------
-// kv_swap_blocks: the pair list is host memory, so it travels in the kernel's
-// parameter space (kSwapChunk pairs per launch, already range-checked on
-// the host).  CTA (k, half) moves block src[k] -> dst[k] of that half.
-// One side is normally pinned host memory reached over the chip-to-host
-// link; the many outstanding 16-byte requests of 256 threads x UNROLL keep
-// the link busy.
-// ---------------------------------------------------------------------------
-constexpr int kSwapChunk = 1536;
 struct SwapPairs {
   int32_t src[kSwapChunk];
   int32_t dst[kSwapChunk];

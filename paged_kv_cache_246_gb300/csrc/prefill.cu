@@ -117,8 +117,7 @@ struct Lay {
                        B_Q2 = B_FIN + 1, B_QS = B_Q2 + 2, B_K8F = B_QS + 2, B_V8F = B_K8F + N8K,
                        B_E8K = B_V8F + N8V, B_E8V = B_E8K + N8K, NBAR = B_E8V + N8V;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_RAMP = OFF_MISC + 64;  // fp32 0, 1, .., BN-1 (ALiBi key offsets)
-  static constexpr int BYTES = OFF_RAMP + BN * 4;
+  static constexpr int BYTES = OFF_MISC + 64;
   // + alignment slack; at least ~118 KB so that one CTA owns an SM (and all
   // of its tensor memory)
   static constexpr int ALLOC = (BYTES + 1024) > 118 * 1024 ? (BYTES + 1024) : 118 * 1024;
@@ -263,8 +262,6 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     prefetch_tensormap(&qmap);
     prefetch_tensormap(&kvmap);
   }
-  if (ALIBI && threadIdx.x < BN)
-    reinterpret_cast<float *>(smem + L::OFF_RAMP)[threadIdx.x] = static_cast<float>(threadIdx.x);
   if (warp == 1) tc5::tmem_alloc<512>(misc);
   tc5::fence_before_sync();
   __syncthreads();
@@ -623,42 +620,32 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
         f2unpack(fadd2(fadd2(ps2[0], ps2[1]), fadd2(ps2[2], ps2[3])), ps0, ps1);
         return ps0 + ps1;
       };
-      // ALiBi: p = 2^(s * sl2 + slope * e + A) for the tile's key offsets
-      // e = j - kv0 (read from the shared ramp), A = slope * (kv0 - i) - mu:
-      // the bias is folded into the exponent's FMA, raw scores untouched.
+      // ALiBi: p = 2^(s * sl2 + (slope * e + A)) for the tile's key offsets
+      // e = j - kv0, A = slope * (kv0 - i) - mu: the bias is folded into the
+      // exponent's FMA (its terms from immediate offsets), raw untouched.
       auto exps_alibi = [&](float A) -> float {
-        const unsigned long long mul2 = f2pack(sl2, sl2), slope2 = f2pack(slope, slope),
-                                 a2 = f2pack(A, A);
-        const float4 *ramp = reinterpret_cast<const float4 *>(smem + L::OFF_RAMP);
-        unsigned long long ps2[4] = {0ull, 0ull, 0ull, 0ull};
+        const unsigned long long mul2 = f2pack(sl2, sl2);
+        unsigned long long ps2[2] = {0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 r = ramp[(32 * c + e) / 4];
-            const unsigned long long b01 = ffma2(slope2, f2pack(r.x, r.y), a2);
-            const unsigned long long b23 = ffma2(slope2, f2pack(r.z, r.w), a2);
-            float x0, x1, x2, x3;
-            f2unpack(ffma2(f2pack(__uint_as_float(raw[32 * c + e]),
-                                  __uint_as_float(raw[32 * c + e + 1])),
-                           mul2, b01),
+          for (int e = 0; e < 32; e += 2) {
+            const int col = 32 * c + e;
+            const float b0 = fmaf(slope, static_cast<float>(col), A);
+            const float b1 = fmaf(slope, static_cast<float>(col + 1), A);
+            float x0, x1;
+            f2unpack(ffma2(f2pack(__uint_as_float(raw[col]), __uint_as_float(raw[col + 1])),
+                           mul2, f2pack(b0, b1)),
                      x0, x1);
-            f2unpack(ffma2(f2pack(__uint_as_float(raw[32 * c + e + 2]),
-                                  __uint_as_float(raw[32 * c + e + 3])),
-                           mul2, b23),
-                     x2, x3);
             const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            const float p2 = fast_exp2(x2), p3 = fast_exp2(x3);
-            ps2[(e / 2) & 3] = fadd2(ps2[(e / 2) & 3], f2pack(p0, p1));
-            ps2[(e / 2 + 1) & 3] = fadd2(ps2[(e / 2 + 1) & 3], f2pack(p2, p3));
+            ps2[(e / 2) & 1] = fadd2(ps2[(e / 2) & 1], f2pack(p0, p1));
             pk[e / 2] = OPT::from_f2(p0, p1);
-            pk[e / 2 + 1] = OPT::from_f2(p2, p3);
           }
           tc5::tmem_st16(sb + 16 * c, pk);
         }
         float ps0, ps1;
-        f2unpack(fadd2(fadd2(ps2[0], ps2[1]), fadd2(ps2[2], ps2[3])), ps0, ps1);
+        f2unpack(fadd2(ps2[0], ps2[1]), ps0, ps1);
         return ps0 + ps1;
       };
       // The reference m moves lazily, so the tile's max only decides
@@ -679,12 +666,11 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
         if constexpr (ALIBI) {
           // x = s * scale * log2e + slope * log2e * (j - i), in pairs
           const float b0 = slope * static_cast<float>(kv0 - pos);
-          const unsigned long long sl2x2 = f2pack(sl2, sl2), slope2 = f2pack(slope, slope),
-                                   b0x2 = f2pack(b0, b0);
+          const unsigned long long sl2x2 = f2pack(sl2, sl2);
 #pragma unroll
           for (int e = 0; e < BN; e += 2) {
-            const unsigned long long bias =
-                ffma2(slope2, f2pack(static_cast<float>(e), static_cast<float>(e + 1)), b0x2);
+            const unsigned long long bias = f2pack(fmaf(slope, static_cast<float>(e), b0),
+                                                   fmaf(slope, static_cast<float>(e + 1), b0));
             float v0, v1;
             f2unpack(ffma2(f2pack(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1])), sl2x2,
                            bias),

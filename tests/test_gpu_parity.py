@@ -364,6 +364,41 @@ def test_copy_blocks_bit_exact_all_layers():
         assert torch.equal(got.cpu().view(torch.int16), ref.view(torch.int16))
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_copy_blocks_many_pairs_ragged_pieces(fp8):
+    """Blocks of 24 KiB (bs 32 x 3 KV heads x 128 dims x 2 B; 12 KiB of codes
+    over an fp8 cache) cut into a full and a partial piece, 700 pairs over 2
+    layers (several ring turns per CTA), and one bad pair in the middle:
+    recorded, skipped, every other pair copied bit-exactly."""
+    g = torch.Generator().manual_seed(63)
+    w = small(63, H=6, KVH=3, bs=32, seq_lens=[40], num_blocks=1500)
+    dt = torch.uint8 if fp8 else w.dtype
+    layers = []
+    for _ in range(2):
+        L = torch.empty(w.kv_cache.shape, dtype=dt)
+        if fp8:
+            L.copy_(torch.randint(0, 256, L.shape, generator=g, dtype=torch.uint8))
+        else:
+            L.view(-1).copy_(torch.randn(L.numel(), generator=g).to(L.dtype))
+        layers.append(L)
+    perm = torch.randperm(1500, generator=g)
+    pairs = torch.stack([perm[:700], perm[700:1400]], 1).to(torch.int64)
+    bad = 333
+    pairs[bad, 0] = 1500 + 9                      # source beyond the pool
+    dev_layers = [L.to(DEV) for L in layers]
+    r = CudaRun(w)
+    p = B.make_params(6, 3, 128, 32, w.dtype, w.scale, kv_cache_dtype="fp8_e4m3", k_scale=0.02,
+                      v_scale=0.02) if fp8 else r.p
+    B.kv_copy_blocks(dev_layers, pairs.to(DEV), p)
+    torch.cuda.synchronize()
+    st, detail = B.device_error()
+    assert st == B.PKV_ERR_BOUNDS and detail == bad
+    good = torch.cat([pairs[:bad], pairs[bad + 1:]]).tolist()
+    O.kv_copy_blocks(layers, good)
+    for got, ref in zip(dev_layers, layers):
+        assert torch.equal(got.cpu().view(torch.uint8), ref.view(torch.uint8))
+
+
 def test_swap_round_trip_pinned_host():
     w = small(61, seq_lens=[300, 200], num_blocks=64)
     r = CudaRun(w)
