@@ -192,61 +192,64 @@ kv_copy_kernel(const __grid_constant__ LayerPtrs caches, const int64_t *__restri
   for (int s = 0; s < kCopyStages; ++s) mbar_init(&bars[s], 1);
   fence_mbar_init();
 
-  // source, destination and size of piece k of this CTA; false for a bad
-  // pair (recorded, never dereferenced)
-  auto locate = [&](int64_t k, const uint8_t *&src, uint8_t *&dst, uint32_t &bytes) -> bool {
-    const int64_t p = p0 + k;
-    const int64_t hb = p / pieces_per_half;
-    const int64_t part = p - hb * pieces_per_half;
-    const int64_t pl = hb >> 1;
-    const int layer = static_cast<int>(pl % num_layers);
-    const int64_t pair = pl / num_layers;
-    const int64_t s = __ldg(pairs + 2 * pair), d = __ldg(pairs + 2 * pair + 1);
-    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
-      record_error(PKV_ERR_BOUNDS, pair);
-      return false;
-    }
-    const int64_t off = part * kCopyPiece;
-    bytes = static_cast<uint32_t>(min(static_cast<int64_t>(kCopyPiece), block_bytes - off));
-    uint8_t *base = caches.p[layer] + (hb & 1) * num_blocks * block_bytes;
-    src = base + s * block_bytes + off;
-    dst = base + d * block_bytes + off;
-    return true;
-  };
+  // Pieces are walked in order: (pair, layer, half, part) advance like an
+  // odometer from this CTA's first piece, so no division is done per piece.
+  // The destination and size of the piece in each stage wait in shared
+  // memory for its store.
+  __shared__ uint8_t *st_dst[kCopyStages];
+  __shared__ uint32_t st_bytes[kCopyStages];
+  int64_t part = p0 % pieces_per_half, hb = p0 / pieces_per_half;
+  int half = static_cast<int>(hb & 1);
+  int layer = static_cast<int>((hb >> 1) % num_layers);
+  int64_t pair = (hb >> 1) / num_layers;
   uint32_t loaded = 0;  // bit s: stage s has a load in flight (or landed, not stored)
   uint32_t phase = 0;   // bit s: parity of stage s's next completion
-  auto load = [&](int64_t k) {
-    const int s = static_cast<int>(k % kCopyStages);
-    const uint8_t *src;
-    uint8_t *dst;
-    uint32_t bytes;
-    if (!locate(k, src, dst, bytes)) return;
-    mbar_arrive_expect_tx(&bars[s], bytes);
-    bulk_load(stages + s * kCopyPiece, src, bytes, &bars[s]);
-    loaded |= 1u << s;
+  // load the next piece of the walk into stage s (bad pair: recorded, skipped)
+  auto load_next = [&](int s) {
+    const int64_t src_b = __ldg(pairs + 2 * pair), dst_b = __ldg(pairs + 2 * pair + 1);
+    if (src_b < 0 || src_b >= num_blocks || dst_b < 0 || dst_b >= num_blocks) {
+      record_error(PKV_ERR_BOUNDS, pair);
+    } else {
+      const int64_t off = part * kCopyPiece;
+      const uint32_t bytes =
+          static_cast<uint32_t>(min(static_cast<int64_t>(kCopyPiece), block_bytes - off));
+      uint8_t *base = caches.p[layer] + half * num_blocks * block_bytes + off;
+      st_dst[s] = base + dst_b * block_bytes;
+      st_bytes[s] = bytes;
+      mbar_arrive_expect_tx(&bars[s], bytes);
+      bulk_load(stages + s * kCopyPiece, base + src_b * block_bytes, bytes, &bars[s]);
+      loaded |= 1u << s;
+    }
+    if (++part == pieces_per_half) {
+      part = 0;
+      half ^= 1;
+      if (half == 0 && ++layer == num_layers) {
+        layer = 0;
+        ++pair;
+      }
+    }
   };
-  for (int64_t k = 0; k < min(static_cast<int64_t>(kCopyStages), n); ++k) load(k);
+  for (int64_t k = 0; k < min(static_cast<int64_t>(kCopyStages), n); ++k)
+    load_next(static_cast<int>(k));
   bool ok = true;
+  int s = 0;  // stage of piece k
   for (int64_t k = 0; ok && k < n; ++k) {
-    const int s = static_cast<int>(k % kCopyStages);
     if (loaded & (1u << s)) {
       ok = mbar_wait_bounded(&bars[s], (phase >> s) & 1u, p0 + k);
       if (!ok) break;
       phase ^= 1u << s;
       loaded &= ~(1u << s);
-      const uint8_t *src;
-      uint8_t *dst;
-      uint32_t bytes;
-      locate(k, src, dst, bytes);
-      bulk_store(dst, stages + s * kCopyPiece, bytes);
+      bulk_store(st_dst[s], stages + s * kCopyPiece, st_bytes[s]);
     }
     bulk_commit();  // one group per piece (empty for a skipped one)
     // the stage of piece k - kCopyLag takes the piece kCopyStages after it,
     // once that piece's store has read the stage
     if (k >= kCopyLag && k - kCopyLag + kCopyStages < n) {
       bulk_wait_read<kCopyLag>();
-      load(k - kCopyLag + kCopyStages);
+      const int r = s >= kCopyLag ? s - kCopyLag : s - kCopyLag + kCopyStages;
+      load_next(r);
     }
+    s = s + 1 == kCopyStages ? 0 : s + 1;
   }
   if (!ok) {  // a load never landed: let the others land before leaving
     for (int s = 0; s < kCopyStages; ++s)
