@@ -132,149 +132,69 @@ cudaError_t launch_kv_write(const void *key, const void *value, int64_t num_toke
 }
 
 // ---------------------------------------------------------------------------
-// kv_copy_blocks: bulk copies through shared memory.  The work is cut into
-// pieces of up to kCopyPiece bytes, index ((pair * layers + layer) * 2 +
-// half) * pieces_per_half + part, and CTA c takes the contiguous range
-// [c * P / G, (c + 1) * P / G) of the P pieces (G CTAs, one per SM), so
-// every CTA moves the same bytes to within one piece.  One thread per CTA
-// streams them through a ring of kCopyStages shared-memory stages:
-// cp.async.bulk loads (completed on an mbarrier each) and cp.async.bulk
-// stores back out.  A store reads its stage only as it drains towards
-// memory, so a stage is refilled kCopyLag pieces after its store was issued:
-// about kCopyLag stores and kCopyStages - kCopyLag loads stay in flight.
+// kv_copy_blocks: CTA (piece, pair, layer) copies piece `piece` (16 KiB, or
+// the rest) of both halves of one block: 256 threads x kCopyUnroll 16-byte
+// chunks in flight per half.  Short CTAs keep the tail of the grid short.
 // ---------------------------------------------------------------------------
 constexpr int kMaxLayers = 256;
 struct LayerPtrs {
-  uint8_t *p[kMaxLayers];
+  uint4 *p[kMaxLayers];
 };
-constexpr int kCopyStages = 12;
-constexpr int kCopyLag = 6;
-constexpr int kCopyPiece = 16384;
-constexpr int kCopySmem = kCopyStages * kCopyPiece + 128;
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+constexpr int kCopyPieceChunks = kCopyThreads * kCopyUnroll;  // 16 KiB
 
-__device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint32_t bytes,
-                                          uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_u32(smem_dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void bulk_store(void *dst, const void *smem_src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-               "r"(smem_u32(smem_src)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// all but the newest N committed groups have finished reading shared memory
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// every committed group has completed
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-__global__ void __launch_bounds__(32, 1)
+__global__ void __launch_bounds__(kCopyThreads)
 kv_copy_kernel(const __grid_constant__ LayerPtrs caches, const int64_t *__restrict__ pairs,
-               int num_layers, int64_t num_blocks, int64_t block_bytes, int64_t pieces_per_half,
-               int64_t total_pieces) {
-  extern __shared__ uint8_t copy_smem_raw[];
-  __shared__ uint64_t bars[kCopyStages];
-  if (threadIdx.x != 0) return;
-  uint8_t *stages = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(copy_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-  const int64_t p0 = total_pieces * blockIdx.x / gridDim.x;
-  const int64_t n = total_pieces * (blockIdx.x + 1) / gridDim.x - p0;
-  for (int s = 0; s < kCopyStages; ++s) mbar_init(&bars[s], 1);
-  fence_mbar_init();
-
-  // Pieces are walked in order: (pair, layer, half, part) advance like an
-  // odometer from this CTA's first piece, so no division is done per piece.
-  // The destination and size of the piece in each stage wait in shared
-  // memory for its store.
-  __shared__ uint8_t *st_dst[kCopyStages];
-  __shared__ uint32_t st_bytes[kCopyStages];
-  int64_t part = p0 % pieces_per_half, hb = p0 / pieces_per_half;
-  int half = static_cast<int>(hb & 1);
-  int layer = static_cast<int>((hb >> 1) % num_layers);
-  int64_t pair = (hb >> 1) / num_layers;
-  uint32_t loaded = 0;  // bit s: stage s has a load in flight (or landed, not stored)
-  uint32_t phase = 0;   // bit s: parity of stage s's next completion
-  // load the next piece of the walk into stage s (bad pair: recorded, skipped)
-  auto load_next = [&](int s) {
-    const int64_t src_b = __ldg(pairs + 2 * pair), dst_b = __ldg(pairs + 2 * pair + 1);
-    if (src_b < 0 || src_b >= num_blocks || dst_b < 0 || dst_b >= num_blocks) {
-      record_error(PKV_ERR_BOUNDS, pair);
-    } else {
-      const int64_t off = part * kCopyPiece;
-      const uint32_t bytes =
-          static_cast<uint32_t>(min(static_cast<int64_t>(kCopyPiece), block_bytes - off));
-      uint8_t *base = caches.p[layer] + half * num_blocks * block_bytes + off;
-      st_dst[s] = base + dst_b * block_bytes;
-      st_bytes[s] = bytes;
-      mbar_arrive_expect_tx(&bars[s], bytes);
-      bulk_load(stages + s * kCopyPiece, base + src_b * block_bytes, bytes, &bars[s]);
-      loaded |= 1u << s;
-    }
-    if (++part == pieces_per_half) {
-      part = 0;
-      half ^= 1;
-      if (half == 0 && ++layer == num_layers) {
-        layer = 0;
-        ++pair;
-      }
-    }
-  };
-  for (int64_t k = 0; k < min(static_cast<int64_t>(kCopyStages), n); ++k)
-    load_next(static_cast<int>(k));
-  bool ok = true;
-  int s = 0;  // stage of piece k
-  for (int64_t k = 0; ok && k < n; ++k) {
-    if (loaded & (1u << s)) {
-      ok = mbar_wait_bounded(&bars[s], (phase >> s) & 1u, p0 + k);
-      if (!ok) break;
-      phase ^= 1u << s;
-      loaded &= ~(1u << s);
-      bulk_store(st_dst[s], stages + s * kCopyPiece, st_bytes[s]);
-    }
-    bulk_commit();  // one group per piece (empty for a skipped one)
-    // the stage of piece k - kCopyLag takes the piece kCopyStages after it,
-    // once that piece's store has read the stage
-    if (k >= kCopyLag && k - kCopyLag + kCopyStages < n) {
-      bulk_wait_read<kCopyLag>();
-      const int r = s >= kCopyLag ? s - kCopyLag : s - kCopyLag + kCopyStages;
-      load_next(r);
-    }
-    s = s + 1 == kCopyStages ? 0 : s + 1;
+               int64_t first_pair, int64_t num_blocks, int64_t block_chunks) {
+  const int64_t pair = first_pair + blockIdx.y;
+  const int layer = blockIdx.z;
+  const int64_t s = __ldg(pairs + 2 * pair);
+  const int64_t d = __ldg(pairs + 2 * pair + 1);
+  if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) record_error(PKV_ERR_BOUNDS, pair);
+    return;
   }
-  if (!ok) {  // a load never landed: let the others land before leaving
-    for (int s = 0; s < kCopyStages; ++s)
-      if (loaded & (1u << s)) (void)mbar_wait_bounded(&bars[s], (phase >> s) & 1u, p0);
+  const int64_t half = num_blocks * block_chunks;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kCopyPieceChunks + threadIdx.x;
+  const uint4 *src = caches.p[layer] + s * block_chunks;
+  uint4 *dst = caches.p[layer] + d * block_chunks;
+  uint4 r[2][kCopyUnroll];
+#pragma unroll
+  for (int u = 0; u < kCopyUnroll; ++u) {
+    const int64_t c = c0 + u * kCopyThreads;
+    if (c < block_chunks) {
+      r[0][u] = src[c];
+      r[1][u] = src[half + c];
+    }
   }
-  bulk_wait_all();  // stores complete (and the stages read) before the CTA ends
+#pragma unroll
+  for (int u = 0; u < kCopyUnroll; ++u) {
+    const int64_t c = c0 + u * kCopyThreads;
+    if (c < block_chunks) {
+      dst[c] = r[0][u];
+      dst[half + c] = r[1][u];
+    }
+  }
 }
 
 cudaError_t launch_kv_copy(void *const *caches, int num_layers, const int64_t *pairs,
                            int64_t num_pairs, const Geometry &g, cudaStream_t stream) {
-  DeviceInfo dev;
-  cudaError_t e = current_device_info(&dev);
-  if (e != cudaSuccess) return e;
   LayerPtrs lp;
   for (int l = 0; l < kMaxLayers; ++l)
-    lp.p[l] = l < num_layers ? static_cast<uint8_t *>(caches[l]) : nullptr;
-  const int64_t pph = (g.block_bytes + kCopyPiece - 1) / kCopyPiece;
-  const int64_t total = num_pairs * num_layers * 2 * pph;
-  e = cudaFuncSetAttribute(kv_copy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kCopySmem);
-  if (e != cudaSuccess) return e;
-  const int grid = static_cast<int>(std::min<int64_t>(total, dev.sms));
-  kv_copy_kernel<<<grid, 32, kCopySmem, stream>>>(lp, pairs, num_layers, g.num_blocks,
-                                                  g.block_bytes, pph, total);
-  return cudaGetLastError();
+    lp.p[l] = l < num_layers ? static_cast<uint4 *>(caches[l]) : nullptr;
+  const int64_t block_chunks = g.block_bytes / 16;
+  const unsigned pieces = static_cast<unsigned>((block_chunks + kCopyPieceChunks - 1) / kCopyPieceChunks);
+  // grid.y may go up to 65535: pairs beyond that are split over launches
+  const int64_t max_y = 65535;
+  for (int64_t a = 0; a < num_pairs; a += max_y) {
+    const int64_t n = std::min(max_y, num_pairs - a);
+    dim3 grid(pieces, static_cast<unsigned>(n), num_layers);
+    kv_copy_kernel<<<grid, kCopyThreads, 0, stream>>>(lp, pairs, a, g.num_blocks, block_chunks);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // ---------------------------------------------------------------------------
