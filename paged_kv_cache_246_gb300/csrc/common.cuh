@@ -184,6 +184,22 @@ __device__ __forceinline__ uint2 e4m3x4_to_h4(uint32_t u) {
   return r;
 }
 
+// Four floats (first in the low byte) as E4M3 codes, nearest even,
+// saturating: hi; and the codes of what hi leaves over: lo.
+__device__ __forceinline__ void split_e4m3x4(float v0, float v1, float v2, float v3, uint32_t &hi,
+                                             uint32_t &lo) {
+  auto pack = [](float a, float b, float c, float d) -> uint32_t {
+    uint16_t p01, p23;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(p01) : "f"(a), "f"(b));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(p23) : "f"(c), "f"(d));
+    return static_cast<uint32_t>(p01) | (static_cast<uint32_t>(p23) << 16);
+  };
+  hi = pack(v0, v1, v2, v3);
+  const uint2 h = e4m3x4_to_h4(hi);  // exact: every E4M3 value is an fp16 value
+  const float2 f01 = FP16::to_f2(h.x), f23 = FP16::to_f2(h.y);
+  lo = pack(v0 - f01.x, v1 - f01.y, v2 - f23.x, v3 - f23.y);
+}
+
 // Packed fp32 pairs (Blackwell f32x2 FMA/ADD/MUL) and the 3-input max: the
 // attention inner loops are instruction-bound, and the packed forms halve
 // their per-element arithmetic.

@@ -251,22 +251,6 @@ __device__ __forceinline__ void mma16832_e4m3_top(float (&d)[2], uint32_t a0, ui
       : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
 }
 
-// Four floats (first in the low byte) as E4M3 codes, nearest even,
-// saturating: hi; and the codes of what hi leaves over: lo.
-__device__ __forceinline__ void split_e4m3x4(float v0, float v1, float v2, float v3, uint32_t &hi,
-                                             uint32_t &lo) {
-  auto pack = [](float a, float b, float c, float d) -> uint32_t {
-    uint16_t p01, p23;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(p01) : "f"(a), "f"(b));
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(p23) : "f"(c), "f"(d));
-    return static_cast<uint32_t>(p01) | (static_cast<uint32_t>(p23) << 16);
-  };
-  hi = pack(v0, v1, v2, v3);
-  const uint2 h = e4m3x4_to_h4(hi);  // exact: every E4M3 value is an fp16 value
-  const float2 f01 = FP16::to_f2(h.x), f23 = FP16::to_f2(h.y);
-  lo = pack(v0 - f01.x, v1 - f01.y, v2 - f23.x, v3 - f23.y);
-}
-
 // Bytes {a.b[j], b.b[j], a.b[j+1], b.b[j+1]} for j = 0 (even m-tile) or 2.
 __device__ __forceinline__ uint32_t interleave2(uint32_t a, uint32_t b, int j) {
   uint32_t r;

@@ -19,7 +19,7 @@
 //               128-byte swizzle) per cache block and 64-dim half, straight
 //               from the paged cache.  Blocks outside the visible range are
 //               loaded from an out-of-range coordinate, which the TMA unit
-//               zero-fills.  K has 3 stages and V 2, each freed by its own
+//               zero-fills.  K and V have 2 stages each, each freed by its own
 //               barrier (a K stage when its QK products are done, a V stage
 //               when its PV products are done), and the next tile's
 //               block-table entries are fetched one tile ahead, so copies
@@ -89,7 +89,7 @@ struct PrefillArgs {
 namespace pf {
 
 constexpr int BM = 128, BN = 128;
-constexpr int NSTK = 3, NSTV = 2;  // K and V pipeline stages
+constexpr int NSTK = 2, NSTV = 2;  // K and V pipeline stages (a third K stage measured no faster)
 constexpr int kThreads = 384;
 
 template <int D, bool KV8 = false>
@@ -98,20 +98,21 @@ struct Lay {
   static constexpr int NREG = D / 64;
   static constexpr int TILE = REG * NREG;
   static constexpr int TILE8 = BN * D;  // one key tile of 8-bit codes
-  // 16-bit K / V stages.  Over an fp8 cache fewer (one K stage: a key tile
-  // is widened a full step before its QK products are issued), plus N8K /
-  // N8V staging areas for the K / V tiles' codes, each refilled as soon as
-  // its codes have been widened.
-  static constexpr int NK = KV8 ? 1 : NSTK, NV = KV8 ? 2 : NSTV;
-  static constexpr int N8K = 2, N8V = 2;
+  // 16-bit K / V stages.  Over an fp8 cache the K codes are the QK operand
+  // as they land (N8K staging areas, no 16-bit K stage); the V codes land in
+  // N8V staging areas, each refilled as soon as its codes were widened into
+  // one of the NV 16-bit V stages.
+  static constexpr int NK = KV8 ? 0 : NSTK, NV = KV8 ? 2 : NSTV;
+  static constexpr int N8K = 3, N8V = 2;
   static constexpr int OFF_Q = 0;  // two Q tiles
   static constexpr int OFF_K = 2 * TILE;
   static constexpr int OFF_V = OFF_K + NK * TILE;
   static constexpr int OFF_STG = OFF_V + NV * TILE;  // N8K K code tiles, then N8V V
   static constexpr int OFF_BAR = OFF_STG + (KV8 ? (N8K + N8V) * TILE8 : 0);
   // B_KF / B_VF: stage ready for the MMA; B_EK / B_EV: stage consumed by the
-  // MMA; B_K8F / B_V8F: codes landed; B_E8K / B_E8V: codes widened; B_QS:
-  // a query tile's largest magnitude gathered; B_Q2: its fp16 copy ready
+  // MMA; B_K8F / B_V8F: codes landed; B_E8K: K codes consumed by the MMA;
+  // B_E8V: V codes widened; B_QS: a query tile's largest magnitude
+  // gathered; B_Q2: its E4M3 terms ready
   static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + NK, B_EK = B_VF + NV, B_EV = B_EK + NK,
                        B_SF = B_EV + NV, B_PF = B_SF + 2, B_O = B_PF + 2, B_FIN = B_O + 2,
                        B_Q2 = B_FIN + 1, B_QS = B_Q2 + 2, B_K8F = B_QS + 2, B_V8F = B_K8F + N8K,
@@ -158,6 +159,10 @@ struct AB<FP16> {
 };
 
 
+__device__ __forceinline__ uint32_t word4(const uint4 &v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 // One query tile of the CTA: head, first row within the sequence, rows,
 // and the half-open range of the CTA's key tiles it needs.
 struct QTile {
@@ -174,8 +179,9 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
   // barriers the K / V copies complete on, and how many stages they have
   constexpr int KFT = KV8 ? L::B_K8F : L::B_KF, VFT = KV8 ? L::B_V8F : L::B_VF;
   constexpr int NKT = KV8 ? L::N8K : NK, NVT = KV8 ? L::N8V : NV;
-  // bf16 queries over an fp8 cache are rewritten as fp16 by their softmax warps
-  constexpr bool QCONV = KV8 && std::is_same<T, BF16>::value;
+  // queries over an fp8 cache are rewritten as E4M3 terms by their softmax warps
+  constexpr bool QCONV = KV8;
+  constexpr int KEB = KV8 ? L::B_E8K : L::B_EK;  // K stage consumed by its QK products
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -247,11 +253,12 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::NBAR; ++i) {
       uint32_t count = (i == L::B_PF || i == L::B_PF + 1) ? 128 : 1;
-      // the softmax warps of a tile release its fp16 queries; the stages and
-      // staging areas are released by the converter warp(s) that widen them
+      // the softmax warps of a tile release its E4M3 query terms; the V
+      // stages and V staging areas are released by the two warps that widen
+      // them (the K staging areas by an MMA commit)
       if (KV8 && (i == L::B_Q2 || i == L::B_Q2 + 1 || i == L::B_QS || i == L::B_QS + 1))
         count = 128;
-      if (KV8 && ((i >= L::B_KF && i < L::B_VF + NV) || (i >= L::B_E8K && i < L::B_E8V + L::N8V)))
+      if (KV8 && ((i >= L::B_VF && i < L::B_VF + NV) || (i >= L::B_E8V && i < L::B_E8V + L::N8V)))
         count = 64;
       mbar_init(&bars[i], count);
     }
@@ -324,30 +331,30 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
           tma_load_4d(smem + L::OFF_STG + (N8K + sv8) * L::TILE8 + lane * BS * D, &kvmap,
                       &bars[L::B_V8F + sv8], 0, g, coord, 1);
         jv = j + 1;
-        continue;
+      } else {
+        const int sk = j % NK;
+        if (j >= NK && !warp_wait(&bars[L::B_EK + sk], ((j / NK) - 1) & 1, abort_flag, where))
+          break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars[L::B_KF + sk], L::TILE);
+        __syncwarp();
+        if (lane < TB) {
+          uint8_t *kd = smem + L::OFF_K + sk * L::TILE + lane * BS * 128;
+          for (int r = 0; r < L::NREG; ++r)
+            tma_load_4d(kd + r * L::REG, &kvmap, &bars[L::B_KF + sk], 64 * r, g, coord, 0);
+        }
+        jk = j + 1;
+        const int sv = j % NV;
+        if (j >= NV && !warp_wait(&bars[L::B_EV + sv], ((j / NV) - 1) & 1, abort_flag, where))
+          break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars[L::B_VF + sv], L::TILE);
+        __syncwarp();
+        if (lane < TB) {
+          uint8_t *vd = smem + L::OFF_V + sv * L::TILE + lane * BS * 128;
+          for (int r = 0; r < L::NREG; ++r)
+            tma_load_4d(vd + r * L::REG, &kvmap, &bars[L::B_VF + sv], 64 * r, g, coord, 1);
+        }
+        jv = j + 1;
       }
-      const int sk = j % NK;
-      if (j >= NK && !warp_wait(&bars[L::B_EK + sk], ((j / NK) - 1) & 1, abort_flag, where))
-        break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[L::B_KF + sk], L::TILE);
-      __syncwarp();
-      if (lane < TB) {
-        uint8_t *kd = smem + L::OFF_K + sk * L::TILE + lane * BS * 128;
-        for (int r = 0; r < L::NREG; ++r)
-          tma_load_4d(kd + r * L::REG, &kvmap, &bars[L::B_KF + sk], 64 * r, g, coord, 0);
-      }
-      jk = j + 1;
-      const int sv = j % NV;
-      if (j >= NV && !warp_wait(&bars[L::B_EV + sv], ((j / NV) - 1) & 1, abort_flag, where))
-        break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[L::B_VF + sv], L::TILE);
-      __syncwarp();
-      if (lane < TB) {
-        uint8_t *vd = smem + L::OFF_V + sv * L::TILE + lane * BS * 128;
-        for (int r = 0; r < L::NREG; ++r)
-          tma_load_4d(vd + r * L::REG, &kvmap, &bars[L::B_VF + sv], 64 * r, g, coord, 1);
-      }
-      jv = j + 1;
     }
     if (lane == 0) {
       misc[2] = static_cast<uint32_t>(jk);
@@ -358,12 +365,17 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     // One thread: the tensor core's instruction queue is shallow, so every
     // cycle this thread spends outside an MMA is a cycle the tensor core may
     // idle.  Waits are scalar; there is no warp-wide synchronisation here.
-    constexpr uint32_t ID_QK = tc5::idesc_f16(AB<OPT>::v, 0, BM, BN);
+    // QK over an fp8 cache: kind::f8f6f4, E4M3 query terms x E4M3 key codes
+    constexpr uint32_t ID_QK = tc5::idesc_f16(KV8 ? 0 : AB<OPT>::v, 0, BM, BN);
     constexpr uint32_t ID_PV = tc5::idesc_f16(AB<OPT>::v, 1, BM, D);
     // Operand descriptors are built once; an MMA only adds a compile-time
-    // offset (in 16-byte units) to a base.
-    const uint64_t q_desc = tc5::sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
-    const uint64_t k_desc = tc5::sdesc_sw128(sbase + L::OFF_K, 16, 1024);
+    // offset (in 16-byte units) to a base.  8-bit operands are K-major rows
+    // of D bytes: 128-byte swizzle for D = 128, 64-byte for D = 64.
+    auto sdesc8 = [&](uint32_t off) -> uint64_t {
+      return D == 128 ? tc5::sdesc_sw128(sbase + off, 16, 1024) : tc5::sdesc_sw64(sbase + off, 16, 512);
+    };
+    const uint64_t q_desc = KV8 ? sdesc8(L::OFF_Q) : tc5::sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
+    const uint64_t k_desc = KV8 ? sdesc8(L::OFF_STG) : tc5::sdesc_sw128(sbase + L::OFF_K, 16, 1024);
     const uint64_t v_desc = tc5::sdesc_sw128(sbase + L::OFF_V, L::REG, 1024);
     const int j0A = qt[0].j0, j1A = qt[0].j1, j0B = qt[1].j0, j1B = qt[1].j1;
     auto active = [&](int x, int j) {
@@ -373,7 +385,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     int k_ready = -1;  // highest key tile known to have landed
     auto need_k = [&](int j) -> bool {
       if (j <= k_ready) return true;
-      if (!wait_or_abort(&bars[L::B_KF + j % NK], (j / NK) & 1, abort_flag, where))
+      if (!wait_or_abort(&bars[KFT + j % NKT], (j / NKT) & 1, abort_flag, where))
         return false;
       tc5::fence_after_sync();
       k_ready = j;
@@ -381,12 +393,23 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     };
     auto qk = [&](int x, int j) {
       const uint64_t qb = q_desc + static_cast<uint64_t>((x * L::TILE) >> 4);
-      const uint64_t kb = k_desc + static_cast<uint64_t>(((j % NK) * L::TILE) >> 4);
       const uint32_t sb = tmem + x * 128;
+      if constexpr (KV8) {
+        // S = Q_hi K^T + Q_lo K^T, 32 codes (32 bytes) per k-step
+        const uint64_t kb = k_desc + static_cast<uint64_t>(((j % L::N8K) * L::TILE8) >> 4);
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint64_t off = static_cast<uint64_t>(((k / 4) * L::REG + (k % 4) * 32) >> 4);
-        tc5::mma_ss(sb, qb + off, kb + off, ID_QK, k > 0 ? 1u : 0u);
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k)
+            tc5::mma_ss_f8(sb, qb + static_cast<uint64_t>((t * BM * D + k * 32) >> 4),
+                           kb + static_cast<uint64_t>(k * 2), ID_QK, (t | k) ? 1u : 0u);
+      } else {
+        const uint64_t kb = k_desc + static_cast<uint64_t>(((j % NK) * L::TILE) >> 4);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t off = static_cast<uint64_t>(((k / 4) * L::REG + (k % 4) * 32) >> 4);
+          tc5::mma_ss(sb, qb + off, kb + off, ID_QK, k > 0 ? 1u : 0u);
+        }
       }
       tc5::commit(&bars[L::B_SF + x]);
     };
@@ -397,7 +420,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       if (ok) {
         if (active(0, 0)) qk(0, 0);
         if (active(1, 0)) qk(1, 0);
-        tc5::commit(&bars[L::B_EK + 0]);  // K(0) free once its QKs finish
+        tc5::commit(&bars[KEB + 0]);  // K(0) free once its QKs finish
       }
     }
     int pf_a = 0, pf_b = 0;  // P tiles consumed per query tile
@@ -442,7 +465,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       }
       if (!step(0, j, sv, pf_a) || !step(1, j, sv, pf_b)) break;
       tc5::commit(&bars[L::B_EV + sv]);                                  // V(j) after its PVs
-      if (j + 1 < ntiles) tc5::commit(&bars[L::B_EK + (j + 1) % NK]);  // K(j+1) after its QKs
+      if (j + 1 < ntiles) tc5::commit(&bars[KEB + (j + 1) % NKT]);  // K(j+1) after its QKs
     }
     // every MMA this thread issued has completed before TMEM is released
     tc5::commit(&bars[L::B_FIN]);
@@ -451,37 +474,41 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     // ------------------------------------------------------------ fp8 widening
     const int cw = warp - 2;
     bool ok = true;
-    // Per key tile the K then the V codes are widened by warps 2 and 3, each
-    // taking half the rows.
-    // Lane (row r0, column group cc) widens 16 codes (one 16-byte load) into
-    // two 16-byte chunks of the swizzled fp16 tile; lanes of the upper column
-    // half store their two chunks in the opposite order, so that the 8 lanes
-    // of one row never hit the same bank group in one store.
+    // Per key tile the V codes are widened by warps 2 and 3, each taking
+    // half the rows (the K codes are the QK operand as they are).
+    // Lane (row r0, column group cc) widens 16 codes (one 16-byte load of
+    // the swizzled code rows) into two 16-byte chunks of the swizzled fp16
+    // tile; lanes of the upper column half store their two chunks in the
+    // opposite order, so that the 8 lanes of one row never hit the same bank
+    // group in one store.
     constexpr int LPR = D / 16, RPI = 32 / LPR;  // lanes per row, rows per pass
     constexpr int ROWS = BM / 2;  // rows each converter warp widens
     const int cc = lane % LPR, r0 = lane / LPR;
     const int row_base = cw * ROWS;
     const int swap = (cc >= LPR / 2) ? 1 : 0;
-    auto widen = [&](int kv, int j) -> bool {
-      const int ns = kv ? NV : NK, n8 = kv ? L::N8V : L::N8K;
-      const int s = j % ns, s8 = j % n8;
-      if (!warp_wait(&bars[(kv ? L::B_V8F : L::B_K8F) + s8], (j / n8) & 1, abort_flag, where))
-        return false;
+    // this lane's row r = row_base + RPI * it + r0 has swizzle phase
+    // r & 7 = r0 ^ ((RPI * it) & 7) for 128-byte rows (D = 128) and
+    // (r >> 1) & 3 = (r0 >> 1) & 3 for 64-byte rows (D = 64)
+    auto code_chunk = [&](int ph) {
+      return D == 128 ? (cc ^ r0 ^ (4 * ph)) : (cc ^ ((r0 >> 1) & 3));
+    };
+    auto widen = [&](int j) -> bool {
+      const int s = j % NV, s8 = j % L::N8V;
+      if (!warp_wait(&bars[L::B_V8F + s8], (j / L::N8V) & 1, abort_flag, where)) return false;
       // the fp16 stage is free once the MMAs of the tile that used it are done
-      if (j >= ns &&
-          !warp_wait(&bars[(kv ? L::B_EV : L::B_EK) + s], ((j / ns) - 1) & 1, abort_flag, where))
+      if (j >= NV && !warp_wait(&bars[L::B_EV + s], ((j / NV) - 1) & 1, abort_flag, where))
         return false;
-      const uint8_t *src = smem + L::OFF_STG + (kv ? L::N8K + s8 : s8) * L::TILE8;
-      uint8_t *dst = smem + (kv ? L::OFF_V : L::OFF_K) + s * L::TILE;
-      // this lane's row r = row_base + RPI * it + r0 has swizzle phase
-      // r & 7 = r0 ^ ((RPI * it) & 7); its two chunks' addresses are a
-      // lane-constant base plus a compile-time offset per pass
-      const uint8_t *ls = src + (row_base + r0) * D + cc * 16;
+      const uint8_t *src = smem + L::OFF_STG + (L::N8K + s8) * L::TILE8;
+      uint8_t *dst = smem + L::OFF_V + s * L::TILE;
+      // the lane's chunk addresses are a lane-constant base plus a
+      // compile-time offset per pass
+      const uint8_t *ls[2];
       uint8_t *ld = dst + (cc / 4) * L::REG + (row_base + r0) * 128;
       const int k0 = (2 * cc) % 8;
       uint8_t *pa[2], *pb[2];  // [phase 0 / 4]: first, second chunk
 #pragma unroll
       for (int ph = 0; ph < 2; ++ph) {
+        ls[ph] = src + (row_base + r0) * D + code_chunk(ph) * 16;
         pa[ph] = ld + ((k0 ^ r0 ^ (4 * ph)) * 16);
         pb[ph] = ld + (((k0 + 1) ^ r0 ^ (4 * ph)) * 16);
         if (swap) {  // store order flipped for the upper column half
@@ -493,7 +520,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
       for (int it = 0; it < ROWS / RPI; ++it) {
         const int ph = ((RPI * it) & 7) ? 1 : 0;
-        const uint4 u = *reinterpret_cast<const uint4 *>(ls + it * RPI * D);
+        const uint4 u = *reinterpret_cast<const uint4 *>(ls[ph] + it * RPI * D);
         const uint2 h0 = e4m3x4_to_h4(u.x), h1 = e4m3x4_to_h4(u.y);
         const uint2 h2 = e4m3x4_to_h4(u.z), h3 = e4m3x4_to_h4(u.w);
         // dims 16cc .. 16cc+7 and 16cc+8 .. 16cc+15 (swapped with the order)
@@ -503,11 +530,11 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
         *reinterpret_cast<uint4 *>(pb[ph] + it * RPI * 128) = swap ? c0 : c1;
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bars[(kv ? L::B_VF : L::B_KF) + s]);
-      mbar_arrive(&bars[(kv ? L::B_E8V : L::B_E8K) + s8]);  // staging area free again
+      mbar_arrive(&bars[L::B_VF + s]);
+      mbar_arrive(&bars[L::B_E8V + s8]);  // staging area free again
       return true;
     };
-    for (int j = 0; ok && j < ntiles; ++j) ok = widen(0, j) && widen(1, j);
+    for (int j = 0; ok && j < ntiles; ++j) ok = widen(j);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int x = warp >= 8 ? 1 : 0;
@@ -526,46 +553,64 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     if constexpr (QCONV) {
-      // This tile's bf16 queries become fp16 * 2^-e, e chosen from their
-      // largest magnitude (exact power-of-two scaling, inside fp16's range);
-      // 2^e joins the score scale.  The four warps exchange their maxima
-      // through an mbarrier (bounded waits: no barrier can strand a warp).
+      // This tile's queries become two E4M3 terms hi + lo of q * 2^-e, e
+      // chosen from their largest magnitude (largest |q| * 2^-e in
+      // [2^7, 2^8): both terms inside E4M3's range; exact power-of-two
+      // scaling), written over the tile as two K-major tiles of D-byte rows
+      // (hi, then lo) in the swizzled layout of the key codes; 2^e joins the
+      // score scale.  The four warps exchange their maxima through an
+      // mbarrier, which also tells every warp that the whole tile has been
+      // read before any of it is overwritten (bounded waits: no barrier can
+      // strand a warp).
+      constexpr int CH = L::TILE / 16 / 128;  // 16-byte chunks per thread
       int e = 0;
       ok = warp_wait(&bars[L::B_Q], 0, abort_flag, where);
-      uint4 *q4 = reinterpret_cast<uint4 *>(smem + L::OFF_Q + x * L::TILE);
+      uint8_t *qt8 = smem + L::OFF_Q + x * L::TILE;
+      const uint4 *q4 = reinterpret_cast<const uint4 *>(qt8);
       const int tid = (warp & 3) * 32 + lane;
+      uint4 qv[CH];
+      uint32_t am = 0;  // largest |q| (fp32 bit pattern)
       if (ok) {
-        uint32_t am = 0;  // per-halfword max of |bf16| bit patterns
-        for (int c = tid; c < L::TILE / 16; c += 128) {
-          const uint4 u = q4[c];
-          am = __vmaxu2(am, __vmaxu2(__vmaxu2(u.x & 0x7fff7fffu, u.y & 0x7fff7fffu),
-                                     __vmaxu2(u.z & 0x7fff7fffu, u.w & 0x7fff7fffu)));
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+          qv[i] = q4[tid + 128 * i];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = T::to_f2(word4(qv[i], k));
+            am = max(am, max(__float_as_uint(fabsf(f.x)), __float_as_uint(fabsf(f.y))));
+          }
         }
-        am = __reduce_max_sync(0xffffffffu, max(am & 0xffffu, am >> 16));
+        am = __reduce_max_sync(0xffffffffu, am);
         if (lane == 0) misc[8 + x * 4 + (warp & 3)] = am;
         mbar_arrive(&bars[L::B_QS + x]);
         ok = warp_wait(&bars[L::B_QS + x], 0, abort_flag, where);
       }
       if (ok) {
-        const uint32_t am = max(max(misc[8 + x * 4], misc[9 + x * 4]),
-                                max(misc[10 + x * 4], misc[11 + x * 4]));
-        const int E = static_cast<int>(am >> 7);  // bf16 exponent field of the largest |q|
-        // largest |q| * 2^-e in [2^14, 2^15): inside fp16's range, full precision
-        e = E == 0 ? 0 : min(64, max(-64, E - 141));
-        const unsigned long long mul2 = f2pack(__int_as_float((127 - e) << 23),
-                                               __int_as_float((127 - e) << 23));
-        for (int c = tid; c < L::TILE / 16; c += 128) {
-          const uint4 u = q4[c];
-          uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        am = max(max(misc[8 + x * 4], misc[9 + x * 4]), max(misc[10 + x * 4], misc[11 + x * 4]));
+        const int E = static_cast<int>(am >> 23);
+        e = E == 0 ? 0 : min(64, max(-64, E - 134));
+        const float mul = __int_as_float((127 - e) << 23);
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+          // chunk c of the 16-bit tile: 64-dim region, row, logical chunk
+          const int c = tid + 128 * i;
+          const int r = c / (L::REG / 16), R = (c % (L::REG / 16)) / 8;
+          const int d0 = 64 * r + 8 * ((c % 8) ^ (R & 7));  // its first of 8 dims
+          float v[8];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            float f0, f1;
-            f2unpack(fmul2(f2pack(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u)),
-                           mul2),
-                     f0, f1);
-            w[k] = FP16::from_f2(f0, f1);
+            const float2 f = T::to_f2(word4(qv[i], k));
+            v[2 * k] = f.x * mul;
+            v[2 * k + 1] = f.y * mul;
           }
-          q4[c] = make_uint4(w[0], w[1], w[2], w[3]);
+          uint32_t h0, l0, h1, l1;
+          split_e4m3x4(v[0], v[1], v[2], v[3], h0, l0);
+          split_e4m3x4(v[4], v[5], v[6], v[7], h1, l1);
+          // its 8 codes at byte d0 of row R of the D-byte swizzled rows
+          const int off = D == 128 ? R * 128 + ((((d0 >> 4) ^ (R & 7)) << 4) | (d0 & 8))
+                                   : R * 64 + ((((d0 >> 4) ^ ((R >> 1) & 3)) << 4) | (d0 & 8));
+          *reinterpret_cast<uint2 *>(qt8 + off) = make_uint2(h0, h1);
+          *reinterpret_cast<uint2 *>(qt8 + BM * D + off) = make_uint2(l0, l1);
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars[L::B_Q2 + x]);
@@ -836,8 +881,10 @@ cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, i
       return cudaErrorInvalidValue;
   }
   {
-    // 16-bit cache: 64-element swizzled boxes; fp8 cache: one plain box of
-    // the whole D-byte row per cache block (the widening warps swizzle)
+    // 16-bit cache: 64-element swizzled boxes; fp8 cache: one box of the
+    // whole D-byte row per cache block, swizzled by its row length (the key
+    // codes are the QK operand as they land; the widening warps read the
+    // value codes through the same swizzle)
     const cuuint64_t eb = static_cast<cuuint64_t>(g.elem_bytes);
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.D), static_cast<cuuint64_t>(g.KVH),
                                 static_cast<cuuint64_t>(g.num_blocks * g.BS), 2};
@@ -846,10 +893,10 @@ cudaError_t launch_prefill(void *out, const void *query, int64_t num_q_tokens, i
                                    static_cast<cuuint64_t>(g.num_blocks * g.block_elems) * eb};
     const cuuint32_t box[4] = {g.fp8 ? static_cast<cuuint32_t>(g.D) : 64u, 1,
                                static_cast<cuuint32_t>(g.BS), 1};
+    const CUtensorMapSwizzle swz = !g.fp8 || g.D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                         : CU_TENSOR_MAP_SWIZZLE_64B;
     if (encode_tensor_map(&kvmap, g.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : dt, 4,
-                          const_cast<void *>(kv_cache), dims, strides, box,
-                          g.fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B) !=
-        CUDA_SUCCESS)
+                          const_cast<void *>(kv_cache), dims, strides, box, swz) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   if (g.D == 128)

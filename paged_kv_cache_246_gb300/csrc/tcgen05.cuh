@@ -90,6 +90,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same for a K-major operand with the 64-byte swizzle (layout type 4):
+// 8-row atoms of 64-byte rows.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (sdesc_sw128(saddr, lbo, sbo) & ~(7ull << 61)) | (4ull << 61);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulate, A/B both bf16
 // (ab = 1) or both fp16 (ab = 0), A K-major, B K-major (b_mn = 0) or
 // MN-major (b_mn = 1), shape M x N.
@@ -105,6 +111,17 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], 8-bit operands (kind::f8f6f4; with the
+// operand format fields 0 the descriptor of idesc_f16(0, ...) reads E4M3).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
