@@ -632,10 +632,22 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
       tc5::tmem_ld_wait();
       const int kv0 = kv_start + j * BN;
       const bool full = (kv0 + BN - 1 <= hi) && (kv0 >= lo);
-      if (!full) {
+      if (__any_sync(0xffffffffu, !full)) {  // every lane enters: the votes below span the warp
+        // per 32-key chunk the warp's rows agree that it is wholly visible
+        // (nothing to do), wholly hidden (all -inf) or needs the per-key mask
+        // (a row whose whole tile is visible finds every chunk visible)
+        const int vlo = lo - kv0, vhi = hi - kv0;  // visible offsets [vlo, vhi]
 #pragma unroll
-        for (int e = 0; e < BN; ++e)
-          if (kv0 + e > hi || kv0 + e < lo) raw[e] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < BN / 32; ++c) {
+          const bool some_hidden = !__all_sync(0xffffffffu, 32 * c >= vlo && 32 * c + 31 <= vhi);
+          const bool all_hidden = __all_sync(0xffffffffu, 32 * c > vhi || 32 * c + 31 < vlo);
+          const int mlo = all_hidden ? BN : vlo, mhi = all_hidden ? -1 : vhi;
+          if (some_hidden) {
+#pragma unroll
+            for (int e = 32 * c; e < 32 * c + 32; ++e)
+              if (e > mhi || e < mlo) raw[e] = __float_as_uint(-INFINITY);
+          }
+        }
       }
       const float unit = ALIBI ? 1.f : sl2;  // log2 units per unit of m
       // p = 2^(x - mu) over the tile, written to TMEM as P; returns the row
