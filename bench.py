@@ -53,6 +53,7 @@ METRIC = ("decode tokens/s and HBM GB/s (%peak); prefill TFLOP/s (%bf16 peak), 1
 # committed ncu summary (kernel source, file) per workload: DRAM traffic per launch
 PROFILE_OF = {2: ("decode.cu", "decode_kernel_llama3_8b_decode.md"),
               3: ("prefill.cu", "prefill_tc_kernel_varlen_prefill.md"),
+              5: ("decode.cu", "decode_kernel_swa_long_decode.md"),
               7: ("decode.cu", "decode_kernel_llama3_8b_decode_fp8.md"),
               8: ("prefill.cu", "prefill_tc_kernel_varlen_prefill_fp8.md"),
               9: ("decode.cu", "decode_kernel_llama3_8b_spec_decode.md")}
