@@ -266,11 +266,15 @@ __device__ __forceinline__ uint32_t swz(int tok, int chunk) {
 }
 
 // HALF: the CTA's rows are 8 or fewer (a single-token decode of up to 8
-// heads per KV head): rows 8..15 of the m16 tile are not kept at all.  (3
-// CTAs per SM in every variant: capping the fp8 half-tile variant at 128
-// registers for a 4th spills, and measured 28% slower.)
+// heads per KV head): rows 8..15 of the m16 tile are not kept at all.
+// CTAs per SM: the fp8 half-tile variant (34 KB of shared memory) runs 4
+// within 128 registers (a few spilled bytes; 0.745 vs 0.711 of HBM with 3);
+// the 16-bit variants are held to 3 by their shared memory (71 KB), the fp8
+// 16-row variant by its registers.
+template <bool KV8, bool HALF>
+constexpr int kDecodeCtasPerSm = (KV8 && HALF) ? 4 : 3;
 template <class T, int D, bool KV8, bool HALF>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm<KV8, HALF>)
 decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   using L = Lay<D, KV8>;
   using MT = std::conditional_t<KV8, FP16, T>;  // MMA operand type (and P)
