@@ -394,15 +394,26 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
   // ---- Q fragments (A operand, row-major 16 x 16 per k-step) ---------------
   uint32_t qa[KS][4];
   float sl2 = a.scale_log2;
+  // fp8 cache, four rows or fewer (a single-token decode of up to 4 heads per
+  // KV head): rows 4..7 of the m16 tile carry the lo query terms of rows
+  // 0..3, so one product per k-step gives both terms (summed across lanes).
+  const bool fold = KV8 && HALF && a.rows <= 4;
   if constexpr (KV8) {
     // E4M3 terms: qa[s] = hi, qa[KS8 + s] = lo of k-step s (32 positions):
     // positions 4tq .. 4tq+3 -> dims tq * D/4 + 8s + 0..3, positions
     // 16 + 4tq .. -> dims tq * D/4 + 8s + 4..7 (eight consecutive elements)
     constexpr int KS8 = D / 32;
+    const int srow = fold ? (g & 3) : g;  // the row whose query this lane's row 0 holds
+    const bool lo_lane = fold && g >= 4;
+    const bool src_valid = fold ? rg * kRows + srow < a.rows : valid[0];
+    const int64_t src_orow = fold ? static_cast<int64_t>(b * q + (rg * kRows + srow) / QPK) * H +
+                                        kvh * QPK + (rg * kRows + srow) % QPK
+                                  : orow[0];
     auto qchunk = [&](int x, int s) -> uint4 {  // this lane's dims tq * D/4 + 8s .. + 7 of row x
-      const uint4 *qp = reinterpret_cast<const uint4 *>(a.query) +
-                        (static_cast<int64_t>(orow[x]) * D + tq * (D / 4)) / 8;
-      return valid[x] ? __ldg(qp + s) : make_uint4(0u, 0u, 0u, 0u);
+      const int64_t r = x == 0 ? src_orow : orow[x];
+      const bool v = x == 0 ? src_valid : valid[x];
+      const uint4 *qp = reinterpret_cast<const uint4 *>(a.query) + (r * D + tq * (D / 4)) / 8;
+      return v ? __ldg(qp + s) : make_uint4(0u, 0u, 0u, 0u);
     };
     uint32_t am = 0;  // largest |q| bit pattern (fp32)
 #pragma unroll
@@ -441,6 +452,10 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
         }
         split_e4m3x4(v[0], v[1], v[2], v[3], qa[s][x], qa[KS8 + s][x]);
         split_e4m3x4(v[4], v[5], v[6], v[7], qa[s][2 + x], qa[KS8 + s][2 + x]);
+        if (x == 0 && lo_lane) {  // rows 4..7 hold the lo terms
+          qa[s][0] = qa[KS8 + s][0];
+          qa[s][2] = qa[KS8 + s][2];
+        }
       }
   } else {
     const uint32_t *q0 = reinterpret_cast<const uint32_t *>(a.query) +
@@ -528,14 +543,22 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
           const uint32_t b0 = word_of(kk[n][(2 * s) / 4], (2 * s) % 4);
           const uint32_t b1 = word_of(kk[n][(2 * s + 1) / 4], (2 * s + 1) % 4);
           if constexpr (HALF) {
-            float d2[2] = {sc[n][0], sc[n][1]};
-            mma16832_e4m3_top(d2, qa[s][0], qa[s][2], b0, b1);
-            sc[n][0] = d2[0];
-            sc[n][1] = d2[1];
-            float e2[2] = {sc2[n][0], sc2[n][1]};
-            mma16832_e4m3_top(e2, qa[KS8 + s][0], qa[KS8 + s][2], b0, b1);
-            sc2[n][0] = e2[0];
-            sc2[n][1] = e2[1];
+            if (fold) {  // both terms in one product: even / odd k-steps apart
+              float(&acc)[4] = (s & 1) ? sc2[n] : sc[n];
+              float d2[2] = {acc[0], acc[1]};
+              mma16832_e4m3_top(d2, qa[s][0], qa[s][2], b0, b1);
+              acc[0] = d2[0];
+              acc[1] = d2[1];
+            } else {
+              float d2[2] = {sc[n][0], sc[n][1]};
+              mma16832_e4m3_top(d2, qa[s][0], qa[s][2], b0, b1);
+              sc[n][0] = d2[0];
+              sc[n][1] = d2[1];
+              float e2[2] = {sc2[n][0], sc2[n][1]};
+              mma16832_e4m3_top(e2, qa[KS8 + s][0], qa[KS8 + s][2], b0, b1);
+              sc2[n][0] = e2[0];
+              sc2[n][1] = e2[1];
+            }
           } else {
             mma16832_e4m3(sc[n], qa[s], b0, b1);
             mma16832_e4m3(sc2[n], qa[KS8 + s], b0, b1);
@@ -556,6 +579,14 @@ decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmap) {
     for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int c = 0; c < 2 * NR; ++c) sc[n][c] += sc2[n][c];
+    if constexpr (KV8 && HALF) {
+      if (fold) {  // row g + 4 holds row g's lo-term product (lane + 16)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) sc[n][c] += __shfl_xor_sync(0xffffffffu, sc[n][c], 16);
+      }
+    }
     // A unit inside [lo_max, pos_min] needs no mask (rows past a.rows hold
     // zero queries; their results are never stored).
     const bool interior = j0 >= lo_max && j0 + (kUnit - 1) * RW <= pos_min;

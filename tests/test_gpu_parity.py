@@ -516,6 +516,10 @@ FP8_DECODE_CASES = {
     "block32_alibi": lambda: fp8(small(95, bs=32, alibi=True, seq_lens=rand_lens(25, 6, 1, 900))),
     "window": lambda: fp8(small(96, window=100, seq_lens=rand_lens(26, 8, 1, 900))),
     "long_single": lambda: fp8(small(97, H=32, KVH=8, seq_lens=[5000])),
+    # four rows or fewer per KV head: the lo query terms ride in rows 4..7
+    "huge_queries_qpk4": lambda: scaled_q(fp8(small(98, seq_lens=rand_lens(27, 6, 1, 700))), 3e4),
+    "tiny_queries_qpk2": lambda: scaled_q(fp8(small(99, H=4, KVH=2, seq_lens=rand_lens(28, 6, 1, 700))),
+                                          1e-6),
 }
 
 
