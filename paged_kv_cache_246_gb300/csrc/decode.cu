@@ -946,11 +946,13 @@ DecodePlan plan_decode(int num_seqs, int query_len, int max_seq_len, const Geome
   const int units = (eff + U - 1) / U + 1;  // a window start can straddle a unit
   p.row_groups = (query_len * g.QPK + dec::kRows - 1) / dec::kRows;
   const int64_t items = static_cast<int64_t>(num_seqs) * g.KVH * p.row_groups;
-  // Splits of up to 128 units (2048 keys): every split writes fp32 partials of
+  // Splits of up to 256 units (4096 keys): every split writes fp32 partials of
   // all its q * QPK rows, so short splits cost real HBM traffic; shrink them
   // only while the grid would leave SMs idle.  (Measured on 128 sequences x 4
-  // tokens, 512..4096 keys: 0.71 / 0.82 / 0.85 of HBM with 32 / 64 / 128.)
-  int split_units = 128;
+  // tokens, 512..4096 keys: 0.71 / 0.82 / 0.85 / 0.876 of HBM with 32 / 64 /
+  // 128 / 256; 256 sequences x 1 token: 0.970 / 0.979 with 128 / 256, where
+  // 256 leaves one split per sequence and no combine pass.)
+  int split_units = 256;
   while (split_units > 8 && items * ((units + split_units - 1) / split_units) < 8LL * sms)
     split_units /= 2;
   if (units <= 2 * split_units) split_units = units;  // short: one split

@@ -126,7 +126,7 @@ def test_multi_decode_validation(lib):
     assert call(fp8) == B.PKV_ERR_INVALID               # supported: null pointers
     assert call(_p(num_heads=24, num_kv_heads=8)) == B.PKV_ERR_INVALID   # any group size
     assert B.paged_attn_decode_multi_workspace_size(4, 4, 64, p) == 0   # one split
-    n = B.paged_attn_decode_multi_workspace_size(128, 4, 4096, p)
+    n = B.paged_attn_decode_multi_workspace_size(128, 4, 16384, p)
     assert n > 0 and n % 256 == 0
     assert B.paged_attn_decode_multi_workspace_size(128, 0, 4096, p) == 0
 
@@ -135,7 +135,7 @@ def test_workspace_size_is_host_only(lib):
     p = _p()
     assert B.paged_attn_decode_workspace_size(0, 100, p) == 0
     assert B.paged_attn_decode_workspace_size(4, 64, p) == 0            # one split
-    n = B.paged_attn_decode_workspace_size(256, 4096, p)
+    n = B.paged_attn_decode_workspace_size(256, 16384, p)
     assert n > 0 and n % 256 == 0
 
 
