@@ -833,19 +833,31 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const Args a) {
   for (int e = 0; e < EPL; ++e) num[e] = 0.f;
   if (M != -INFINITY) {
     const float *po = a.part_o + hh * a.max_splits * D + lane * EPL;
-    for (int s = 0; s < sp.nsplit; ++s) {
-      const float w = fast_exp2(ml[2 * s] - M) * ml[2 * s + 1];
-      float v[EPL];
-      if constexpr (EPL == 4) {
-        const float4 t = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(s) * D);
-        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-      } else {
-        const float2 t = *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(s) * D);
-        v[0] = t.x; v[1] = t.y;
+    // four splits' loads in flight at a time (the partials come from L2)
+    constexpr int G = 4;
+    for (int s0 = 0; s0 < sp.nsplit; s0 += G) {
+      float mm[G], ll[G], v[G][EPL];
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const int s = min(s0 + i, sp.nsplit - 1);
+        mm[i] = ml[2 * s];
+        ll[i] = ml[2 * s + 1];
+        if constexpr (EPL == 4) {
+          const float4 t = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(s) * D);
+          v[i][0] = t.x; v[i][1] = t.y; v[i][2] = t.z; v[i][3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(s) * D);
+          v[i][0] = t.x; v[i][1] = t.y;
+        }
       }
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) num[e] = fmaf(w, v[e], num[e]);
-      den += w;
+      for (int i = 0; i < G; ++i) {
+        if (s0 + i >= sp.nsplit) break;
+        const float w = fast_exp2(mm[i] - M) * ll[i];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) num[e] = fmaf(w, v[i][e], num[e]);
+        den += w;
+      }
     }
   }
   float val[EPL];
