@@ -269,8 +269,9 @@ def step_io_bytes(st: Step):
 def time_block_moves(st: Step, w: W.Workload, B, args, hbm: float):
     """kv_copy_blocks and kv_swap_blocks of the workload, timed apart from the
     step with CUDA events: copy against the HBM roofline (read + write
-    bytes), swap out / in against a same-size contiguous pinned copy in the
-    same direction (the host link), measured here."""
+    bytes) and against a same-size contiguous device copy measured here
+    (the ceiling for a move this short), swap out / in against a same-size
+    contiguous pinned copy in the same direction (the host link)."""
     stream = torch.cuda.current_stream()
     block_bytes = 2 * w.kv_cache.shape[2] * w.kv_cache.element_size()   # K and V of one block
     n_copy, n_swap = int(w.copy_pairs.shape[0]), int(w.swap_pairs.shape[0])
@@ -280,6 +281,8 @@ def time_block_moves(st: Step, w: W.Workload, B, args, hbm: float):
     in_pairs = w.swap_pairs[:, [1, 0]].contiguous()
     flat_dev = torch.empty(n_swap * block_bytes, dtype=torch.uint8, device=st.dev)
     flat_host = torch.empty(n_swap * block_bytes, dtype=torch.uint8).pin_memory()
+    flat_a = torch.ones(n_copy * block_bytes, dtype=torch.uint8, device=st.dev)
+    flat_b = torch.empty_like(flat_a)
 
     def timed(fn, reps):
         for _ in range(3):
@@ -296,16 +299,20 @@ def time_block_moves(st: Step, w: W.Workload, B, args, hbm: float):
 
     reps = max(5, min(args.steps, 50))
     copy_ms = timed(lambda: B.kv_copy_blocks([st.cache], pairs_dev, st.p), reps)
+    dev_copy_ms = timed(lambda: flat_b.copy_(flat_a), reps)
     out_ms = timed(lambda: B.kv_swap_blocks(st.cache, host, out_pairs, st.p), reps)
     in_ms = timed(lambda: B.kv_swap_blocks(host, st.cache, in_pairs, st.p), reps)
     link_out_ms = timed(lambda: flat_host.copy_(flat_dev, non_blocking=True), reps)
     link_in_ms = timed(lambda: flat_dev.copy_(flat_host, non_blocking=True), reps)
     B.check_device_error("block moves")
     copy_gbs = 2 * n_copy * block_bytes / (copy_ms * 1e-3) / 1e9
+    dev_copy_gbs = 2 * n_copy * block_bytes / (dev_copy_ms * 1e-3) / 1e9
     swap_bytes = n_swap * block_bytes
     gbs = lambda ms: swap_bytes / (ms * 1e-3) / 1e9
     return {"copy_blocks": {"pairs": n_copy, "ms": copy_ms, "gbs": copy_gbs,
-                            "frac_of_hbm": copy_gbs / hbm},
+                            "frac_of_hbm": copy_gbs / hbm,
+                            "same_size_copy_gbs": dev_copy_gbs,
+                            "frac_of_same_size_copy": copy_gbs / dev_copy_gbs},
             "swap_out": {"blocks": n_swap, "ms": out_ms, "gbs": gbs(out_ms),
                          "link_gbs": gbs(link_out_ms), "frac_of_link": link_out_ms / out_ms},
             "swap_in": {"blocks": n_swap, "ms": in_ms, "gbs": gbs(in_ms),
