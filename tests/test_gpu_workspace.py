@@ -32,7 +32,7 @@ def test_one_workspace_across_sizes_and_contents(fill):
     # batch of 4-token decodes with another split plan, on one workspace
     # whose bytes start as `fill` (0xFF: every partial a NaN)
     wa = _workload(61, _lens(61, 6, 3000, 9000))
-    wb = _workload(62, _lens(62, 40, 100, 1500), multi=4)
+    wb = _workload(62, _lens(62, 8, 100, 1500), multi=4)
     ra, rb = CudaRun(wa), CudaRun(wb)
     ra.write()
     rb.write()
