@@ -3,7 +3,8 @@
 Headline workload: the Llama-3-8B-shaped decode step (bf16, 256 sequences,
 32 query / 8 KV heads, head 128, block 16, seq_len ~ U[512, 4096], pool =
 needed blocks + 10%, tables randomly permuted).  One step = kv_cache_write of
-the 256 new tokens, then paged_attn_decode (split-KV pass + combine).
+the 256 new tokens, then paged_attn_decode (split-KV pass, and the combine
+when a sequence is split).
 
 Beside it the default run measures, each with its own warm-up, timed steps
 and clock record, and reports in the line's ``workloads`` object:
@@ -53,6 +54,7 @@ METRIC = ("decode tokens/s and HBM GB/s (%peak); prefill TFLOP/s (%bf16 peak), 1
 # committed ncu summary (kernel source, file) per workload: DRAM traffic per launch
 PROFILE_OF = {2: ("decode.cu", "decode_kernel_llama3_8b_decode.md"),
               3: ("prefill.cu", "prefill_tc_kernel_varlen_prefill.md"),
+              4: ("decode.cu", "decode_kernel_mixed_chunked_alibi.md"),
               5: ("decode.cu", "decode_kernel_swa_long_decode.md"),
               7: ("decode.cu", "decode_kernel_llama3_8b_decode_fp8.md"),
               8: ("prefill.cu", "prefill_tc_kernel_varlen_prefill_fp8.md"),
@@ -572,9 +574,9 @@ def measure(args, cfg: int, world: int, rank: int, local: int, B, full: bool) ->
     decode = prefill = None
     if st.has_decode:
         gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
-        decode = {"kernel": ("paged_attn_decode_multi (tensor-core split pass + combine)"
+        decode = {"kernel": ("paged_attn_decode_multi (split pass, + combine when split)"
                              if w.multi_query_len else
-                             "paged_attn_decode (split-KV pass + combine)"),
+                             "paged_attn_decode (split-KV pass, + combine when split)"),
                   "gbs": gbs, "frac_of_hbm": gbs / hbm, "avg_launch_ms": dec_ms,
                   "algorithmic_bytes_per_launch": dec_bytes}
     if st.has_prefill:
@@ -589,8 +591,12 @@ def measure(args, cfg: int, world: int, rank: int, local: int, B, full: bool) ->
     else:
         value, unit = flops * world / (ms_step * 1e-3) / 1e12, "TFLOP/s"
         e2e_value = flops * world / (e2e["ms_per_step"] * 1e-3) / 1e12 if e2e else None
-    # the roofline object describes the call that takes most of the step
-    if decode and (not prefill or dec_ms >= pre_ms):
+    # the roofline object describes the call that takes most of the step; the
+    # profiled traffic belongs to it only if the summary is of that kernel
+    decode_roof = bool(decode and (not prefill or dec_ms >= pre_ms))
+    if traffic is not None and PROFILE_OF[cfg][0].startswith("decode") != decode_roof:
+        traffic = None
+    if decode_roof:
         roof = {"bound": "hbm", "achieved": decode["gbs"], "peak": hbm, "unit": "GB/s",
                 "frac": decode["frac_of_hbm"], "traffic": traffic, "kernel": decode["kernel"],
                 "peak_kind": peak_kind, "algorithmic_bytes_per_launch": dec_bytes,
@@ -769,7 +775,7 @@ def run_dcp_share(args, world, rank, local):
                        "parallelism": "dcp2 rank share on 1 GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": None,
-                         "kernel": "paged_attn_decode_dcp_partial (split pass + combine)",
+                         "kernel": "paged_attn_decode_dcp_partial (split pass, + combine when split)",
                          "peak_kind": peak_kind, "algorithmic_bytes_per_launch": share_bytes,
                          "avg_launch_ms": share_ms},
             "merge": {"ms": merge_ms, "gbs": merge_bytes / (merge_ms * 1e-3) / 1e9},
