@@ -151,3 +151,22 @@ def test_copy_and_swap_validation(lib):
     pairs = (ctypes.c_int64 * 2)(9, 0)        # source out of range
     assert lib.kv_swap_blocks(fake, 8, fake, 8, pairs, 1, ctypes.byref(p),
                               nul) == B.PKV_ERR_INVALID
+
+
+def test_split_plan_at_the_bench_shapes(lib):
+    """The split planner (host only; 152 SMs without a device): splits of up
+    to 4096 keys, halved while the grid would hold fewer than 8 CTAs per SM.
+    The workspace is rows x splits x (head_size + 2) fp32 values, each part
+    rounded up to 256 bytes."""
+    p, win = _p(), _p(sliding_window=4096)
+    # 2048 (sequence, KV head) items fill the GPU with one split each
+    assert B.paged_attn_decode_workspace_size(256, 4096, p) == 0
+    assert B.paged_attn_decode_multi_workspace_size(128, 4, 4096, p) == 0
+    # 512 items: 4096-key splits are halved to 2048; 257 units (a window
+    # start can straddle one) make three splits
+    three = 64 * 32 * 3
+    assert B.paged_attn_decode_workspace_size(64, 4096, p) == three * 128 * 4 + three * 2 * 4
+    assert B.paged_attn_decode_workspace_size(64, 32768, win) == three * 128 * 4 + three * 2 * 4
+    # 32 items over 65536 keys: halved down to 1024-key splits, 65 of them
+    many = 4 * 32 * 65
+    assert B.paged_attn_decode_workspace_size(4, 65536, p) == many * 128 * 4 + many * 2 * 4
