@@ -164,9 +164,11 @@ pkv_status kv_cache_write(const void *key, const void *value,
  * PagedAttention.forward_decode; cpu_attn TorchSDPABackendImpl.forward ->
  * forward_decode).  The new token was already written, so seq_lens counts it
  * and the query sits at position seq_len - 1 (xformers.py XFormersMetadata
- * note on context_len).  Split-KV: a sequence's keys are cut into pieces
- * processed in parallel whose partial softmax states are merged by a second
- * kernel (needs `workspace`).
+ * note on context_len).  Split-KV: when the batch alone would leave SMs idle,
+ * or a sequence is longer than 4096 keys, a sequence's keys are cut into
+ * pieces processed in parallel whose partial softmax states are merged by a
+ * second kernel (needs `workspace`; paged_attn_decode_workspace_size returns
+ * 0 when no sequence is split).
  *
  *   out            [num_seqs][num_heads * head_size] elements
  *   query          [num_seqs][num_heads * head_size] elements
